@@ -1,0 +1,87 @@
+"""CPU tests: the fp64 oracle against its pins, and planted mistakes in copies
+of the oracle that the pins must catch."""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import oracle_pins as pins
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_meets_pin(pin):
+    pin(oracle.attn_fwd)
+
+
+# Each planted mistake is a one-line edit of the oracle's C source (built into
+# a temporary library on the CPU); at least one pin must reject it.
+MUTANTS = {
+    "dropped_scale": ("s[j] = job->scale * dot;", "s[j] = dot;"),
+    "causal_excludes_diagonal": ("job->causal ? i + 1 : N", "job->causal ? i : N"),
+    "exp_sign_flipped": ("exp(s[j] - m)", "exp(m - s[j])"),
+    "lse_log2": ("m + log(l)", "m + log2(l)"),
+    "lse_without_max": ("job->lse[out_idx] = m + log(l);", "job->lse[out_idx] = log(l);"),
+    "no_normalisation": ("oi[c] /= l;", "oi[c] /= 1.0;"),
+    "values_reversed": ("const double *vj = vh + j * d;",
+                        "const double *vj = vh + (n_keys - 1 - j) * d;"),
+    "max_not_subtracted_in_exp": ("exp(s[j] - m)", "exp(s[j])"),
+    "query_of_wrong_row": ("const double *qi = job->q + grow * d;",
+                           "const double *qi = job->q + (head * N) * d;"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, mutant_dir):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, "mutation anchor vanished: %r" % old
+    c_path = os.path.join(mutant_dir, name + ".c")
+    so_path = os.path.join(mutant_dir, name + ".so")
+    with open(c_path, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", so_path,
+                    c_path, "-lm"], check=True)
+    fn = oracle.bind(so_path)
+    failed = []
+    with np.errstate(all="ignore"):
+        for pin in pins.ALL_PINS:
+            try:
+                pin(fn)
+            except AssertionError:
+                failed.append(pin.__name__)
+    assert failed, "planted mistake %s passed every pin" % name
+
+
+def test_oracle_rejects_bad_arguments():
+    q = torch.zeros(1, 1, 4, 2, dtype=torch.float64)
+    with pytest.raises(RuntimeError):
+        oracle.attn_fwd(q, q, q, 1.0, False, rows=[4])  # row id out of range
+    with pytest.raises(RuntimeError):
+        oracle.attn_fwd(q, q, q, 1.0, False, rows=[-1])
+    with pytest.raises(ValueError):
+        oracle.attn_fwd(q, q[:, :, :3], q, 1.0, False)
+
+
+def test_oracle_empty_inputs():
+    q = torch.zeros(1, 1, 0, 8, dtype=torch.float64)
+    o, lse = oracle.attn_fwd(q, q, q, 1.0, True)
+    assert o.shape == (0, 8) and lse.shape == (0,)
+    q = torch.zeros(0, 3, 5, 8, dtype=torch.float64)
+    o, lse = oracle.attn_fwd(q, q, q, 1.0, False)
+    assert o.shape == (0, 8)
+
+
+def test_oracle_threads_do_not_change_results():
+    g = torch.Generator().manual_seed(5)
+    q, k, v = (torch.randn(2, 2, 70, 8, generator=g, dtype=torch.float64) for _ in range(3))
+    o1, l1 = oracle.attn_fwd(q, k, v, 0.3, True, threads=1)
+    o7, l7 = oracle.attn_fwd(q, k, v, 0.3, True, threads=7)
+    assert np.array_equal(o1, o7) and np.array_equal(l1, l7)

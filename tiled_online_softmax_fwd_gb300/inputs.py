@@ -1,0 +1,111 @@
+"""Seeded synthetic inputs for the attention forward pass.
+
+This module only draws random numbers and names workloads; it holds none of
+the attention arithmetic.  The CUDA path (through ``bench.py`` and the tests)
+and the fp64 oracle (through the tests) both take their inputs from here.
+
+Recipe (the pages use no dataset; the shapes are the ones the pages' kernels
+are written for -- [B, H, N, d] per-head contiguous rows, head dims 64/128,
+sequence lengths from a few hundred to 64K):
+
+  g = torch.Generator("cpu").manual_seed(seed)
+  q = randn(B,H,N,d, generator=g) * sigma_qk   (float32, then RNE to bf16)
+  k = randn(B,H,N,d, generator=g) * sigma_qk
+  v = randn(B,H,N,d, generator=g) * 1.0
+  sampled rows (when asked): continuing the same generator, for each head in
+  row-major (b, h) order, randperm(N, generator=g)[:rows_per_head], sorted.
+"""
+from __future__ import annotations
+
+import dataclasses
+import hashlib
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    sigma_qk: float = 1.0
+    rows_per_head: int | None = None  # oracle checks only these rows (None: all)
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale 1/sqrt(d), as the fp32 value the kernel receives."""
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    @property
+    def flops(self) -> float:
+        """4*B*H*N^2*d, halved for the causal mask."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    @property
+    def io_bytes(self) -> int:
+        """Bytes of Q, K, V read and O written (bf16) plus LSE written (fp32)."""
+        n = self.B * self.H * self.N
+        return 4 * n * self.d * 2 + n * 4
+
+    def describe(self) -> dict:
+        return {"B": self.B, "H": self.H, "N": self.N, "d": self.d,
+                "causal": self.causal, "seed": self.seed, "sigma_qk": self.sigma_qk}
+
+
+# The five workloads the method is exercised on (shape / mask / seed / logit scale).
+WORKLOADS = {
+    "B1_H1_N256_d64": Workload("B1_H1_N256_d64", 1, 1, 256, 64, False, 0),
+    "B1_H1_N4096_d64": Workload("B1_H1_N4096_d64", 1, 1, 4096, 64, False, 1),
+    "B4_H16_N4096_d128_causal": Workload("B4_H16_N4096_d128_causal", 4, 16, 4096, 128, True, 2,
+                                         rows_per_head=512),
+    "B1_H32_N16384_d128_causal_sigma3": Workload("B1_H32_N16384_d128_causal_sigma3", 1, 32, 16384,
+                                                 128, True, 3, sigma_qk=3.0, rows_per_head=1024),
+    "B2_H8_N65536_d64": Workload("B2_H8_N65536_d64", 2, 8, 65536, 64, False, 4,
+                                 rows_per_head=1024),
+}
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+def make_qkv(B: int, H: int, N: int, d: int, seed: int, sigma_qk: float = 1.0,
+             generator: torch.Generator | None = None):
+    """Return bf16 CPU tensors q, k, v of shape [B, H, N, d] (contiguous)."""
+    g = generator if generator is not None else torch.Generator("cpu").manual_seed(seed)
+    shape = (B, H, N, d)
+    q = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma_qk).to(torch.bfloat16)
+    k = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma_qk).to(torch.bfloat16)
+    v = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return q.contiguous(), k.contiguous(), v.contiguous()
+
+
+def sample_rows(B: int, H: int, N: int, per_head: int, generator: torch.Generator):
+    """Global row ids (b*H + h)*N + i: ``per_head`` distinct rows of every head."""
+    out = []
+    per = min(per_head, N)
+    for bh in range(B * H):
+        idx = torch.randperm(N, generator=generator)[:per].sort().values
+        out.append(idx.to(torch.int64) + bh * N)
+    return torch.cat(out) if out else torch.zeros(0, dtype=torch.int64)
+
+
+def make_workload(w: Workload):
+    """q, k, v (bf16, CPU) and the checked row ids (None when all rows are checked)."""
+    g = torch.Generator("cpu").manual_seed(w.seed)
+    q, k, v = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, generator=g)
+    rows = None
+    if w.rows_per_head is not None:
+        rows = sample_rows(w.B, w.H, w.N, w.rows_per_head, g)
+    return q, k, v, rows
+
+
+def digest(*tensors) -> str:
+    """SHA-256 over the raw bytes of the given CPU tensors (first 16 hex chars)."""
+    h = hashlib.sha256()
+    for t in tensors:
+        h.update(t.contiguous().view(torch.uint8).numpy().tobytes())
+    return h.hexdigest()[:16]
