@@ -1,0 +1,359 @@
+#!/usr/bin/env python3
+"""Benchmark of libfattn attn_fwd: attention forward TFLOP/s (bf16, 1x GB300)
+and fraction of the dense BF16 tensor-core peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one attn_fwd call over the whole workload (B*H*N query rows,
+inputs resident in HBM).  FLOPs = 4*B*H*N^2*d, halved under the causal mask.
+The default workload is B=1, H=32, N=16384, d=128, causal, Q/K ~ N(0, 3^2):
+its inputs (402 MB) exceed the 126 MB L2, so no flush is needed between
+steps; smaller workloads flush L2 before every step (outside the timed
+events) and are timed step by step.
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs the same
+workload on its own GPU (independent replicas, weak scaling); the time is the
+maximum over ranks and rank 0 prints.  ``--impl reference`` times the fp64
+CPU oracle instead (rank 0 only), each step one seeded query row per head.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import glob
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tiled_online_softmax_fwd_gb300.inputs import WORKLOADS, digest, make_workload  # noqa: E402
+
+DEFAULT_WORKLOAD = "B1_H32_N16384_d128_causal_sigma3"
+METRIC = "attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAK_TFLOPS = 1900.0
+KERNEL_SOURCES = ["tiled_online_softmax_fwd_gb300/csrc/fattn_fwd_sm103.cu",
+                  "tiled_online_softmax_fwd_gb300/csrc/ptx_sm103.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), "measured burst cuBLAS bf16 (MEASURED_PEAKS.json)"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, "fallback 1.9 PFLOP/s bf16 (no MEASURED_PEAKS.json)"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary of this kernel source
+    and workload (null when none matches the current source)."""
+    want = kernel_source_hash()
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        fields = {}
+        for line in open(path):
+            if line.startswith("bench-key "):
+                k, _, v = line[len("bench-key "):].strip().partition("=")
+                fields[k.strip()] = v.strip()
+        if fields.get("workload") == workload and fields.get("kernel_source") == want:
+            try:
+                return int(float(fields["dram_bytes_per_launch"])), os.path.basename(path)
+            except (KeyError, ValueError):
+                pass
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (read-only)."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_rows_for_steps(w, rows_all, steps):
+    """One seeded row per head for each step (cycling through the sample)."""
+    per_head = rows_all.view(w.B * w.H, -1)
+    cols = per_head.shape[1]
+    return [per_head[:, s % cols].clone() for s in range(steps)]
+
+
+def rows_flops(w, rows) -> float:
+    i = rows % w.N
+    keys = (i + 1).double() if w.causal else torch.full_like(i, w.N).double()
+    return float((4.0 * keys * w.d).sum())
+
+
+def cpu_baseline(w, q, k, v, rows_all, budget_s=15.0):
+    """The oracle as it stands on this host's cores, over a bounded sample of
+    the workload's rows; returns the same metric (TFLOP/s)."""
+    import oracle
+    threads = oracle.default_threads()
+    qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+    per_head = rows_all.view(w.B * w.H, -1)
+    total_rows, total_flops, t_total, used = 0, 0.0, 0.0, 0
+    col = 0
+    while t_total < budget_s and col < per_head.shape[1]:
+        take = per_head[:, col:col + 8].reshape(-1)
+        col += 8
+        t0 = time.perf_counter()
+        oracle.attn_fwd(qd, kd, vd, w.scale, w.causal, rows=take.numpy(), threads=threads)
+        t_total += time.perf_counter() - t0
+        total_rows += take.numel()
+        total_flops += rows_flops(w, take)
+        used += 1
+    return {"value": total_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d query rows (%d seeded rows per head x %d heads, all their keys), %.1f s" %
+                      (total_rows, total_rows // (w.B * w.H), w.B * w.H, t_total)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    w = WORKLOADS[args.workload]
+    g = torch.Generator("cpu").manual_seed(w.seed)
+    from tiled_online_softmax_fwd_gb300.inputs import make_qkv, sample_rows
+    q, k, v = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, generator=g)
+    rows_all = sample_rows(w.B, w.H, w.N, 1024, g)
+    qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+    threads = oracle.default_threads()
+    plan = oracle_rows_for_steps(w, rows_all, args.warmup + args.steps)
+    for s in range(args.warmup):
+        oracle.attn_fwd(qd, kd, vd, w.scale, w.causal, rows=plan[s].numpy(), threads=threads)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for s in range(args.warmup, args.warmup + args.steps):
+        oracle.attn_fwd(qd, kd, vd, w.scale, w.causal, rows=plan[s].numpy(), threads=threads)
+        flops += rows_flops(w, plan[s])
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = "each step: one seeded query row per head (%d rows, all their keys)" % (w.B * w.H)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, **w.describe()},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, world, rank, local):
+    from tiled_online_softmax_fwd_gb300 import fattn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fattn.load()
+    w = WORKLOADS[args.workload]
+    q, k, v, rows_all = make_workload(w)
+    in_digest = digest(q, k, v)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    do = torch.empty_like(dq)
+    dl = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    big = w.io_bytes > L2_BYTES
+    flush = None if big else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        fattn.attn_fwd(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, lse=dl, stream=stream)
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clocks:
+        t_wall0 = time.perf_counter()
+        if big:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            kernel_ms = e0.elapsed_time(e1) / args.steps
+        else:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for a, b in evs:
+                flush.zero_()
+                a.record(stream)
+                step()
+                b.record(stream)
+            torch.cuda.synchronize()
+            kernel_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+        wall_ms = (time.perf_counter() - t_wall0) * 1e3 / args.steps
+    barrier(world)
+    torch.cuda.synchronize()
+    status = fattn.device_status()
+    ms = max_over_ranks(world, kernel_ms)
+    value = world * w.flops / (ms * 1e-3) / 1e12
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+
+    # End to end through the C ABI with host buffers (pinned), copies timed.
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        ho = torch.empty_like(q).pin_memory()
+        hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        n_e2e = max(3, min(args.steps, 20))
+        for _ in range(2):
+            fattn.attn_fwd_host(hq, hk, hv, ho, hl, dq, dk, dv, do, dl, causal=w.causal,
+                                scale=w.scale, stream=stream)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            fattn.attn_fwd_host(hq, hk, hv, ho, hl, dq, dk, dv, do, dl, causal=w.causal,
+                                scale=w.scale, stream=stream)
+        e2e_ms = max_over_ranks(world, (time.perf_counter() - t0) * 1e3 / n_e2e)
+        barrier(world)
+        e2e = {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "steps": n_e2e,
+               "h2d_bytes_per_step": 3 * q.numel() * 2,
+               "d2h_bytes_per_step": q.numel() * 2 + w.B * w.H * w.N * 4}
+
+    if rank != 0:
+        return 0
+    peak, peak_src = measured_peak()
+    traffic, traffic_src = profiled_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, **w.describe(), "parallelism": "replicas" if world > 1 else "single",
+                   "l2": ("inputs larger than L2 (%d MB)" % (w.io_bytes // 10**6)) if big
+                         else "L2 flushed (256 MiB write) before every step, outside the timed events",
+                   "input_digest": in_digest},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
+                     "traffic_source": traffic_src,
+                     "algorithmic_flops_per_launch": w.flops,
+                     "algorithmic_bytes_per_launch": w.io_bytes},
+        "gpu_launches": args.steps,
+        "kernel": "fattn fwd_kernel<%d> (tcgen05/TMA, persistent)" % w.d,
+        "wall_ms_per_step": wall_ms,
+        "clocks": clocks.summary(),
+        "device_status": status,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v, rows_all if rows_all is not None else
+                                            torch.arange(w.B * w.H * w.N),
+                                            budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="libfattn", choices=["libfattn", "reference"])
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

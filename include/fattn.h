@@ -1,0 +1,134 @@
+/*
+ * fattn.h -- C ABI of libfattn, the GB300 (sm_103a) attention forward pass.
+ *
+ * The operation is the FlashAttention forward pass that the pages build up
+ * to: for every head (b, h) and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] ) * V[b,h,j,:]
+ *     lse[b,h,i] = log( sum_j exp( scale * Q[b,h,i,:] . K[b,h,j,:] ) )
+ *
+ * with j over all keys, or over j <= i when `causal` is set (the lower
+ * triangle including the diagonal).  Sources: "OpenAI Triton: from
+ * introduction to model practice", section 3 (the standard attention it
+ * replaces: scores scaled by 1/sqrt(head_dim), causal masked_fill, softmax,
+ * times V) and section 5 (Figure 5 and Source 2: one fused kernel that keeps
+ * a running row max m_i and exp-sum l_i, rescales the accumulator, and writes
+ * the output plus lse = m_i + log(l_i) in natural log); "Triton hand-written
+ * kernels: vector add -> tiled GEMM -> FlashAttention core", section 4 (the
+ * online softmax with m_i, l_i and acc; fp32 accumulation, 16-bit P into the
+ * second product).  The N x N score matrix is never written to memory.
+ *
+ * Conventions shared by every call:
+ *   - Tensors q, k, v, o are contiguous bf16 [B][H][N][d]: element (b,h,i,c)
+ *     lives at ((b*H + h)*N + i)*d + c.  lse is contiguous fp32 [B][H][N].
+ *   - Device pointers must come from the CUDA device that is current on the
+ *     calling thread and be 16-byte aligned.  The caller allocates and owns
+ *     every buffer; q, k, v are only read; o and lse are fully overwritten
+ *     (every row 0..N-1 of every head).  o and lse must not overlap q, k, v
+ *     or each other.
+ *   - Supported: d in {64, 128}; B, H, N >= 0 with B*H < 2^31 and each
+ *     tensor under 2^39 bytes; scale finite and > 0; causal in {0, 1}.
+ *     Any N works: a ragged last tile is masked (keys past N get weight 0,
+ *     rows past N are not written).
+ *   - Calls are asynchronous: the work is enqueued on `stream` (NULL = the
+ *     legacy default stream) and the call returns; results are valid once
+ *     the stream has been synchronised.  Arguments are checked synchronously
+ *     and nothing is enqueued when a check fails.  B*H*N == 0 is a no-op that
+ *     returns FATTN_OK.
+ *   - The library keeps no per-call allocations and no hidden workspace.
+ *   - Calls are thread-safe; concurrent calls on different streams may run
+ *     concurrently on the device.
+ */
+#ifndef FATTN_H
+#define FATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t / CUstream */
+
+typedef enum fattn_status {
+    FATTN_OK = 0,
+    FATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, misalignment, overlap */
+    FATTN_ERR_UNSUPPORTED = 2, /* d not in {64,128}, tensor too large, device is not sm_103 */
+    FATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; see fattn_last_cuda_error() */
+    FATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a pipeline wait (see fattn_get_device_status) */
+} fattn_status_t;
+
+/*
+ * attn_fwd -- the attention forward pass on device buffers.
+ *
+ *   q, k, v : device, bf16 [B][H][N][d], read only
+ *   o       : device, bf16 [B][H][N][d], written: the normalised output
+ *   lse     : device, fp32 [B][H][N], written: natural-log log-sum-exp of
+ *             the scaled (and masked) scores of each row
+ *   B, H, N : batch, heads, sequence length (queries and keys alike)
+ *   d       : head dimension, 64 or 128
+ *   scale   : multiplies Q.K before masking and softmax (usually 1/sqrt(d))
+ *   causal  : 1 keeps keys j <= i for query i, 0 keeps all keys
+ *   stream  : CUDA stream the kernel is enqueued on
+ *
+ * Returns FATTN_OK once the kernel is enqueued, or an error status without
+ * enqueuing anything.  A pipeline timeout inside the kernel is not reported
+ * here (the call has already returned); it leaves o/lse undefined and sets the
+ * device status word read by fattn_get_device_status().
+ */
+fattn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int B, int H, int N, int d, float scale, int causal,
+                        struct CUstream_st *stream);
+
+/*
+ * attn_fwd_host -- the same operation on HOST buffers, end to end.
+ *
+ * Copies q_host, k_host, v_host to the caller's device buffers dq, dk, dv,
+ * runs attn_fwd into do_ / dlse, and copies the results back to o_host and
+ * lse_host, all enqueued on `stream`; it then synchronises the stream and
+ * returns.  Host buffers should be page-locked (cudaHostAlloc / pinned) for
+ * asynchronous full-bandwidth copies; pageable memory works but is slower.
+ * Device buffers follow attn_fwd's rules.  The library allocates nothing.
+ * The return value includes any error raised while the stream drained.
+ */
+fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                             void *o_host, float *lse_host,
+                             void *dq, void *dk, void *dv, void *do_, float *dlse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             struct CUstream_st *stream);
+
+/*
+ * attn_fwd_simt -- the same operation and contract as attn_fwd, computed by a
+ * plain fp32 SIMT kernel (no tensor cores, no 16-bit rounding of P).  It is
+ * an independent second GPU implementation for cross-checking results at
+ * sizes where the CPU reference is too slow; it is far slower than attn_fwd.
+ */
+fattn_status_t attn_fwd_simt(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             struct CUstream_st *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *fattn_status_string(fattn_status_t status);
+
+/* The CUDA error code (cudaError_t value) behind the calling thread's most
+ * recent FATTN_ERR_CUDA, or 0. */
+int fattn_last_cuda_error(void);
+
+/*
+ * fattn_get_device_status -- read and clear the device status word of the
+ * current device, after synchronising `stream`.
+ *
+ * *status receives 0 when no kernel reported a problem since the last read,
+ * otherwise a nonzero code: bits 0..7 = FATTN_ERR_TIMEOUT, bits 8..15 = the
+ * role that gave up (1 load, 2 mma, 3 softmax, 4 epilogue), bits 16..31 = the
+ * CTA index.  Returns FATTN_ERR_TIMEOUT if *status is nonzero, FATTN_OK if it
+ * is zero, or FATTN_ERR_INVALID_ARG / FATTN_ERR_CUDA.
+ */
+fattn_status_t fattn_get_device_status(int *status, struct CUstream_st *stream);
+
+/* Library version string, e.g. "libfattn 0.1.0 sm_103a". */
+const char *fattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H */

@@ -1,0 +1,123 @@
+"""CPU tests of the C-ABI boundary: the library loads, exports every function
+that include/*.h declares, and rejects bad arguments synchronously (these
+checks run before any device call, so no GPU is needed)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from tiled_online_softmax_fwd_gb300 import build as fbuild
+from tiled_online_softmax_fwd_gb300 import fattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fattn.library_path()):
+        fbuild.build()
+    return fattn.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_host", "attn_fwd_simt", "fattn_status_string",
+              "fattn_last_cuda_error", "fattn_get_device_status", "fattn_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), "libfattn.so does not export %s" % name
+
+
+def test_library_exports_nothing_else():
+    nm = os.popen("nm -D --defined-only %s" % fattn.library_path()).read().split("\n")
+    funcs = sorted(l.split()[-1] for l in nm if " T " in l)
+    assert funcs == declared_functions(), funcs
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fattn_status_string(0) == b"FATTN_OK"
+    assert lib.fattn_status_string(1) == b"FATTN_ERR_INVALID_ARG"
+    assert lib.fattn_status_string(4) == b"FATTN_ERR_TIMEOUT"
+    assert lib.fattn_status_string(99) == b"FATTN_UNKNOWN_STATUS"
+    assert fattn.version().startswith("libfattn")
+
+
+A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced by these calls
+
+
+def call(lib, q=A, k=A + (1 << 24), v=A + (2 << 24), o=A + (3 << 24), lse=A + (4 << 24),
+         B=1, H=2, N=64, d=64, scale=0.125, causal=0):
+    return lib.attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, None)
+
+
+def test_empty_problems_are_noops(lib):
+    # Nothing to do: OK without touching pointers or the device.
+    assert call(lib, q=0, k=0, v=0, o=0, lse=0, N=0) == OK
+    assert call(lib, q=0, k=0, v=0, o=0, lse=0, B=0) == OK
+    assert call(lib, q=0, k=0, v=0, o=0, lse=0, H=0) == OK
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=-1), INVALID), (dict(H=-1), INVALID), (dict(N=-5), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(d=0), UNSUPPORTED), (dict(d=256), UNSUPPORTED),
+    (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID),
+    (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(causal=2), INVALID), (dict(causal=-1), INVALID),
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(v=0), INVALID), (dict(o=0), INVALID),
+    (dict(lse=0), INVALID),
+    (dict(q=A + 8), INVALID), (dict(o=A + (3 << 24) + 2), INVALID), (dict(lse=A + (4 << 24) + 4), INVALID),
+    (dict(o=A), INVALID),                         # output aliases q
+    (dict(o=A + 4096), INVALID),                  # output overlaps q
+    (dict(lse=A + (3 << 24) + 4096), INVALID),    # lse inside o
+    (dict(lse=A + (2 << 24)), INVALID),           # lse aliases v
+    (dict(B=1 << 20, H=1 << 12, N=1), UNSUPPORTED),        # B*H beyond the tensor-map range
+    (dict(B=1024, H=1024, N=1 << 20, d=128), UNSUPPORTED),  # tensor beyond 2^39 bytes
+])
+def test_bad_arguments_are_rejected(lib, kw, expect):
+    assert call(lib, **kw) == expect
+
+
+def test_inputs_may_alias_each_other_but_not_outputs(lib):
+    # q == k == v is legal (self-attention on one buffer); validation then
+    # proceeds to the device query, which is not reached for the output cases.
+    assert call(lib, k=A, v=A, o=A) == INVALID
+
+
+def test_host_entry_validates_before_copying(lib):
+    f = lib.attn_fwd_host
+    dev = [A, A + (1 << 24), A + (2 << 24), A + (3 << 24), A + (4 << 24)]
+    host = [A + (10 << 24), A + (11 << 24), A + (12 << 24), A + (13 << 24), A + (14 << 24)]
+    # a bad device buffer is reported before any copy
+    assert f(*host, 0, *dev[1:], 1, 1, 64, 64, 0.125, 0, None) == INVALID
+    # unsupported head dim
+    assert f(*host, *dev, 1, 1, 64, 80, 0.125, 0, None) == UNSUPPORTED
+    # empty problem
+    assert f(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1, 1, 0, 64, 0.125, 0, None) == OK
+
+
+def test_python_binding_checks(lib):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fattn.attn_fwd(q, q, q)  # CPU tensors
+    with pytest.raises(TypeError):
+        fattn.attn_fwd(None, q, q)
+
+
+def test_device_status_argument_check(lib):
+    assert lib.fattn_get_device_status(ctypes.POINTER(ctypes.c_int)(), None) == INVALID

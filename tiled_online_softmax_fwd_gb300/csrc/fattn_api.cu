@@ -1,0 +1,302 @@
+// fattn_api.cu -- the C ABI of libfattn (see include/fattn.h).
+//
+// Validation follows the wrapper conventions of "Triton programming
+// template" (check device, shape, dtype and layout before launching; return
+// early for empty inputs; launch asynchronously on the caller's stream).  All
+// checks are synchronous and nothing is enqueued when one fails.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fattn.h"
+#include "fattn_internal.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+fattn_status_t cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = static_cast<int>(e);
+    return FATTN_ERR_CUDA;
+}
+
+// Per-device facts, read once.
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int num_sms = 0;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+fattn_status_t current_device(int *dev, DeviceInfo *info)
+{
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    if (*dev < 0 || *dev >= kMaxDevices)
+        return FATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[*dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess)
+            return cuda_fail(e);
+        d.supported = (major == 10 && minor == 3);  // the kernels are built for sm_103a only
+        d.num_sms = sms;
+        d.probed = true;
+    }
+    *info = d;
+    return d.supported ? FATTN_OK : FATTN_ERR_UNSUPPORTED;
+}
+
+fattn_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
+{
+    std::call_once(g_encode_once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (g_encode_err != cudaSuccess || g_encode == nullptr)
+        return cuda_fail(g_encode_err != cudaSuccess ? g_encode_err : cudaErrorSymbolNotFound);
+    *fn = g_encode;
+    return FATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Shape and scalar checks that need no device.  Sets *empty when there is no
+// work (B*H*N == 0).
+fattn_status_t check_shape(int B, int H, int N, int d, float scale, int causal, bool *empty)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1)
+        return FATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale))
+        return FATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128)
+        return FATTN_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(B) * H * N;
+    *empty = rows == 0;
+    // Each tensor must stay below 2^40 bytes (tensor-map stride limit) and
+    // B*H must fit the tensor map's outer dimension.
+    if (static_cast<long long>(B) * H > 0x7fffffffLL)
+        return FATTN_ERR_UNSUPPORTED;
+    if (!*empty && rows > (1LL << 39) / (2LL * d))
+        return FATTN_ERR_UNSUPPORTED;
+    return FATTN_OK;
+}
+
+// Pointer checks: non-null, 16-byte aligned, no output overlapping an input or
+// the other output.
+fattn_status_t check_pointers(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, size_t tensor_bytes, size_t lse_bytes)
+{
+    if (!q || !k || !v || !o || !lse)
+        return FATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FATTN_ERR_INVALID_ARG;
+    if (overlap(o, tensor_bytes, q, tensor_bytes) || overlap(o, tensor_bytes, k, tensor_bytes) ||
+        overlap(o, tensor_bytes, v, tensor_bytes) || overlap(o, tensor_bytes, lse, lse_bytes) ||
+        overlap(lse, lse_bytes, q, tensor_bytes) || overlap(lse, lse_bytes, k, tensor_bytes) ||
+        overlap(lse, lse_bytes, v, tensor_bytes))
+        return FATTN_ERR_INVALID_ARG;
+    return FATTN_OK;
+}
+
+// The buffer must be device (or managed) memory of the current device.
+fattn_status_t check_device_buffer(const void *p, int dev)
+{
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error state of this query
+        return FATTN_ERR_INVALID_ARG;
+    }
+    if (attr.type == cudaMemoryTypeDevice)
+        return attr.device == dev ? FATTN_OK : FATTN_ERR_INVALID_ARG;
+    if (attr.type == cudaMemoryTypeManaged)
+        return FATTN_OK;
+    return FATTN_ERR_INVALID_ARG;
+}
+
+fattn_status_t make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m, const void *ptr,
+                        int N, int d, long long BH)
+{
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+                              strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return FATTN_ERR_CUDA;
+    }
+    return FATTN_OK;
+}
+
+enum class Kernel { kTcgen05, kSimt };
+
+// Every check of a forward call.  On FATTN_OK, *empty tells whether there is
+// any work, and (when there is) *dev / *info describe the current device.
+fattn_status_t validate(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, int B, int H, int N, int d, float scale, int causal,
+                        bool *empty, int *dev, DeviceInfo *info)
+{
+    fattn_status_t s = check_shape(B, H, N, d, scale, causal, empty);
+    if (s != FATTN_OK || *empty)
+        return s;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    if ((s = check_pointers(q, k, v, o, lse, rows * d * 2, rows * 4)) != FATTN_OK)
+        return s;
+    if ((s = current_device(dev, info)) != FATTN_OK)
+        return s;
+    const void *bufs[5] = {q, k, v, o, lse};
+    for (const void *p : bufs)
+        if ((s = check_device_buffer(p, *dev)) != FATTN_OK)
+            return s;
+    return FATTN_OK;
+}
+
+// Enqueue one validated forward call.
+fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const void *k,
+                      const void *v, void *o, float *lse, int B, int H, int N, int d, float scale,
+                      int causal, cudaStream_t stream)
+{
+    fattn::FwdArgs a{q, k, v, o, lse, B, H, N, d, scale, causal};
+    cudaError_t e;
+    if (which == Kernel::kSimt) {
+        e = fattn::launch_fwd_simt(a, stream);
+    } else {
+        PFN_cuTensorMapEncodeTiled_v12000 encode;
+        fattn_status_t s;
+        if ((s = get_encoder(&encode)) != FATTN_OK)
+            return s;
+        fattn::FwdMaps maps;
+        const long long BH = static_cast<long long>(B) * H;
+        if ((s = make_map(encode, &maps.q, q, N, d, BH)) != FATTN_OK ||
+            (s = make_map(encode, &maps.k, k, N, d, BH)) != FATTN_OK ||
+            (s = make_map(encode, &maps.v, v, N, d, BH)) != FATTN_OK)
+            return s;
+        e = fattn::launch_fwd_sm103(a, maps, info.num_sms, stream);
+    }
+    return e == cudaSuccess ? FATTN_OK : cuda_fail(e);
+}
+
+fattn_status_t forward(Kernel which, const void *q, const void *k, const void *v, void *o,
+                       float *lse, int B, int H, int N, int d, float scale, int causal,
+                       cudaStream_t stream)
+{
+    bool empty = false;
+    int dev = 0;
+    DeviceInfo info;
+    fattn_status_t s = validate(q, k, v, o, lse, B, H, N, d, scale, causal, &empty, &dev, &info);
+    if (s != FATTN_OK || empty)
+        return s;
+    return launch(which, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fattn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                        int H, int N, int d, float scale, int causal, struct CUstream_st *stream)
+{
+    return forward(Kernel::kTcgen05, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+fattn_status_t attn_fwd_simt(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             struct CUstream_st *stream)
+{
+    return forward(Kernel::kSimt, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                             void *o_host, float *lse_host, void *dq, void *dk, void *dv, void *do_,
+                             float *dlse, int B, int H, int N, int d, float scale, int causal,
+                             struct CUstream_st *stream)
+{
+    bool empty = false;
+    int dev = 0;
+    DeviceInfo info;
+    fattn_status_t s = validate(dq, dk, dv, do_, dlse, B, H, N, d, scale, causal, &empty, &dev,
+                                &info);
+    if (s != FATTN_OK || empty)
+        return s;
+    if (!q_host || !k_host || !v_host || !o_host || !lse_host)
+        return FATTN_ERR_INVALID_ARG;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    const size_t tensor_bytes = rows * d * 2, lse_bytes = rows * 4;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(dq, q_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dk, k_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dv, v_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((s = launch(Kernel::kTcgen05, info, dq, dk, dv, do_, dlse, B, H, N, d, scale, causal,
+                    stream)) != FATTN_OK)
+        return s;
+    if ((e = cudaMemcpyAsync(o_host, do_, tensor_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(lse_host, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess)
+        return cuda_fail(e);
+    return FATTN_OK;
+}
+
+const char *fattn_status_string(fattn_status_t status)
+{
+    switch (status) {
+    case FATTN_OK: return "FATTN_OK";
+    case FATTN_ERR_INVALID_ARG: return "FATTN_ERR_INVALID_ARG";
+    case FATTN_ERR_UNSUPPORTED: return "FATTN_ERR_UNSUPPORTED";
+    case FATTN_ERR_CUDA: return "FATTN_ERR_CUDA";
+    case FATTN_ERR_TIMEOUT: return "FATTN_ERR_TIMEOUT";
+    }
+    return "FATTN_UNKNOWN_STATUS";
+}
+
+int fattn_last_cuda_error(void) { return t_last_cuda_error; }
+
+fattn_status_t fattn_get_device_status(int *status, struct CUstream_st *stream)
+{
+    if (!status)
+        return FATTN_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    const cudaError_t e = fattn::read_and_clear_status(&word, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    *status = static_cast<int>(word);
+    return word == 0 ? FATTN_OK : FATTN_ERR_TIMEOUT;
+}
+
+const char *fattn_version(void) { return "libfattn 0.1.0 sm_103a"; }
+
+}  // extern "C"

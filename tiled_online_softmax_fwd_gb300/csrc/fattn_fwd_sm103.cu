@@ -1,0 +1,590 @@
+// fattn_fwd_sm103.cu -- attention forward pass for GB300 (sm_103a).
+//
+// The method is the FlashAttention forward pass with an online softmax
+// ("Triton hand-written kernels: vector add -> tiled GEMM -> FlashAttention
+// core", section 4; "OpenAI Triton: from introduction to model practice",
+// section 5, Figure 5 and Source 2): for each tile of query rows, stream the
+// key/value tiles, form S = scale * Q K^T, keep a running row max m and
+// exp-sum l, rescale the accumulator when m grows, add P V, and at the end
+// write O = acc / l and lse = m + ln l.  Scores never leave the chip.
+//
+// GB300 design (one persistent CTA per SM, 320 threads):
+//   warp 8      TMA producer: Q tiles and a ring of K/V tiles in 128-byte
+//               swizzled shared memory, completion tracked by mbarriers.
+//   warp 9      MMA issuer (one thread): S = Q K^T and O += P V as tcgen05
+//               MMAs (bf16 in, fp32 accumulate) into tensor memory (TMEM).
+//   warps 0-7   two softmax warpgroups, one per 128-row Q tile; they
+//               alternate (ping-pong) so that one computes exponentials
+//               while the tensor core works on the other tile.  Each thread
+//               owns one query row: it reads its S row from TMEM, applies
+//               the causal / tail mask, updates m and l, writes P (bf16)
+//               back into TMEM over its S row, rescales its O row in TMEM
+//               when needed, and finally normalises and stores O and lse.
+// A work unit is two consecutive 128-row Q tiles of one (batch, head).  The
+// units are ordered heaviest first (for the causal mask the work of a Q tile
+// grows with its index) and dealt to the CTAs in a serpentine order so that
+// no SM is left with a long tail ("wave quantisation").  Under the causal
+// mask, key tiles entirely above the diagonal are skipped and only the
+// diagonal tile is masked element-wise.
+//
+// Tensor memory (512 columns x 128 lanes, fp32 words):
+//   [0,128)   S of tile 0 (P of tile 0 overwrites its first 64 columns)
+//   [128,256) S of tile 1 (likewise)
+//   [256,256+D)      O accumulator of tile 0
+//   [256+D,256+2D)   O accumulator of tile 1
+//
+// Softmax details.  Scores are handled in the base-2 domain: x = s * scale *
+// log2(e), p = 2^(x - m).  The running max m is only raised when a new row
+// maximum exceeds it by more than kRescaleLog2 (so O and l need rescaling
+// rarely); until then p may exceed 1 by at most 2^kRescaleLog2.  This is
+// exact algebra: O and l always refer to the same m, so O / l and
+// lse = ln2 * (m + log2 l) are unchanged.  l is summed from the bf16-rounded
+// probabilities that actually enter P V, so the weights applied to V are
+// exactly normalised.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fattn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace fattn {
+
+// Device status word: 0, or the first timeout code recorded by any CTA.
+__device__ uint32_t g_fattn_status;
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;  // query rows per Q tile (= MMA M = TMEM lanes)
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kChunkBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 box
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along d
+    static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring depth
+    static constexpr uint32_t kTilesBytes = (2 + kStages) * kTileBytes;
+    static constexpr uint32_t kColO0 = 256;
+    static constexpr uint32_t kColO1 = 256 + D;
+};
+
+struct Bars {
+    uint64_t q_full[2], q_empty[2];
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct Params {
+    __nv_bfloat16 *o;
+    float *lse;
+    int N;      // sequence length
+    int BH;     // batch * heads
+    int QT;     // query tiles per head = ceil(N / 128)
+    int KT;     // key tiles per head
+    int pairs;  // work units per head = ceil(QT / 2)
+    int units;  // BH * pairs
+    int causal;
+    float sl2;  // scale * log2(e)
+};
+
+struct Unit {
+    int bh;
+    int qt[2];
+    int nkv[2];  // key tiles visited by each Q tile (0: tile absent)
+    int nkv_max;
+};
+
+__device__ __forceinline__ Unit unit_at(const Params &p, int k)
+{
+    Unit u;
+    const int pair = p.pairs - 1 - k / p.BH;  // heaviest pairs first
+    u.bh = k % p.BH;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        u.qt[t] = 2 * pair + t;
+        if (u.qt[t] >= p.QT)
+            u.nkv[t] = 0;
+        else
+            u.nkv[t] = p.causal ? min(u.qt[t] + 1, p.KT) : p.KT;
+    }
+    u.nkv_max = max(u.nkv[0], u.nkv[1]);
+    return u;
+}
+
+// Serpentine deal: round r gives CTA c the unit r*G + c (r even) or
+// r*G + G-1-c (r odd).
+__device__ __forceinline__ int unit_index(int round, int cta, int grid)
+{
+    return round * grid + ((round & 1) ? grid - 1 - cta : cta);
+}
+
+__device__ __forceinline__ void record_failure(Bars &b, uint32_t role)
+{
+    const uint32_t code = 4u /* FATTN_ERR_TIMEOUT */ | (role << 8) | ((blockIdx.x & 0xffffu) << 16);
+    atomicCAS(&g_fattn_status, 0u, code);
+    *reinterpret_cast<volatile int *>(&b.abort) = 1;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUtensorMap *mq,
+                         const CUtensorMap *mk, const CUtensorMap *mv)
+{
+    using C = Cfg<D>;
+    const volatile int *abort = &b.abort;
+    uint32_t q_phase[2] = {0, 0};
+    uint32_t pos = 0;  // K/V ring position (K_j, V_j alternate)
+    bool ok = true;
+    int last_q_parity[2] = {-1, -1};
+    for (int r = 0; ok; ++r) {
+        const int k = unit_index(r, blockIdx.x, gridDim.x);
+        if (k >= p.units)
+            break;
+        const Unit u = unit_at(p, k);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (!ok || u.nkv[t] == 0)
+                continue;
+            const uint32_t full = smem_addr(&b.q_full[t]);
+            if (!mbar_wait(smem_addr(&b.q_empty[t]), q_phase[t] ^ 1, kWaitLimitNs, abort)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(full, C::kTileBytes);
+            const uint32_t dst = smem_base + t * C::kTileBytes;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(dst + c * kChunkBytes, mq, full, 64 * c, u.qt[t] * kBM, u.bh);
+            last_q_parity[t] = q_phase[t];
+            q_phase[t] ^= 1;
+        }
+        for (int j = 0; ok && j < u.nkv_max; ++j) {
+#pragma unroll
+            for (int which = 0; which < 2; ++which, ++pos) {
+                const uint32_t stage = pos % C::kStages;
+                const uint32_t phase = (pos / C::kStages) & 1;
+                if (!mbar_wait(smem_addr(&b.kv_empty[stage]), phase ^ 1, kWaitLimitNs, abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = smem_addr(&b.kv_full[stage]);
+                mbar_arrive_expect_tx(full, C::kTileBytes);
+                const uint32_t dst = smem_base + (2 + stage) * C::kTileBytes;
+                const CUtensorMap *m = which == 0 ? mk : mv;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(dst + c * kChunkBytes, m, full, 64 * c, j * kBN, u.bh);
+            }
+        }
+    }
+    if (!ok) {
+        record_failure(b, kRoleLoad);
+        // Let the copies already issued land before the CTA exits.
+        const uint32_t issued = pos;
+        const uint32_t first = issued > (uint32_t)C::kStages ? issued - C::kStages : 0;
+        for (uint32_t q = first; q < issued; ++q)
+            mbar_wait(smem_addr(&b.kv_full[q % C::kStages]), (q / C::kStages) & 1,
+                      kWaitLimitNs / 8, nullptr);
+        for (int t = 0; t < 2; ++t)
+            if (last_q_parity[t] >= 0)
+                mbar_wait(smem_addr(&b.q_full[t]), last_q_parity[t], kWaitLimitNs / 8, nullptr);
+    }
+}
+
+// ------------------------------------------------------------------ MMA issue
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem)
+{
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+        mma_ss(tmem_d, smem_desc(q_smem + off, 16, 1024), smem_desc(k_smem + off, 16, 1024),
+               idesc, kk > 0);
+    }
+}
+
+// V tiles are MN-major (d contiguous) for the P V product: the stride between
+// 8-key groups is 1024 bytes (SBO) and the stride between the two 64-column
+// halves of d = 128 is one 16 KB box (LBO; with d = 64 there is one half and
+// the value is irrelevant, so it is kept inside the tile).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_smem,
+                                         bool accumulate)
+{
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+    constexpr uint32_t kVLbo = D == 128 ? kChunkBytes : 1024;
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_ts(tmem_d, tmem_p + kk * 8, smem_desc(v_smem + kk * 16 * 128, kVLbo, 1024), idesc,
+               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int D>
+__device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t tmem)
+{
+    using C = Cfg<D>;
+    const volatile int *abort = &b.abort;
+    const uint32_t col_s[2] = {0, 128};
+    const uint32_t col_o[2] = {C::kColO0, C::kColO1};
+    uint32_t q_phase[2] = {0, 0}, p_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
+    uint32_t pos = 0;
+    bool ok = true;
+
+    auto kv_stage = [&](uint32_t at) { return at % C::kStages; };
+    auto kv_wait = [&](uint32_t at) {
+        return mbar_wait(smem_addr(&b.kv_full[at % C::kStages]), (at / C::kStages) & 1,
+                         kWaitLimitNs, abort);
+    };
+    auto kv_smem = [&](uint32_t at) { return smem_base + (2 + kv_stage(at)) * C::kTileBytes; };
+
+    for (int r = 0; ok; ++r) {
+        const int k = unit_index(r, blockIdx.x, gridDim.x);
+        if (k >= p.units)
+            break;
+        const Unit u = unit_at(p, k);
+        const uint32_t base = pos;  // K_j at base + 2j, V_j at base + 2j + 1
+        for (int t = 0; t < 2 && ok; ++t)
+            if (u.nkv[t] > 0) {
+                ok = mbar_wait(smem_addr(&b.q_full[t]), q_phase[t], kWaitLimitNs, abort);
+                q_phase[t] ^= 1;
+            }
+        if (ok)
+            ok = kv_wait(base);
+        if (!ok)
+            break;
+        tc_fence_after();
+        // Key tile 0: S for both Q tiles.
+        for (int t = 0; t < 2; ++t) {
+            if (u.nkv[t] == 0)
+                continue;
+            issue_s<D>(tmem + col_s[t], smem_base + t * C::kTileBytes, kv_smem(base));
+            mma_commit(smem_addr(&b.s_full[t]));
+            if (u.nkv[t] == 1)
+                mma_commit(smem_addr(&b.q_empty[t]));
+        }
+        mma_commit(smem_addr(&b.kv_empty[kv_stage(base)]));
+
+        // Key tiles 1..n-1: P V of the previous tile, then S of this one.
+        for (int j = 1; j <= u.nkv_max && ok; ++j) {
+            const uint32_t at_v = base + 2 * (j - 1) + 1;
+            const uint32_t at_k = base + 2 * j;
+            const bool has_k = j < u.nkv_max;
+            ok = kv_wait(at_v) && (!has_k || kv_wait(at_k));
+            if (!ok)
+                break;
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (j - 1 >= u.nkv[t])
+                    continue;  // tile t finished earlier (or is absent)
+                ok = mbar_wait(smem_addr(&b.p_full[t]), p_phase[t], kWaitLimitNs, abort);
+                p_phase[t] ^= 1;
+                if (ok && j - 1 == 0) {  // first P V of the unit overwrites O
+                    ok = mbar_wait(smem_addr(&b.o_empty[t]), oe_phase[t] ^ 1, kWaitLimitNs, abort);
+                    oe_phase[t] ^= 1;
+                }
+                if (!ok)
+                    break;
+                tc_fence_after();
+                issue_pv<D>(tmem + col_o[t], tmem + col_s[t], kv_smem(at_v), j - 1 > 0);
+                if (j < u.nkv[t]) {
+                    issue_s<D>(tmem + col_s[t], smem_base + t * C::kTileBytes, kv_smem(at_k));
+                    mma_commit(smem_addr(&b.s_full[t]));
+                    if (j == u.nkv[t] - 1)
+                        mma_commit(smem_addr(&b.q_empty[t]));
+                } else {
+                    mma_commit(smem_addr(&b.o_full[t]));
+                }
+            }
+            if (!ok)
+                break;
+            mma_commit(smem_addr(&b.kv_empty[kv_stage(at_v)]));
+            if (has_k)
+                mma_commit(smem_addr(&b.kv_empty[kv_stage(at_k)]));
+        }
+        pos = base + 2 * u.nkv_max;
+    }
+    if (!ok)
+        record_failure(b, kRoleMma);
+    // Wait until every MMA this thread issued has completed.
+    mma_commit(smem_addr(&b.drain));
+    mbar_wait(smem_addr(&b.drain), 0, kWaitLimitNs, nullptr);
+}
+
+// ------------------------------------------------------------------ softmax
+template <int D>
+__device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
+{
+    using C = Cfg<D>;
+    const volatile int *abort = &b.abort;
+    const int warp = (threadIdx.x / 32) & 3;
+    const int lane = threadIdx.x & 31;
+    const int r = warp * 32 + lane;                          // row within the Q tile
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + (t == 0 ? 0u : 128u);
+    const uint32_t t_o = tmem + lane_off + (t == 0 ? C::kColO0 : C::kColO1);
+    uint32_t s_phase = 0, of_phase = 0;
+    bool ok = true;
+
+    for (int rr = 0; ok; ++rr) {
+        const int k = unit_index(rr, blockIdx.x, gridDim.x);
+        if (k >= p.units)
+            break;
+        const Unit u = unit_at(p, k);
+        if (u.nkv[t] == 0)
+            continue;
+        const int qt = u.qt[t];
+        const int row = qt * kBM + r;
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < u.nkv[t]; ++j) {
+            ok = mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, abort);
+            s_phase ^= 1;
+            if (!ok)
+                break;
+            tc_fence_after();
+            __syncwarp();
+            float s[kBN];
+            {
+                uint32_t raw[32];
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) {
+                    tmem_ld32(t_s + c * 32, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        s[c * 32 + i] = __uint_as_float(raw[i]);
+                }
+            }
+            // Mask (only on the diagonal tile and the ragged last tile; the
+            // branch is uniform across the warp): keys above the diagonal
+            // and keys past N get -inf, i.e. weight exactly 0.
+            const bool diag = p.causal && j == qt;
+            const bool tail = (j + 1) * kBN > p.N;
+            if (diag || tail) {
+                int limit = diag ? r : kBN - 1;
+                if (tail)
+                    limit = min(limit, p.N - 1 - j * kBN);
+#pragma unroll
+                for (int i = 0; i < kBN; ++i)
+                    s[i] = i > limit ? -INFINITY : s[i];
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int i = 1; i < kBN; ++i)
+                mx = fmaxf(mx, s[i]);
+            const float cand = mx * p.sl2;
+            const float m_new = (j == 0 || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
+            const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
+            float rowsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], p.sl2, -m_new));
+                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], p.sl2, -m_new));
+                    pk[i] = pack_bf16x2(p0, p1);
+                    rowsum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                }
+                tmem_st16(t_s + c * 16, pk);
+            }
+            l = l * alpha + rowsum;
+            if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(t_o + c * 32, o);
+                }
+            }
+            m = m_new;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&b.p_full[t]));
+        }
+        if (!ok)
+            break;
+        // Epilogue: O / l in bf16, lse = ln2 * (m + log2 l).
+        ok = mbar_wait(smem_addr(&b.o_full[t]), of_phase, kWaitLimitNs, abort);
+        of_phase ^= 1;
+        if (!ok)
+            break;
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        const bool live = row < p.N;
+        __nv_bfloat16 *orow = p.o + (static_cast<size_t>(u.bh) * p.N + row) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            __syncwarp();
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (live) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+        if (live)
+            p.lse[static_cast<size_t>(u.bh) * p.N + row] = (m + log2f(l)) * kLn2;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&b.o_empty[t]));
+    }
+    if (!ok)
+        record_failure(b, kRoleSoftmax);
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const Params p)
+{
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t smem_base = (raw + 1023u) & ~1023u;
+    Bars &b = *reinterpret_cast<Bars *>(smem_raw + (smem_base - raw) + C::kTilesBytes);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_addr(&b.q_full[t]), 1);
+            mbar_init(smem_addr(&b.q_empty[t]), 1);
+            mbar_init(smem_addr(&b.s_full[t]), 1);
+            mbar_init(smem_addr(&b.p_full[t]), 4);
+            mbar_init(smem_addr(&b.o_full[t]), 1);
+            mbar_init(smem_addr(&b.o_empty[t]), 4);
+        }
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_addr(&b.kv_full[s]), 1);
+            mbar_init(smem_addr(&b.kv_empty[s]), 1);
+        }
+        mbar_init(smem_addr(&b.drain), 1);
+        b.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_addr(&b.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kWarpLoad && lane == 0) {
+        prefetch_tensormap(&mq);
+        prefetch_tensormap(&mk);
+        prefetch_tensormap(&mv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = b.tmem_base;
+
+    if (warp < 8) {
+        run_softmax<D>(p, b, tmem, warp / 4);
+    } else if (warp == kWarpLoad) {
+        if (lane == 0)
+            run_load<D>(p, b, smem_base, &mq, &mk, &mv);
+    } else if (warp == kWarpMma) {
+        if (lane == 0)
+            run_mma<D>(p, b, smem_base, tmem);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, int num_sms, cudaStream_t stream)
+{
+    using C = Cfg<D>;
+    Params p;
+    p.o = static_cast<__nv_bfloat16 *>(a.o);
+    p.lse = a.lse;
+    p.N = a.N;
+    p.BH = a.B * a.H;
+    p.QT = (a.N + kBM - 1) / kBM;
+    p.KT = (a.N + kBN - 1) / kBN;
+    p.pairs = (p.QT + 1) / 2;
+    const long long units = static_cast<long long>(p.BH) * p.pairs;
+    if (units == 0)
+        return cudaSuccess;
+    if (units > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    p.units = static_cast<int>(units);
+    p.causal = a.causal;
+    p.sl2 = a.scale * kLog2e;
+    const size_t smem = C::kTilesBytes + sizeof(Bars) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+    fwd_kernel<D><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, int num_sms,
+                             cudaStream_t stream)
+{
+    return a.d == 64 ? launch<64>(a, maps, num_sms, stream) : launch<128>(a, maps, num_sms, stream);
+}
+
+cudaError_t read_and_clear_status(uint32_t *out, cudaStream_t stream)
+{
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fattn_status, sizeof(uint32_t), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return e;
+    if (*out != 0) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_fattn_status, &zero, sizeof(uint32_t), 0,
+                                    cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(stream);
+    }
+    return e;
+}
+
+}  // namespace fattn

@@ -1,0 +1,41 @@
+// fattn_internal.h -- declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fattn {
+
+// Arguments of one forward call, already validated by the C-ABI layer.
+struct FwdArgs {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *o;
+    float *lse;
+    int B, H, N, d;
+    float scale;
+    int causal;
+};
+
+// Tensor maps over Q, K, V viewed as 3-D bf16 arrays (d, N, B*H), box
+// (64, 128, 1), 128-byte swizzle, zero fill outside N.
+struct FwdMaps {
+    CUtensorMap q, k, v;
+};
+
+// Device status word codes (see fattn_get_device_status in fattn.h).
+enum DeviceRole : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleEpilogue = 4 };
+
+// tcgen05 / TMA kernel: one persistent CTA per SM.
+cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, int num_sms,
+                             cudaStream_t stream);
+// Reads (and clears) the device status word of the current device.
+cudaError_t read_and_clear_status(uint32_t *out, cudaStream_t stream);
+
+// Plain SIMT kernel (fp32 CUDA cores): a second, independent GPU path used by
+// the tests as a cross-check.  Not used by attn_fwd.
+cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t stream);
+
+}  // namespace fattn

@@ -1,0 +1,202 @@
+"""ctypes binding of libfattn's C ABI (include/fattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch supplies device memory and streams.  The checks mirror the
+wrapper of "Triton programming template" (device, shape, dtype, contiguity)
+so that misuse raises in Python before the C layer sees it; the C layer
+checks again and is the authority.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libfattn.so")
+
+FATTN_OK = 0
+STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
+                3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
+EXPORTED = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "fattn_status_string",
+            "fattn_last_cuda_error", "fattn_get_device_status", "fattn_version"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FattnError(RuntimeError):
+    """A libfattn call returned a status other than FATTN_OK."""
+
+    def __init__(self, status: int, what: str, cuda_error: int = 0):
+        name = STATUS_NAMES.get(status, "status %d" % status)
+        msg = "%s: %s" % (what, name)
+        if cuda_error:
+            msg += " (CUDA error %d)" % cuda_error
+        super().__init__(msg)
+        self.status = status
+        self.cuda_error = cuda_error
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libfattn.so (raises if it has not been built: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                "libfattn.so is not built (%s); run `python -m tiled_online_softmax_fwd_gb300.build`"
+                % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fwd_args = [vp, vp, vp, vp, vp, ip, ip, ip, ip, fp, ip, vp]
+        for name in ("attn_fwd", "attn_fwd_simt"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = fwd_args
+        lib.attn_fwd_host.restype = ctypes.c_int
+        lib.attn_fwd_host.argtypes = [vp] * 10 + [ip, ip, ip, ip, fp, ip, vp]
+        lib.fattn_status_string.restype = ctypes.c_char_p
+        lib.fattn_status_string.argtypes = [ctypes.c_int]
+        lib.fattn_last_cuda_error.restype = ctypes.c_int
+        lib.fattn_last_cuda_error.argtypes = []
+        lib.fattn_get_device_status.restype = ctypes.c_int
+        lib.fattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
+        lib.fattn_version.restype = ctypes.c_char_p
+        lib.fattn_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str):
+    if status != FATTN_OK:
+        cuda_err = load().fattn_last_cuda_error() if status == 3 else 0
+        raise FattnError(status, what, cuda_err)
+
+
+def default_scale(d: int) -> float:
+    """1/sqrt(d) rounded to the fp32 value the kernel receives."""
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _validate(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % name)
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if t.dtype != torch.bfloat16:
+            raise ValueError("%s must be bfloat16, got %s" % (name, t.dtype))
+        if t.dim() != 4:
+            raise ValueError("%s must be [B, H, N, d]" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v shapes differ: %s %s %s" % (q.shape, k.shape, v.shape))
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v are on different devices")
+    if q.shape[-1] not in (64, 128):
+        raise ValueError("head dimension must be 64 or 128, got %d" % q.shape[-1])
+
+
+def _forward(entry: str, q, k, v, causal, scale, out, lse, stream):
+    _validate(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+            or out.device != q.device:
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor on q's device")
+    lib = load()
+    with torch.cuda.device(q.device):
+        st = getattr(lib, entry)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, float(scale), 1 if causal else 0,
+                                 _stream_handle(stream, q.device))
+    _check(st, entry)
+    return out, lse
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             stream=None):
+    """O, lse = attention forward of bf16 [B, H, N, d] CUDA tensors (libfattn attn_fwd).
+
+    scale defaults to 1/sqrt(d).  ``out`` / ``lse`` may be preallocated.  The
+    kernel is enqueued on ``stream`` (default: the current stream)."""
+    return _forward("attn_fwd", q, k, v, causal, scale, out, lse, stream)
+
+
+def attn_fwd_simt(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                  stream=None):
+    """Same as attn_fwd through the plain SIMT cross-check kernel."""
+    return _forward("attn_fwd_simt", q, k, v, causal, scale, out, lse, stream)
+
+
+def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, dq, dk, dv, do, dlse,
+                  causal: bool = False, scale: float | None = None, stream=None):
+    """End-to-end call on host tensors through libfattn attn_fwd_host: copy in,
+    compute, copy out, synchronise.  Host tensors should be pinned; the device
+    tensors are the caller's buffers of matching shape."""
+    B, H, N, d = q_host.shape
+    for t in (q_host, k_host, v_host, o_host, lse_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+    for t in (q_host, k_host, v_host, o_host):
+        if t.dtype != torch.bfloat16 or t.shape != (B, H, N, d):
+            raise ValueError("host q/k/v/o must be bf16 [B, H, N, d]")
+    if lse_host.dtype != torch.float32 or lse_host.shape != (B, H, N):
+        raise ValueError("host lse must be fp32 [B, H, N]")
+    _validate(dq, dk, dv)
+    if scale is None:
+        scale = default_scale(d)
+    lib = load()
+    with torch.cuda.device(dq.device):
+        st = lib.attn_fwd_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                               o_host.data_ptr(), lse_host.data_ptr(), dq.data_ptr(),
+                               dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
+                               B, H, N, d, float(scale), 1 if causal else 0,
+                               _stream_handle(stream, dq.device))
+    _check(st, "attn_fwd_host")
+    return o_host, lse_host
+
+
+def device_status(stream=None, device=None) -> int:
+    """Read and clear the device status word (0 = no kernel reported a problem)."""
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    word = ctypes.c_int(0)
+    with torch.cuda.device(dev):
+        st = lib.fattn_get_device_status(ctypes.byref(word), _stream_handle(stream, dev))
+    if st not in (FATTN_OK, 4):
+        _check(st, "fattn_get_device_status")
+    return word.value
+
+
+def version() -> str:
+    return load().fattn_version().decode()
+
+
+def raw_call(entry: str, *args) -> int:
+    """Call a C entry point with raw integer/float arguments and return its
+    status (used by the boundary tests to probe argument checking)."""
+    return getattr(load(), entry)(*args)
