@@ -38,9 +38,10 @@
 // maximum exceeds it by more than kRescaleLog2 (so O and l need rescaling
 // rarely); until then p may exceed 1 by at most 2^kRescaleLog2.  This is
 // exact algebra: O and l always refer to the same m, so O / l and
-// lse = ln2 * (m + log2 l) are unchanged.  l is summed from the bf16-rounded
-// probabilities that actually enter P V, so the weights applied to V are
-// exactly normalised.
+// lse = ln2 * (m + log2 l) are unchanged.  Two row sums are kept: l of the
+// fp32 probabilities, for lse, and l_round of the bf16-rounded probabilities
+// that actually enter P V, which normalises O, so that the weights applied to
+// V sum to one exactly (the rounding of a dominant p cancels in O / l_round).
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -353,7 +354,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             continue;
         const int qt = u.qt[t];
         const int row = qt * kBM + r;
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f, l_round = 0.f;
         for (int j = 0; j < u.nkv[t]; ++j) {
             ok = mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, abort);
             s_phase ^= 1;
@@ -386,27 +387,42 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                 for (int i = 0; i < kBN; ++i)
                     s[i] = i > limit ? -INFINITY : s[i];
             }
-            float mx = s[0];
+            float mx0 = s[0], mx1 = s[1];
 #pragma unroll
-            for (int i = 1; i < kBN; ++i)
-                mx = fmaxf(mx, s[i]);
-            const float cand = mx * p.sl2;
+            for (int i = 2; i < kBN; i += 4) {
+                mx0 = fmax3(mx0, s[i], s[i + 1]);
+                mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+            }
+            const float cand = fmaxf(mx0, mx1) * p.sl2;
             const float m_new = (j == 0 || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
             const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
-            float rowsum = 0.f;
+            // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row
+            // sums: of the fp32 p (for lse) and of the bf16-rounded p that
+            // P V actually uses (to normalise O).
+            const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
+            const uint64_t negm = f2_pack(-m_new, -m_new);
+            uint64_t sum_exact = f2_pack(0.f, 0.f), sum_round = f2_pack(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], p.sl2, -m_new));
-                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], p.sl2, -m_new));
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm),
+                              x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
                     pk[i] = pack_bf16x2(p0, p1);
-                    rowsum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                    sum_exact = f2_add(sum_exact, f2_pack(p0, p1));
+                    sum_round = f2_add(sum_round, f2_pack(__uint_as_float(pk[i] << 16),
+                                                          __uint_as_float(pk[i] & 0xffff0000u)));
                 }
                 tmem_st16(t_s + c * 16, pk);
             }
-            l = l * alpha + rowsum;
+            float e0, e1, r0, r1;
+            f2_unpack(sum_exact, e0, e1);
+            f2_unpack(sum_round, r0, r1);
+            l = l * alpha + (e0 + e1);
+            l_round = l_round * alpha + (r0 + r1);
             if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -434,7 +450,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         if (!ok)
             break;
         tc_fence_after();
-        const float inv_l = 1.f / l;
+        const float inv_l = 1.f / l_round;
         const bool live = row < p.N;
         __nv_bfloat16 *orow = p.o + (static_cast<size_t>(u.bh) * p.N + row) * D;
 #pragma unroll 1
