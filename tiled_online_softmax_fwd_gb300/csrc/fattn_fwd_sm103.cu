@@ -212,32 +212,42 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
 }
 
 // ------------------------------------------------------------------ MMA issue
+// S = Q K^T: both operands K-major (d contiguous), 128-byte swizzled, 8-row
+// groups 1024 bytes apart.  Each K = 16 step moves 32 bytes along d inside a
+// 64-column box, or to the next 16 KB box.  The start address occupies the
+// low 14 bits of the descriptor's low word and never carries out of them
+// (shared memory is below 256 KB), so a step is one 32-bit add.
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem)
 {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+    constexpr uint32_t hi = smem_desc_hi(1024);
+    const uint32_t a_lo = smem_desc_lo(q_smem, 16), b_lo = smem_desc_lo(k_smem, 16);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-        mma_ss(tmem_d, smem_desc(q_smem + off, 16, 1024), smem_desc(k_smem + off, 16, 1024),
-               idesc, kk > 0);
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss_w(tmem_d, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 // V tiles are MN-major (d contiguous) for the P V product: the stride between
 // 8-key groups is 1024 bytes (SBO) and the stride between the two 64-column
 // halves of d = 128 is one 16 KB box (LBO; with d = 64 there is one half and
-// the value is irrelevant, so it is kept inside the tile).
+// the value is irrelevant, so it is kept inside the tile).  P is read from
+// tensor memory, 8 columns (16 keys of bf16 pairs) per K = 16 step.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_smem,
                                          bool accumulate)
 {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
     constexpr uint32_t kVLbo = D == 128 ? kChunkBytes : 1024;
+    constexpr uint32_t hi = smem_desc_hi(1024);
+    const uint32_t b_lo = smem_desc_lo(v_smem, kVLbo);
+    const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_ts(tmem_d, tmem_p + kk * 8, smem_desc(v_smem + kk * 16 * 128, kVLbo, 1024), idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts_w(tmem_d, tmem_p + kk * 8, b_lo + ((kk * 16 * 128) >> 4), hi, idesc,
+                 kk > 0 ? 1u : acc0);
 }
 
 template <int D>
@@ -362,18 +372,16 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                 break;
             tc_fence_after();
             __syncwarp();
+            // The whole S row: four 32-column loads in flight, one wait.
+            uint32_t sraw[kBN / 32][32];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c)
+                tmem_ld32(t_s + c * 32, sraw[c]);
+            tmem_wait_ld();
             float s[kBN];
-            {
-                uint32_t raw[32];
 #pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    tmem_ld32(t_s + c * 32, raw);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        s[c * 32 + i] = __uint_as_float(raw[i]);
-                }
-            }
+            for (int i = 0; i < kBN; ++i)
+                s[i] = __uint_as_float(sraw[i / 32][i % 32]);
             // Mask (only on the diagonal tile and the ragged last tile; the
             // branch is uniform across the warp): keys above the diagonal
             // and keys past N get -inf, i.e. weight exactly 0.
@@ -387,13 +395,15 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                 for (int i = 0; i < kBN; ++i)
                     s[i] = i > limit ? -INFINITY : s[i];
             }
-            float mx0 = s[0], mx1 = s[1];
+            // Row max: four independent chains of 3-input max.
+            float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-            for (int i = 2; i < kBN; i += 4) {
-                mx0 = fmax3(mx0, s[i], s[i + 1]);
-                mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+            for (int i = 4; i < kBN; i += 8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
             }
-            const float cand = fmaxf(mx0, mx1) * p.sl2;
+            const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
             const float m_new = (j == 0 || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
             const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
             // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row
@@ -401,7 +411,9 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             // P V actually uses (to normalise O).
             const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
             const uint64_t negm = f2_pack(-m_new, -m_new);
-            uint64_t sum_exact = f2_pack(0.f, 0.f), sum_round = f2_pack(0.f, 0.f);
+            // Two independent packed accumulators per sum (four partials).
+            uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+            uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t pk[16];
@@ -412,17 +424,20 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                               x0, x1);
                     const float p0 = ex2(x0), p1 = ex2(x1);
                     pk[i] = pack_bf16x2(p0, p1);
-                    sum_exact = f2_add(sum_exact, f2_pack(p0, p1));
-                    sum_round = f2_add(sum_round, f2_pack(__uint_as_float(pk[i] << 16),
-                                                          __uint_as_float(pk[i] & 0xffff0000u)));
+                    sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
+                    sum_round[i & 1] =
+                        f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                         __uint_as_float(pk[i] & 0xffff0000u)));
                 }
                 tmem_st16(t_s + c * 16, pk);
             }
-            float e0, e1, r0, r1;
-            f2_unpack(sum_exact, e0, e1);
-            f2_unpack(sum_round, r0, r1);
-            l = l * alpha + (e0 + e1);
-            l_round = l_round * alpha + (r0 + r1);
+            float e0, e1, e2, e3, r0, r1, r2, r3;
+            f2_unpack(sum_exact[0], e0, e1);
+            f2_unpack(sum_exact[1], e2, e3);
+            f2_unpack(sum_round[0], r0, r1);
+            f2_unpack(sum_round[1], r2, r3);
+            l = l * alpha + ((e0 + e1) + (e2 + e3));
+            l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
             if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
