@@ -86,6 +86,8 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    float xmax[2][2 * kBM];  // row-half exchange (double-buffered): partial max / l_round
+    float xsum[2][2 * kBM];  // row-half exchange: partial l
 };
 
 struct Params {
@@ -146,12 +148,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 }
 
 // ------------------------------------------------------------------ producer
+// The producer and MMA roles run on a whole converged warp so that their
+// address and descriptor arithmetic stays warp-uniform; one elected lane
+// issues each TMA copy, MMA and commit.  Waits are done by every lane and
+// their outcome is made warp-uniform with a vote.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int *abort)
+{
+    const bool ok = mbar_wait(bar, parity, kWaitLimitNs, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <int D>
 __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUtensorMap *mq,
                          const CUtensorMap *mk, const CUtensorMap *mv)
 {
     using C = Cfg<D>;
     const volatile int *abort = &b.abort;
+    const bool leader = elect_one();
     uint32_t q_phase[2] = {0, 0};
     uint32_t pos = 0;  // K/V ring position (K_j, V_j alternate)
     bool ok = true;
@@ -166,15 +179,17 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
             if (!ok || u.nkv[t] == 0)
                 continue;
             const uint32_t full = smem_addr(&b.q_full[t]);
-            if (!mbar_wait(smem_addr(&b.q_empty[t]), q_phase[t] ^ 1, kWaitLimitNs, abort)) {
+            if (!warp_wait(smem_addr(&b.q_empty[t]), q_phase[t] ^ 1, abort)) {
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(full, C::kTileBytes);
-            const uint32_t dst = smem_base + t * C::kTileBytes;
+            if (leader) {
+                mbar_arrive_expect_tx(full, C::kTileBytes);
+                const uint32_t dst = smem_base + t * C::kTileBytes;
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(dst + c * kChunkBytes, mq, full, 64 * c, u.qt[t] * kBM, u.bh);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(dst + c * kChunkBytes, mq, full, 64 * c, u.qt[t] * kBM, u.bh);
+            }
             last_q_parity[t] = q_phase[t];
             q_phase[t] ^= 1;
         }
@@ -183,22 +198,25 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
             for (int which = 0; which < 2; ++which, ++pos) {
                 const uint32_t stage = pos % C::kStages;
                 const uint32_t phase = (pos / C::kStages) & 1;
-                if (!mbar_wait(smem_addr(&b.kv_empty[stage]), phase ^ 1, kWaitLimitNs, abort)) {
+                if (!warp_wait(smem_addr(&b.kv_empty[stage]), phase ^ 1, abort)) {
                     ok = false;
                     break;
                 }
-                const uint32_t full = smem_addr(&b.kv_full[stage]);
-                mbar_arrive_expect_tx(full, C::kTileBytes);
-                const uint32_t dst = smem_base + (2 + stage) * C::kTileBytes;
-                const CUtensorMap *m = which == 0 ? mk : mv;
+                if (leader) {
+                    const uint32_t full = smem_addr(&b.kv_full[stage]);
+                    mbar_arrive_expect_tx(full, C::kTileBytes);
+                    const uint32_t dst = smem_base + (2 + stage) * C::kTileBytes;
+                    const CUtensorMap *m = which == 0 ? mk : mv;
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(dst + c * kChunkBytes, m, full, 64 * c, j * kBN, u.bh);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(dst + c * kChunkBytes, m, full, 64 * c, j * kBN, u.bh);
+                }
             }
         }
     }
     if (!ok) {
-        record_failure(b, kRoleLoad);
+        if (leader)
+            record_failure(b, kRoleLoad);
         // Let the copies already issued land before the CTA exits.
         const uint32_t issued = pos;
         const uint32_t first = issued > (uint32_t)C::kStages ? issued - C::kStages : 0;
@@ -255,18 +273,20 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
 {
     using C = Cfg<D>;
     const volatile int *abort = &b.abort;
-    const uint32_t col_s[2] = {0, 128};
-    const uint32_t col_o[2] = {C::kColO0, C::kColO1};
+    const bool leader = elect_one();
     uint32_t q_phase[2] = {0, 0}, p_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
     uint32_t pos = 0;
     bool ok = true;
 
     auto kv_stage = [&](uint32_t at) { return at % C::kStages; };
     auto kv_wait = [&](uint32_t at) {
-        return mbar_wait(smem_addr(&b.kv_full[at % C::kStages]), (at / C::kStages) & 1,
-                         kWaitLimitNs, abort);
+        return warp_wait(smem_addr(&b.kv_full[at % C::kStages]), (at / C::kStages) & 1, abort);
     };
     auto kv_smem = [&](uint32_t at) { return smem_base + (2 + kv_stage(at)) * C::kTileBytes; };
+    auto commit = [&](uint64_t &bar) {
+        if (leader)
+            mma_commit(smem_addr(&bar));
+    };
 
     for (int r = 0; ok; ++r) {
         const int k = unit_index(r, blockIdx.x, gridDim.x);
@@ -276,7 +296,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
         const uint32_t base = pos;  // K_j at base + 2j, V_j at base + 2j + 1
         for (int t = 0; t < 2 && ok; ++t)
             if (u.nkv[t] > 0) {
-                ok = mbar_wait(smem_addr(&b.q_full[t]), q_phase[t], kWaitLimitNs, abort);
+                ok = warp_wait(smem_addr(&b.q_full[t]), q_phase[t], abort);
                 q_phase[t] ^= 1;
             }
         if (ok)
@@ -288,12 +308,14 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
         for (int t = 0; t < 2; ++t) {
             if (u.nkv[t] == 0)
                 continue;
-            issue_s<D>(tmem + col_s[t], smem_base + t * C::kTileBytes, kv_smem(base));
-            mma_commit(smem_addr(&b.s_full[t]));
+            if (leader)
+                issue_s<D>(tmem + (t == 0 ? 0u : 128u), smem_base + t * C::kTileBytes,
+                           kv_smem(base));
+            commit(b.s_full[t]);
             if (u.nkv[t] == 1)
-                mma_commit(smem_addr(&b.q_empty[t]));
+                commit(b.q_empty[t]);
         }
-        mma_commit(smem_addr(&b.kv_empty[kv_stage(base)]));
+        commit(b.kv_empty[kv_stage(base)]);
 
         // Key tiles 1..n-1: P V of the previous tile, then S of this one.
         for (int j = 1; j <= u.nkv_max && ok; ++j) {
@@ -306,192 +328,263 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
             for (int t = 0; t < 2 && ok; ++t) {
                 if (j - 1 >= u.nkv[t])
                     continue;  // tile t finished earlier (or is absent)
-                ok = mbar_wait(smem_addr(&b.p_full[t]), p_phase[t], kWaitLimitNs, abort);
+                ok = warp_wait(smem_addr(&b.p_full[t]), p_phase[t], abort);
                 p_phase[t] ^= 1;
                 if (ok && j - 1 == 0) {  // first P V of the unit overwrites O
-                    ok = mbar_wait(smem_addr(&b.o_empty[t]), oe_phase[t] ^ 1, kWaitLimitNs, abort);
+                    ok = warp_wait(smem_addr(&b.o_empty[t]), oe_phase[t] ^ 1, abort);
                     oe_phase[t] ^= 1;
                 }
                 if (!ok)
                     break;
                 tc_fence_after();
-                issue_pv<D>(tmem + col_o[t], tmem + col_s[t], kv_smem(at_v), j - 1 > 0);
+                const uint32_t col_s = t == 0 ? 0u : 128u;
+                const uint32_t col_o = t == 0 ? C::kColO0 : C::kColO1;
+                if (leader)
+                    issue_pv<D>(tmem + col_o, tmem + col_s, kv_smem(at_v), j - 1 > 0);
                 if (j < u.nkv[t]) {
-                    issue_s<D>(tmem + col_s[t], smem_base + t * C::kTileBytes, kv_smem(at_k));
-                    mma_commit(smem_addr(&b.s_full[t]));
+                    if (leader)
+                        issue_s<D>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
+                    commit(b.s_full[t]);
                     if (j == u.nkv[t] - 1)
-                        mma_commit(smem_addr(&b.q_empty[t]));
+                        commit(b.q_empty[t]);
                 } else {
-                    mma_commit(smem_addr(&b.o_full[t]));
+                    commit(b.o_full[t]);
                 }
             }
             if (!ok)
                 break;
-            mma_commit(smem_addr(&b.kv_empty[kv_stage(at_v)]));
+            commit(b.kv_empty[kv_stage(at_v)]);
             if (has_k)
-                mma_commit(smem_addr(&b.kv_empty[kv_stage(at_k)]));
+                commit(b.kv_empty[kv_stage(at_k)]);
         }
         pos = base + 2 * u.nkv_max;
     }
-    if (!ok)
+    if (!ok && leader)
         record_failure(b, kRoleMma);
-    // Wait until every MMA this thread issued has completed.
-    mma_commit(smem_addr(&b.drain));
+    // Wait until every MMA this warp issued has completed.
+    commit(b.drain);
     mbar_wait(smem_addr(&b.drain), 0, kWaitLimitNs, nullptr);
 }
 
 // ------------------------------------------------------------------ softmax
+// Both softmax warpgroups work on the same Q tile at a time (tile 0, then
+// tile 1, then tile 0 of the next key tile ...), so that two warps per SM
+// sub-partition share the latency-bound softmax of one tile.  Thread (h, r)
+// owns half h of row r: keys 64h..64h+63 of every key tile and O columns
+// [h*D/2, (h+1)*D/2).  The two halves of a row exchange their partial row
+// maxima through shared memory under a 64-thread named barrier (warps w and
+// w+4 hold the same rows), so both compute the same running max m; the row
+// sums stay per half until the epilogue adds them.
+
+// Running state of one row half for one Q tile.
+struct RowState {
+    float m, l, l_round;
+};
+
+__device__ __forceinline__ void pair_barrier(int wq)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + wq) : "memory");
+}
+
 template <int D>
-__device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
+__device__ __forceinline__ bool softmax_tile(const Params &p, Bars &b, uint32_t tmem, int t,
+                                             int j, int qt, int half, int wq, int lane,
+                                             RowState &st, uint32_t &s_phase, int &xbuf)
 {
     using C = Cfg<D>;
-    const volatile int *abort = &b.abort;
-    const int warp = (threadIdx.x / 32) & 3;
-    const int lane = threadIdx.x & 31;
-    const int r = warp * 32 + lane;                          // row within the Q tile
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    constexpr int kHalf = kBN / 2;  // keys per row half
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + (t == 0 ? 0u : 128u);
-    const uint32_t t_o = tmem + lane_off + (t == 0 ? C::kColO0 : C::kColO1);
-    uint32_t s_phase = 0, of_phase = 0;
-    bool ok = true;
+    const uint32_t t_o = tmem + lane_off + (t == 0 ? C::kColO0 : C::kColO1) + half * (D / 2);
 
+    if (!mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, &b.abort))
+        return false;
+    s_phase ^= 1;
+    tc_fence_after();
+    __syncwarp();
+    uint32_t sraw[kHalf / 32][32];
+#pragma unroll
+    for (int c = 0; c < kHalf / 32; ++c)
+        tmem_ld32(t_s + half * kHalf + c * 32, sraw[c]);
+    tmem_wait_ld();
+    float s[kHalf];
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i)
+        s[i] = __uint_as_float(sraw[i / 32][i % 32]);
+
+    // Mask (diagonal tile and ragged last tile only; uniform across the
+    // warp): keys above the diagonal and keys past N get -inf.
+    const bool diag = p.causal && j == qt;
+    const bool tail = (j + 1) * kBN > p.N;
+    if (diag || tail) {
+        int limit = diag ? r : kBN - 1;
+        if (tail)
+            limit = min(limit, p.N - 1 - j * kBN);
+        limit -= half * kHalf;  // in this half's key numbering (may be < 0)
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i)
+            s[i] = i > limit ? -INFINITY : s[i];
+    }
+    float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+    for (int i = 4; i < kHalf; i += 8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
+    }
+    float mhalf = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    // Exchange with the other half of the row.
+    // The barrier also orders this half's TMEM loads of S before the other
+    // half's stores of P into the same columns (P of keys 64..127 is written
+    // over S of keys 32..63).
+    float *x = b.xmax[xbuf];
+    x[half * kBM + r] = mhalf;
+    tc_fence_before();
+    pair_barrier(wq);
+    tc_fence_after();
+    const float mrow = fmaxf(mhalf, x[(1 - half) * kBM + r]);
+    xbuf ^= 1;
+
+    const float cand = mrow * p.sl2;
+    const float m_new = (j == 0 || cand > st.m + kRescaleLog2) ? fmaxf(st.m, cand) : st.m;
+    const float alpha = ex2(st.m - m_new);  // 0 on the first tile, 1 when m is kept
+    const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
+    const uint64_t negm = f2_pack(-m_new, -m_new);
+    uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+    uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+    for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm), x0,
+                      x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            pk[i] = pack_bf16x2(p0, p1);
+            sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
+            sum_round[i & 1] = f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                                __uint_as_float(pk[i] & 0xffff0000u)));
+        }
+        tmem_st16(t_s + half * (kHalf / 2) + c * 16, pk);
+    }
+    float e0, e1, e2, e3, r0, r1, r2, r3;
+    f2_unpack(sum_exact[0], e0, e1);
+    f2_unpack(sum_exact[1], e2, e3);
+    f2_unpack(sum_round[0], r0, r1);
+    f2_unpack(sum_round[1], r2, r3);
+    st.l = st.l * alpha + ((e0 + e1) + (e2 + e3));
+    st.l_round = st.l_round * alpha + ((r0 + r1) + (r2 + r3));
+    if (j > 0 && __any_sync(0xffffffffu, m_new != st.m)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(t_o + c * 32, o);
+        }
+    }
+    st.m = m_new;
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(smem_addr(&b.p_full[t]));
+    return true;
+}
+
+// Epilogue of one Q tile: O / l_round in bf16 (each half its D/2 columns),
+// lse = ln2 * (m + log2 l) from half 0.
+template <int D>
+__device__ __forceinline__ bool epilogue_tile(const Params &p, Bars &b, uint32_t tmem, int t,
+                                              int bh, int qt, int half, int wq, int lane,
+                                              const RowState &st, uint32_t &of_phase, int &xbuf)
+{
+    using C = Cfg<D>;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_o = tmem + lane_off + (t == 0 ? C::kColO0 : C::kColO1) + half * (D / 2);
+    // Combine the two halves' sums.
+    float *x = b.xmax[xbuf];
+    x[half * kBM + r] = st.l_round;
+    float *x2 = b.xsum[xbuf];
+    x2[half * kBM + r] = st.l;
+    pair_barrier(wq);
+    const float l_round = st.l_round + x[(1 - half) * kBM + r];
+    const float l = st.l + x2[(1 - half) * kBM + r];
+    xbuf ^= 1;
+
+    if (!mbar_wait(smem_addr(&b.o_full[t]), of_phase, kWaitLimitNs, &b.abort))
+        return false;
+    of_phase ^= 1;
+    tc_fence_after();
+    const float inv_l = 1.f / l_round;
+    const int row = qt * kBM + r;
+    const bool live = row < p.N;
+    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * p.N + row) * D + half * (D / 2);
+#pragma unroll 1
+    for (int c = 0; c < D / 64; ++c) {
+        uint32_t o[32];
+        __syncwarp();
+        tmem_ld32(t_o + c * 32, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (live) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+    }
+    if (live && half == 0)
+        p.lse[static_cast<size_t>(bh) * p.N + row] = (st.m + log2f(l)) * kLn2;
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(smem_addr(&b.o_empty[t]));
+    return true;
+}
+
+template <int D>
+__device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem)
+{
+    const int warp = threadIdx.x / 32;
+    const int half = warp >> 2;
+    const int wq = warp & 3;
+    const int lane = threadIdx.x & 31;
+    uint32_t s_phase[2] = {0, 0}, of_phase[2] = {0, 0};
+    int xbuf = 0;
+    bool ok = true;
     for (int rr = 0; ok; ++rr) {
         const int k = unit_index(rr, blockIdx.x, gridDim.x);
         if (k >= p.units)
             break;
         const Unit u = unit_at(p, k);
-        if (u.nkv[t] == 0)
-            continue;
-        const int qt = u.qt[t];
-        const int row = qt * kBM + r;
-        float m = -INFINITY, l = 0.f, l_round = 0.f;
-        for (int j = 0; j < u.nkv[t]; ++j) {
-            ok = mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, abort);
-            s_phase ^= 1;
-            if (!ok)
-                break;
-            tc_fence_after();
-            __syncwarp();
-            // The whole S row: four 32-column loads in flight, one wait.
-            uint32_t sraw[kBN / 32][32];
+        RowState st[2];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                tmem_ld32(t_s + c * 32, sraw[c]);
-            tmem_wait_ld();
-            float s[kBN];
+        for (int t = 0; t < 2; ++t)
+            st[t] = RowState{-INFINITY, 0.f, 0.f};
+        // Same order as the MMA issuer: S0(j), S1(j), S0(j+1), ...
+        for (int j = 0; ok && j < u.nkv_max; ++j) {
 #pragma unroll
-            for (int i = 0; i < kBN; ++i)
-                s[i] = __uint_as_float(sraw[i / 32][i % 32]);
-            // Mask (only on the diagonal tile and the ragged last tile; the
-            // branch is uniform across the warp): keys above the diagonal
-            // and keys past N get -inf, i.e. weight exactly 0.
-            const bool diag = p.causal && j == qt;
-            const bool tail = (j + 1) * kBN > p.N;
-            if (diag || tail) {
-                int limit = diag ? r : kBN - 1;
-                if (tail)
-                    limit = min(limit, p.N - 1 - j * kBN);
-#pragma unroll
-                for (int i = 0; i < kBN; ++i)
-                    s[i] = i > limit ? -INFINITY : s[i];
-            }
-            // Row max: four independent chains of 3-input max.
-            float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-            for (int i = 4; i < kBN; i += 8) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
-            }
-            const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
-            const float m_new = (j == 0 || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
-            const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
-            // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row
-            // sums: of the fp32 p (for lse) and of the bf16-rounded p that
-            // P V actually uses (to normalise O).
-            const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
-            const uint64_t negm = f2_pack(-m_new, -m_new);
-            // Two independent packed accumulators per sum (four partials).
-            uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-            uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm),
-                              x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    pk[i] = pack_bf16x2(p0, p1);
-                    sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
-                    sum_round[i & 1] =
-                        f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                         __uint_as_float(pk[i] & 0xffff0000u)));
-                }
-                tmem_st16(t_s + c * 16, pk);
-            }
-            float e0, e1, e2, e3, r0, r1, r2, r3;
-            f2_unpack(sum_exact[0], e0, e1);
-            f2_unpack(sum_exact[1], e2, e3);
-            f2_unpack(sum_round[0], r0, r1);
-            f2_unpack(sum_round[1], r2, r3);
-            l = l * alpha + ((e0 + e1) + (e2 + e3));
-            l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
-            if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(t_o + c * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(t_o + c * 32, o);
-                }
-            }
-            m = m_new;
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_addr(&b.p_full[t]));
+            for (int t = 0; t < 2; ++t)
+                if (ok && j < u.nkv[t])
+                    ok = softmax_tile<D>(p, b, tmem, t, j, u.qt[t], half, wq, lane, st[t],
+                                         s_phase[t], xbuf);
         }
-        if (!ok)
-            break;
-        // Epilogue: O / l in bf16, lse = ln2 * (m + log2 l).
-        ok = mbar_wait(smem_addr(&b.o_full[t]), of_phase, kWaitLimitNs, abort);
-        of_phase ^= 1;
-        if (!ok)
-            break;
-        tc_fence_after();
-        const float inv_l = 1.f / l_round;
-        const bool live = row < p.N;
-        __nv_bfloat16 *orow = p.o + (static_cast<size_t>(u.bh) * p.N + row) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            __syncwarp();
-            tmem_ld32(t_o + c * 32, o);
-            tmem_wait_ld();
-            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                    __uint_as_float(o[2 * i + 1]) * inv_l);
-            if (live) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
-        }
-        if (live)
-            p.lse[static_cast<size_t>(u.bh) * p.N + row] = (m + log2f(l)) * kLn2;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_addr(&b.o_empty[t]));
+        for (int t = 0; t < 2; ++t)
+            if (ok && u.nkv[t] > 0)
+                ok = epilogue_tile<D>(p, b, tmem, t, u.bh, u.qt[t], half, wq, lane, st[t],
+                                      of_phase[t], xbuf);
     }
     if (!ok)
         record_failure(b, kRoleSoftmax);
@@ -516,9 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&b.q_full[t]), 1);
             mbar_init(smem_addr(&b.q_empty[t]), 1);
             mbar_init(smem_addr(&b.s_full[t]), 1);
-            mbar_init(smem_addr(&b.p_full[t]), 4);
+            mbar_init(smem_addr(&b.p_full[t]), 8);
             mbar_init(smem_addr(&b.o_full[t]), 1);
-            mbar_init(smem_addr(&b.o_empty[t]), 4);
+            mbar_init(smem_addr(&b.o_empty[t]), 8);
         }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_addr(&b.kv_full[s]), 1);
@@ -543,13 +636,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = b.tmem_base;
 
     if (warp < 8) {
-        run_softmax<D>(p, b, tmem, warp / 4);
+        run_softmax<D>(p, b, tmem);
     } else if (warp == kWarpLoad) {
-        if (lane == 0)
-            run_load<D>(p, b, smem_base, &mq, &mk, &mv);
+        run_load<D>(p, b, smem_base, &mq, &mk, &mv);
     } else if (warp == kWarpMma) {
-        if (lane == 0)
-            run_mma<D>(p, b, smem_base, tmem);
+        run_mma<D>(p, b, smem_base, tmem);
     }
 
     tc_fence_before();
