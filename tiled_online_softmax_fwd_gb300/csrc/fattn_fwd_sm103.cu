@@ -11,8 +11,9 @@
 // GB300 design (one persistent CTA per SM, 320 threads):
 //   warp 8      TMA producer: Q tiles and a ring of K/V tiles in 128-byte
 //               swizzled shared memory, completion tracked by mbarriers.
-//   warp 9      MMA issuer (one thread): S = Q K^T and O += P V as tcgen05
-//               MMAs (bf16 in, fp32 accumulate) into tensor memory (TMEM).
+//   warp 9      MMA issuer: S = Q K^T and O += P V as tcgen05 MMAs (bf16 in,
+//               fp32 accumulate) into tensor memory (TMEM); the warp runs
+//               converged and one elected lane issues.
 //   warps 0-7   two softmax warpgroups, one per 128-row Q tile; they
 //               alternate (ping-pong) so that one computes exponentials
 //               while the tensor core works on the other tile.  Each thread
@@ -367,224 +368,157 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
 }
 
 // ------------------------------------------------------------------ softmax
-// Both softmax warpgroups work on the same Q tile at a time (tile 0, then
-// tile 1, then tile 0 of the next key tile ...), so that two warps per SM
-// sub-partition share the latency-bound softmax of one tile.  Thread (h, r)
-// owns half h of row r: keys 64h..64h+63 of every key tile and O columns
-// [h*D/2, (h+1)*D/2).  The two halves of a row exchange their partial row
-// maxima through shared memory under a 64-thread named barrier (warps w and
-// w+4 hold the same rows), so both compute the same running max m; the row
-// sums stay per half until the epilogue adds them.
-
-// Running state of one row half for one Q tile.
-struct RowState {
-    float m, l, l_round;
-};
-
-__device__ __forceinline__ void pair_barrier(int wq)
-{
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + wq) : "memory");
-}
-
 template <int D>
-__device__ __forceinline__ bool softmax_tile(const Params &p, Bars &b, uint32_t tmem, int t,
-                                             int j, int qt, int half, int wq, int lane,
-                                             RowState &st, uint32_t &s_phase, int &xbuf)
+__device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 {
     using C = Cfg<D>;
-    constexpr int kHalf = kBN / 2;  // keys per row half
-    const int r = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + (t == 0 ? 0u : 128u);
-    const uint32_t t_o = tmem + lane_off + (t == 0 ? C::kColO0 : C::kColO1) + half * (D / 2);
-
-    if (!mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, &b.abort))
-        return false;
-    s_phase ^= 1;
-    tc_fence_after();
-    __syncwarp();
-    uint32_t sraw[kHalf / 32][32];
-#pragma unroll
-    for (int c = 0; c < kHalf / 32; ++c)
-        tmem_ld32(t_s + half * kHalf + c * 32, sraw[c]);
-    tmem_wait_ld();
-    float s[kHalf];
-#pragma unroll
-    for (int i = 0; i < kHalf; ++i)
-        s[i] = __uint_as_float(sraw[i / 32][i % 32]);
-
-    // Mask (diagonal tile and ragged last tile only; uniform across the
-    // warp): keys above the diagonal and keys past N get -inf.
-    const bool diag = p.causal && j == qt;
-    const bool tail = (j + 1) * kBN > p.N;
-    if (diag || tail) {
-        int limit = diag ? r : kBN - 1;
-        if (tail)
-            limit = min(limit, p.N - 1 - j * kBN);
-        limit -= half * kHalf;  // in this half's key numbering (may be < 0)
-#pragma unroll
-        for (int i = 0; i < kHalf; ++i)
-            s[i] = i > limit ? -INFINITY : s[i];
-    }
-    float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-    for (int i = 4; i < kHalf; i += 8) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
-    }
-    float mhalf = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    // Exchange with the other half of the row.
-    // The barrier also orders this half's TMEM loads of S before the other
-    // half's stores of P into the same columns (P of keys 64..127 is written
-    // over S of keys 32..63).
-    float *x = b.xmax[xbuf];
-    x[half * kBM + r] = mhalf;
-    tc_fence_before();
-    pair_barrier(wq);
-    tc_fence_after();
-    const float mrow = fmaxf(mhalf, x[(1 - half) * kBM + r]);
-    xbuf ^= 1;
-
-    const float cand = mrow * p.sl2;
-    const float m_new = (j == 0 || cand > st.m + kRescaleLog2) ? fmaxf(st.m, cand) : st.m;
-    const float alpha = ex2(st.m - m_new);  // 0 on the first tile, 1 when m is kept
-    const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
-    const uint64_t negm = f2_pack(-m_new, -m_new);
-    uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-    uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-    for (int c = 0; c < kHalf / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm), x0,
-                      x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            pk[i] = pack_bf16x2(p0, p1);
-            sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
-            sum_round[i & 1] = f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                                __uint_as_float(pk[i] & 0xffff0000u)));
-        }
-        tmem_st16(t_s + half * (kHalf / 2) + c * 16, pk);
-    }
-    float e0, e1, e2, e3, r0, r1, r2, r3;
-    f2_unpack(sum_exact[0], e0, e1);
-    f2_unpack(sum_exact[1], e2, e3);
-    f2_unpack(sum_round[0], r0, r1);
-    f2_unpack(sum_round[1], r2, r3);
-    st.l = st.l * alpha + ((e0 + e1) + (e2 + e3));
-    st.l_round = st.l_round * alpha + ((r0 + r1) + (r2 + r3));
-    if (j > 0 && __any_sync(0xffffffffu, m_new != st.m)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(t_o + c * 32, o);
-        }
-    }
-    st.m = m_new;
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0)
-        mbar_arrive(smem_addr(&b.p_full[t]));
-    return true;
-}
-
-// Epilogue of one Q tile: O / l_round in bf16 (each half its D/2 columns),
-// lse = ln2 * (m + log2 l) from half 0.
-template <int D>
-__device__ __forceinline__ bool epilogue_tile(const Params &p, Bars &b, uint32_t tmem, int t,
-                                              int bh, int qt, int half, int wq, int lane,
-                                              const RowState &st, uint32_t &of_phase, int &xbuf)
-{
-    using C = Cfg<D>;
-    const int r = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t t_o = tmem + lane_off + (t == 0 ? C::kColO0 : C::kColO1) + half * (D / 2);
-    // Combine the two halves' sums.
-    float *x = b.xmax[xbuf];
-    x[half * kBM + r] = st.l_round;
-    float *x2 = b.xsum[xbuf];
-    x2[half * kBM + r] = st.l;
-    pair_barrier(wq);
-    const float l_round = st.l_round + x[(1 - half) * kBM + r];
-    const float l = st.l + x2[(1 - half) * kBM + r];
-    xbuf ^= 1;
-
-    if (!mbar_wait(smem_addr(&b.o_full[t]), of_phase, kWaitLimitNs, &b.abort))
-        return false;
-    of_phase ^= 1;
-    tc_fence_after();
-    const float inv_l = 1.f / l_round;
-    const int row = qt * kBM + r;
-    const bool live = row < p.N;
-    __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * p.N + row) * D + half * (D / 2);
-#pragma unroll 1
-    for (int c = 0; c < D / 64; ++c) {
-        uint32_t o[32];
-        __syncwarp();
-        tmem_ld32(t_o + c * 32, o);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (live) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
-    }
-    if (live && half == 0)
-        p.lse[static_cast<size_t>(bh) * p.N + row] = (st.m + log2f(l)) * kLn2;
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0)
-        mbar_arrive(smem_addr(&b.o_empty[t]));
-    return true;
-}
-
-template <int D>
-__device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem)
-{
-    const int warp = threadIdx.x / 32;
-    const int half = warp >> 2;
-    const int wq = warp & 3;
+    const volatile int *abort = &b.abort;
+    const int warp = (threadIdx.x / 32) & 3;
     const int lane = threadIdx.x & 31;
-    uint32_t s_phase[2] = {0, 0}, of_phase[2] = {0, 0};
-    int xbuf = 0;
+    const int r = warp * 32 + lane;                          // row within the Q tile
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + (t == 0 ? 0u : 128u);
+    const uint32_t t_o = tmem + lane_off + (t == 0 ? C::kColO0 : C::kColO1);
+    uint32_t s_phase = 0, of_phase = 0;
     bool ok = true;
+
     for (int rr = 0; ok; ++rr) {
         const int k = unit_index(rr, blockIdx.x, gridDim.x);
         if (k >= p.units)
             break;
         const Unit u = unit_at(p, k);
-        RowState st[2];
+        if (u.nkv[t] == 0)
+            continue;
+        const int qt = u.qt[t];
+        const int row = qt * kBM + r;
+        float m = -INFINITY, l = 0.f, l_round = 0.f;
+        for (int j = 0; j < u.nkv[t]; ++j) {
+            ok = mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, abort);
+            s_phase ^= 1;
+            if (!ok)
+                break;
+            tc_fence_after();
+            __syncwarp();
+            // The whole S row: four 32-column loads in flight, one wait.
+            uint32_t sraw[kBN / 32][32];
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-            st[t] = RowState{-INFINITY, 0.f, 0.f};
-        // Same order as the MMA issuer: S0(j), S1(j), S0(j+1), ...
-        for (int j = 0; ok && j < u.nkv_max; ++j) {
+            for (int c = 0; c < kBN / 32; ++c)
+                tmem_ld32(t_s + c * 32, sraw[c]);
+            tmem_wait_ld();
+            float s[kBN];
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
-                if (ok && j < u.nkv[t])
-                    ok = softmax_tile<D>(p, b, tmem, t, j, u.qt[t], half, wq, lane, st[t],
-                                         s_phase[t], xbuf);
+            for (int i = 0; i < kBN; ++i)
+                s[i] = __uint_as_float(sraw[i / 32][i % 32]);
+            // Mask (only on the diagonal tile and the ragged last tile; the
+            // branch is uniform across the warp): keys above the diagonal
+            // and keys past N get -inf, i.e. weight exactly 0.
+            const bool diag = p.causal && j == qt;
+            const bool tail = (j + 1) * kBN > p.N;
+            if (diag || tail) {
+                int limit = diag ? r : kBN - 1;
+                if (tail)
+                    limit = min(limit, p.N - 1 - j * kBN);
+#pragma unroll
+                for (int i = 0; i < kBN; ++i)
+                    s[i] = i > limit ? -INFINITY : s[i];
+            }
+            // Row max: four independent chains of 3-input max.
+            float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+            for (int i = 4; i < kBN; i += 8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
+            }
+            const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
+            const float m_new = (j == 0 || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
+            const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
+            // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row
+            // sums: of the fp32 p (for lse) and of the bf16-rounded p that
+            // P V actually uses (to normalise O).
+            const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
+            const uint64_t negm = f2_pack(-m_new, -m_new);
+            // Two independent packed accumulators per sum (four partials).
+            uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+            uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm),
+                              x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    pk[i] = pack_bf16x2(p0, p1);
+                    sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
+                    sum_round[i & 1] =
+                        f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                         __uint_as_float(pk[i] & 0xffff0000u)));
+                }
+                tmem_st16(t_s + c * 16, pk);
+            }
+            float e0, e1, e2, e3, r0, r1, r2, r3;
+            f2_unpack(sum_exact[0], e0, e1);
+            f2_unpack(sum_exact[1], e2, e3);
+            f2_unpack(sum_round[0], r0, r1);
+            f2_unpack(sum_round[1], r2, r3);
+            l = l * alpha + ((e0 + e1) + (e2 + e3));
+            l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
+            if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(t_o + c * 32, o);
+                }
+            }
+            m = m_new;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&b.p_full[t]));
         }
+        if (!ok)
+            break;
+        // Epilogue: O / l in bf16, lse = ln2 * (m + log2 l).
+        ok = mbar_wait(smem_addr(&b.o_full[t]), of_phase, kWaitLimitNs, abort);
+        of_phase ^= 1;
+        if (!ok)
+            break;
+        tc_fence_after();
+        const float inv_l = 1.f / l_round;
+        const bool live = row < p.N;
+        __nv_bfloat16 *orow = p.o + (static_cast<size_t>(u.bh) * p.N + row) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            __syncwarp();
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+            uint32_t pk[16];
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-            if (ok && u.nkv[t] > 0)
-                ok = epilogue_tile<D>(p, b, tmem, t, u.bh, u.qt[t], half, wq, lane, st[t],
-                                      of_phase[t], xbuf);
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (live) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+        if (live)
+            p.lse[static_cast<size_t>(u.bh) * p.N + row] = (m + log2f(l)) * kLn2;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&b.o_empty[t]));
     }
     if (!ok)
         record_failure(b, kRoleSoftmax);
@@ -609,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&b.q_full[t]), 1);
             mbar_init(smem_addr(&b.q_empty[t]), 1);
             mbar_init(smem_addr(&b.s_full[t]), 1);
-            mbar_init(smem_addr(&b.p_full[t]), 8);
+            mbar_init(smem_addr(&b.p_full[t]), 4);
             mbar_init(smem_addr(&b.o_full[t]), 1);
-            mbar_init(smem_addr(&b.o_empty[t]), 8);
+            mbar_init(smem_addr(&b.o_empty[t]), 4);
         }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_addr(&b.kv_full[s]), 1);
@@ -636,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = b.tmem_base;
 
     if (warp < 8) {
-        run_softmax<D>(p, b, tmem);
+        run_softmax<D>(p, b, tmem, warp / 4);
     } else if (warp == kWarpLoad) {
         run_load<D>(p, b, smem_base, &mq, &mk, &mv);
     } else if (warp == kWarpMma) {
