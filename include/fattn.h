@@ -118,11 +118,24 @@ int fattn_last_cuda_error(void);
  *
  * *status receives 0 when no kernel reported a problem since the last read,
  * otherwise a nonzero code: bits 0..7 = FATTN_ERR_TIMEOUT, bits 8..15 = the
- * role that gave up (1 load, 2 mma, 3 softmax, 4 epilogue), bits 16..31 = the
- * CTA index.  Returns FATTN_ERR_TIMEOUT if *status is nonzero, FATTN_OK if it
+ * role that gave up (1 load, 2 mma, 3 softmax, 4 epilogue, 5 self-test),
+ * bits 16..31 = the CTA index.  Returns FATTN_ERR_TIMEOUT if *status is nonzero, FATTN_OK if it
  * is zero, or FATTN_ERR_INVALID_ARG / FATTN_ERR_CUDA.
  */
 fattn_status_t fattn_get_device_status(int *status, struct CUstream_st *stream);
+
+/*
+ * fattn_selftest_wait_timeout -- exercise the failure path without a fault.
+ *
+ * Enqueues on `stream` a one-warp kernel that waits, with the same bounded
+ * wait the forward kernel's pipeline roles use, on a barrier that nothing
+ * ever signals.  After `limit_us` microseconds (1 .. 2,000,000) the wait gives
+ * up, the kernel records FATTN_ERR_TIMEOUT with role 5 in the device status
+ * word (see fattn_get_device_status) and returns; the CUDA context stays
+ * usable.  Returns FATTN_OK once enqueued, FATTN_ERR_INVALID_ARG for a limit
+ * out of range, FATTN_ERR_UNSUPPORTED / FATTN_ERR_CUDA for device problems.
+ */
+fattn_status_t fattn_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st *stream);
 
 /* Library version string, e.g. "libfattn 0.1.0 sm_103a". */
 const char *fattn_version(void);

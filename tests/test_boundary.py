@@ -121,3 +121,8 @@ def test_python_binding_checks(lib):
 
 def test_device_status_argument_check(lib):
     assert lib.fattn_get_device_status(ctypes.POINTER(ctypes.c_int)(), None) == INVALID
+
+
+def test_selftest_limit_is_checked_before_any_device_call(lib):
+    assert lib.fattn_selftest_wait_timeout(0, None) == INVALID
+    assert lib.fattn_selftest_wait_timeout(2000001, None) == INVALID

@@ -238,3 +238,18 @@ def test_rejects_host_pointer_for_device_buffer():
     st = fattn.raw_call("attn_fwd", hq.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(),
                         lse.data_ptr(), 1, 1, 64, 64, 0.125, 0, None)
     assert st == 1
+
+
+def test_stalled_wait_reports_timeout_and_context_survives():
+    """A pipeline wait that nothing satisfies gives up after its limit, records
+    FATTN_ERR_TIMEOUT (role 5) in the device status word, and the context stays
+    usable: a forward call afterwards is correct and leaves the word clear."""
+    assert fattn.device_status() == 0
+    fattn.selftest_wait_timeout(limit_us=20000)
+    torch.cuda.synchronize()
+    word = fattn.device_status()
+    assert word & 0xff == 4 and (word >> 8) & 0xff == 5, hex(word)
+    assert fattn.device_status() == 0  # reading clears it
+    q, k, v = make_qkv(1, 2, 300, 128, seed=41)
+    check_case("after_selftest", q, k, v, True, fattn.default_scale(128))
+    assert fattn.device_status() == 0

@@ -297,6 +297,20 @@ fattn_status_t fattn_get_device_status(int *status, struct CUstream_st *stream)
     return word == 0 ? FATTN_OK : FATTN_ERR_TIMEOUT;
 }
 
+fattn_status_t fattn_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st *stream)
+{
+    if (limit_us == 0 || limit_us > 2000000u)
+        return FATTN_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceInfo info;
+    fattn_status_t s = current_device(&dev, &info);
+    if (s != FATTN_OK)
+        return s;
+    const cudaError_t e =
+        fattn::launch_selftest_wait_timeout(static_cast<uint64_t>(limit_us) * 1000u, stream);
+    return e == cudaSuccess ? FATTN_OK : cuda_fail(e);
+}
+
 const char *fattn_version(void) { return "libfattn 0.1.0 sm_103a"; }
 
 }  // extern "C"

@@ -624,6 +624,37 @@ cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, int num_sms,
     return a.d == 64 ? launch<64>(a, maps, num_sms, stream) : launch<128>(a, maps, num_sms, stream);
 }
 
+namespace {
+
+// Self-test of the failure path: one warp waits on an mbarrier that nothing
+// ever arrives on, with the same bounded wait as the pipeline roles; when the
+// limit passes it records a timeout in the status word and returns.
+__global__ void selftest_wait_timeout_kernel(uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(smem_addr(&bar), 0, limit_ns, &abort_flag);
+    if (!ok && threadIdx.x == 0) {
+        const uint32_t code = 4u | (static_cast<uint32_t>(kRoleSelfTest) << 8) |
+                              ((blockIdx.x & 0xffffu) << 16);
+        atomicCAS(&g_fattn_status, 0u, code);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream)
+{
+    selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_status(uint32_t *out, cudaStream_t stream)
 {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fattn_status, sizeof(uint32_t), 0,

@@ -26,11 +26,19 @@ struct FwdMaps {
 };
 
 // Device status word codes (see fattn_get_device_status in fattn.h).
-enum DeviceRole : uint32_t { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleEpilogue = 4 };
+enum DeviceRole : uint32_t {
+    kRoleLoad = 1,
+    kRoleMma = 2,
+    kRoleSoftmax = 3,
+    kRoleEpilogue = 4,
+    kRoleSelfTest = 5
+};
 
 // tcgen05 / TMA kernel: one persistent CTA per SM.
 cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, int num_sms,
                              cudaStream_t stream);
+// Failure-path self-test: a wait that nothing satisfies, limited to limit_ns.
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 // Reads (and clears) the device status word of the current device.
 cudaError_t read_and_clear_status(uint32_t *out, cudaStream_t stream);
 

@@ -22,7 +22,8 @@ FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
                 3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
 EXPORTED = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "fattn_status_string",
-            "fattn_last_cuda_error", "fattn_get_device_status", "fattn_version"]
+            "fattn_last_cuda_error", "fattn_get_device_status", "fattn_selftest_wait_timeout",
+            "fattn_version"]
 
 _lib = None
 _lock = threading.Lock()
@@ -70,6 +71,8 @@ def load():
         lib.fattn_last_cuda_error.argtypes = []
         lib.fattn_get_device_status.restype = ctypes.c_int
         lib.fattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
+        lib.fattn_selftest_wait_timeout.restype = ctypes.c_int
+        lib.fattn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
         lib.fattn_version.restype = ctypes.c_char_p
         lib.fattn_version.argtypes = []
         _lib = lib
@@ -190,6 +193,16 @@ def device_status(stream=None, device=None) -> int:
     if st not in (FATTN_OK, 4):
         _check(st, "fattn_get_device_status")
     return word.value
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None, device=None):
+    """Launch the failure-path self-test (a wait nothing satisfies, bounded by
+    limit_us); read the result with device_status() after it completes."""
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        st = lib.fattn_selftest_wait_timeout(int(limit_us), _stream_handle(stream, dev))
+    _check(st, "fattn_selftest_wait_timeout")
 
 
 def version() -> str:
