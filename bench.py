@@ -240,9 +240,20 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     big = w.io_bytes > L2_BYTES
     flush = None if big else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    # Key-range split when the library recommends it (few work units per SM).
+    splits = 1 if args.split == "off" else fattn.split_count(w.B, w.H, w.N, w.d, w.causal, dev)
+    ws = None
+    if splits > 1:
+        ws = torch.empty(fattn.split_workspace_size(w.B, w.H, w.N, w.d, splits), dtype=torch.uint8,
+                         device=dev)
 
     def step():
-        fattn.attn_fwd(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, lse=dl, stream=stream)
+        if splits > 1:
+            fattn.attn_fwd_split(dq, dk, dv, causal=w.causal, scale=w.scale, num_splits=splits,
+                                 workspace=ws, out=do, lse=dl, stream=stream)
+        else:
+            fattn.attn_fwd(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, lse=dl,
+                           stream=stream)
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -313,6 +324,7 @@ def run_gpu(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, **w.describe(), "parallelism": "replicas" if world > 1 else "single",
+                   "splits": splits,
                    "l2": ("inputs larger than L2 (%d MB)" % (w.io_bytes // 10**6)) if big
                          else "L2 flushed (256 MiB write) before every step, outside the timed events",
                    "input_digest": in_digest},
@@ -322,8 +334,10 @@ def run_gpu(args, world, rank, local):
                      "traffic_source": traffic_src,
                      "algorithmic_flops_per_launch": w.flops,
                      "algorithmic_bytes_per_launch": w.io_bytes},
-        "gpu_launches": args.steps,
-        "kernel": "fattn fwd_kernel<%d> (tcgen05/TMA, persistent)" % w.d,
+        "gpu_launches": args.steps * (2 if splits > 1 else 1),
+        "kernel": "fattn fwd_kernel<%d> (tcgen05/TMA, persistent)%s" % (
+            w.d, " + combine_kernel, %d key-range splits; roofline.achieved uses the whole step" % splits
+            if splits > 1 else ""),
         "wall_ms_per_step": wall_ms,
         "clocks": clocks.summary(),
         "device_status": status,
@@ -348,6 +362,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--split", default="auto", choices=["auto", "off"],
+                    help="key-range split when the library recommends one (auto) or never")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

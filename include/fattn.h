@@ -42,6 +42,8 @@
 #ifndef FATTN_H
 #define FATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -94,6 +96,37 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
                              void *dq, void *dk, void *dv, void *do_, float *dlse,
                              int B, int H, int N, int d, float scale, int causal,
                              struct CUstream_st *stream);
+
+/*
+ * Key-range split (split-KV).  When B*H*ceil(N/256) work units are fewer
+ * than the device's SMs (few heads, or one long sequence), attn_fwd leaves
+ * most SMs idle.  attn_fwd_split divides the keys of every pair of 128-row
+ * query tiles into num_splits contiguous ranges processed by different CTAs,
+ * each producing a partial output and partial log-sum-exp, and a second
+ * kernel merges them exactly: lse = log(sum_s exp(lse_s)) and
+ * O = sum_s exp(lse_s - lse) O_s -- the blocked softmax statistics merge
+ * ("OpenAI Triton: from introduction to model practice", section 1.1,
+ * example 3: per-block max and sum combined into the global max and sum).
+ *
+ * attn_fwd_split_count: the number of splits the library would use on the
+ *   current device for this shape (1 = no split helps), or 0 on invalid
+ *   arguments / no usable device.
+ * attn_fwd_split_workspace_size: bytes of device scratch attn_fwd_split
+ *   needs for num_splits (0 when num_splits == 1 or on invalid arguments):
+ *   num_splits * B*H*N * (4*d + 8) bytes plus alignment.
+ * attn_fwd_split: attn_fwd's arguments and contract, plus num_splits
+ *   (1..64; 1 is exactly attn_fwd and ignores the workspace) and the
+ *   caller-owned device workspace (16-byte aligned, at least the size above,
+ *   not overlapping q, k, v, o, lse; its contents on entry are ignored and on
+ *   exit are undefined).  Two kernels are enqueued on `stream`; calls that
+ *   share one workspace must not overlap on the device.
+ */
+int attn_fwd_split_count(int B, int H, int N, int d, int causal);
+size_t attn_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits);
+fattn_status_t attn_fwd_split(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int H, int N, int d, float scale, int causal, int num_splits,
+                              void *workspace, size_t workspace_bytes,
+                              struct CUstream_st *stream);
 
 /*
  * attn_fwd_simt -- the same operation and contract as attn_fwd, computed by a

@@ -126,3 +126,24 @@ def test_device_status_argument_check(lib):
 def test_selftest_limit_is_checked_before_any_device_call(lib):
     assert lib.fattn_selftest_wait_timeout(0, None) == INVALID
     assert lib.fattn_selftest_wait_timeout(2000001, None) == INVALID
+
+
+def test_split_workspace_size(lib):
+    f = lib.attn_fwd_split_workspace_size
+    f.restype = ctypes.c_size_t
+    assert f(1, 1, 4096, 64, 1) == 0                  # no split, no scratch
+    rows = 4096
+    o_bytes = 10 * rows * 64 * 4
+    aligned = (o_bytes + 255) // 256 * 256
+    assert f(1, 1, 4096, 64, 10) == aligned + 10 * rows * 8
+    assert f(1, 1, 4096, 96, 2) == 0 and f(1, 1, 4096, 64, 0) == 0 and f(1, 1, 4096, 64, 65) == 0
+
+
+def test_split_arguments_are_checked(lib):
+    f = lib.attn_fwd_split
+    base = [A, A + (1 << 24), A + (2 << 24), A + (3 << 24), A + (4 << 24), 1, 1, 4096, 64, 0.125, 0]
+    ws = A + (8 << 24)
+    assert f(*base, 0, ws, 1 << 30, None) == INVALID       # num_splits out of range
+    assert f(*base, 65, ws, 1 << 30, None) == INVALID
+    assert f(*base[:5], 1, 1, 4096, 80, 0.125, 0, 4, ws, 1 << 30, None) == UNSUPPORTED
+    assert f(*base[:5], 1, 1, 0, 64, 0.125, 0, 4, 0, 0, None) == OK   # empty: no-op

@@ -253,3 +253,49 @@ def test_stalled_wait_reports_timeout_and_context_survives():
     q, k, v = make_qkv(1, 2, 300, 128, seed=41)
     check_case("after_selftest", q, k, v, True, fattn.default_scale(128))
     assert fattn.device_status() == 0
+
+
+# ----------------------------------------------------------------- key-range split
+SPLIT_CASES = [(1, 1, 4096, 64, False, None), (1, 1, 4096, 64, True, None),
+               (1, 2, 1000, 128, True, 3), (2, 1, 777, 64, False, 5),
+               (1, 1, 300, 128, True, 2), (1, 3, 2048, 128, False, 16),
+               (1, 1, 128, 64, False, 2), (1, 1, 4096, 128, True, 7), (3, 2, 513, 64, True, 64)]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,splits", SPLIT_CASES,
+                         ids=["B%dH%dN%dd%d%s_s%s" % (b, h, n, d, "c" if c else "", s)
+                              for b, h, n, d, c, s in SPLIT_CASES])
+def test_split_matches_oracle(B, H, N, d, causal, splits):
+    """Key-range split + combine against the oracle (and close to the
+    unsplit kernel)."""
+    q, k, v = make_qkv(B, H, N, d, seed=500 + N + d, sigma_qk=2.0)
+    scale = fattn.default_scale(d)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fattn.attn_fwd_split(dq, dk, dv, causal=causal, scale=scale, num_splits=splits)
+    o1, l1 = fattn.attn_fwd(dq, dk, dv, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    r = compare(o.cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref, mean_rule="floor")
+    report("split_B%dH%dN%dd%d_c%d_s%s" % (B, H, N, d, causal, splits), r)
+    assert_parity(r, "split")
+    assert (o.float() - o1.float()).abs().max().item() <= 2 ** -5
+    assert (lse - l1).abs().max().item() <= 1e-4
+
+
+def test_split_count_fills_the_device():
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    s = fattn.split_count(1, 1, 4096, 64, False)
+    assert 1 < s <= 16 and 16 * s >= min(n_sm, 16 * 16)
+    assert fattn.split_count(1, 32, 16384, 128, True) == 1   # already more units than SMs
+
+
+def test_split_workload_single_head():
+    """The single-head N=4096 workload through the automatic split."""
+    w = WORKLOADS["B1_H1_N4096_d64"]
+    q, k, v, _ = make_workload(w)
+    o, lse = fattn.attn_fwd_split(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.scale, w.causal)
+    r = compare(o.cpu().reshape(-1, w.d), lse.cpu().reshape(-1), o_ref, lse_ref)
+    report("split_workload_" + w.name, r)
+    assert_parity(r, w.name)

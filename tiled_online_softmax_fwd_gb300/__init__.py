@@ -5,8 +5,8 @@ sm_103a; this package only marshals arguments to its C ABI (``fattn.py``).
 Importing the package does not load the library: the first call does, and it
 raises if the library has not been built (there is no CPU fallback).
 """
-__all__ = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "FattnError", "device_status",
-           "library_path", "version"]
+__all__ = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "attn_fwd_split", "split_count",
+           "split_workspace_size", "FattnError", "device_status", "library_path", "version"]
 
 
 def __getattr__(name):

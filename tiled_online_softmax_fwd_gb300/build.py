@@ -24,7 +24,7 @@ LIB = os.path.join(BUILD, "libfattn.so")
 
 SOURCES = ["fattn_api.cu", "fattn_fwd_sm103.cu", "fattn_fwd_simt.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
-EXPORTS = "{ global: attn_fwd; attn_fwd_host; attn_fwd_simt; fattn_*; local: *; };\n"
+EXPORTS = "{ global: attn_fwd*; fattn_*; local: *; };\n"
 
 
 def nvcc() -> str:

@@ -184,10 +184,12 @@ fattn_status_t validate(const void *q, const void *k, const void *v, const void 
     return FATTN_OK;
 }
 
-// Enqueue one validated forward call.
+// Enqueue one validated forward call (split.splits > 1: key-range split with
+// the caller's scratch).
 fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const void *k,
                       const void *v, void *o, float *lse, int B, int H, int N, int d, float scale,
-                      int causal, cudaStream_t stream)
+                      int causal, cudaStream_t stream,
+                      const fattn::FwdSplit &split = fattn::FwdSplit{1, nullptr, nullptr})
 {
     fattn::FwdArgs a{q, k, v, o, lse, B, H, N, d, scale, causal};
     cudaError_t e;
@@ -204,7 +206,7 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
             (s = make_map(encode, &maps.k, k, N, d, BH)) != FATTN_OK ||
             (s = make_map(encode, &maps.v, v, N, d, BH)) != FATTN_OK)
             return s;
-        e = fattn::launch_fwd_sm103(a, maps, info.num_sms, stream);
+        e = fattn::launch_fwd_sm103(a, maps, split, info.num_sms, stream);
     }
     return e == cudaSuccess ? FATTN_OK : cuda_fail(e);
 }
@@ -222,6 +224,72 @@ fattn_status_t forward(Kernel which, const void *q, const void *k, const void *v
     return launch(which, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
 }
 
+constexpr int kMaxSplits = 64;
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Scratch layout of a split call: fp32 partial O, then (256-byte aligned) the
+// base-2 partial lse pairs.
+size_t split_ws_o_bytes(int B, int H, int N, int d, int splits)
+{
+    return static_cast<size_t>(splits) * B * H * N * d * sizeof(float);
+}
+size_t split_ws_bytes(int B, int H, int N, int d, int splits)
+{
+    if (splits <= 1)
+        return 0;
+    return align_up(split_ws_o_bytes(B, H, N, d, splits), kWsAlign) +
+           static_cast<size_t>(splits) * B * H * N * 2 * sizeof(float);
+}
+
+// Splits that fill the device: ceil(#SMs / units) for a grid of fewer work
+// units than SMs, at most one split per two key tiles and at most 16.
+int choose_splits(int B, int H, int N, int num_sms)
+{
+    const long long pairs = ((static_cast<long long>(N) + 127) / 128 + 1) / 2;
+    const long long units = static_cast<long long>(B) * H * pairs;
+    const long long key_tiles = (static_cast<long long>(N) + 127) / 128;
+    if (units <= 0 || units >= num_sms)
+        return 1;
+    long long s = (num_sms + units - 1) / units;
+    s = s > 16 ? 16 : s;
+    s = s > key_tiles / 2 ? key_tiles / 2 : s;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+fattn_status_t forward_split(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float scale, int causal, int num_splits,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (num_splits < 1 || num_splits > kMaxSplits)
+        return FATTN_ERR_INVALID_ARG;
+    bool empty = false;
+    int dev = 0;
+    DeviceInfo info;
+    fattn_status_t s = validate(q, k, v, o, lse, B, H, N, d, scale, causal, &empty, &dev, &info);
+    if (s != FATTN_OK || empty)
+        return s;
+    if (num_splits == 1)
+        return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+    const size_t need = split_ws_bytes(B, H, N, d, num_splits);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return FATTN_ERR_INVALID_ARG;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    const size_t tb = rows * d * 2, lb = rows * 4;
+    if (overlap(workspace, need, q, tb) || overlap(workspace, need, k, tb) ||
+        overlap(workspace, need, v, tb) || overlap(workspace, need, o, tb) ||
+        overlap(workspace, need, lse, lb))
+        return FATTN_ERR_INVALID_ARG;
+    if ((s = check_device_buffer(workspace, dev)) != FATTN_OK)
+        return s;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const fattn::FwdSplit split{
+        num_splits, reinterpret_cast<float *>(ws),
+        reinterpret_cast<float *>(ws + align_up(split_ws_o_bytes(B, H, N, d, num_splits), kWsAlign))};
+    return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream, split);
+}
+
 }  // namespace
 
 extern "C" {
@@ -230,6 +298,37 @@ fattn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, fl
                         int H, int N, int d, float scale, int causal, struct CUstream_st *stream)
 {
     return forward(Kernel::kTcgen05, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+int attn_fwd_split_count(int B, int H, int N, int d, int causal)
+{
+    bool empty = false;
+    if (check_shape(B, H, N, d, 1.0f, causal, &empty) != FATTN_OK)
+        return 0;
+    if (empty)
+        return 1;
+    int dev = 0;
+    DeviceInfo info;
+    if (current_device(&dev, &info) != FATTN_OK)
+        return 0;
+    return choose_splits(B, H, N, info.num_sms);
+}
+
+size_t attn_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits)
+{
+    bool empty = false;
+    if (num_splits < 1 || num_splits > kMaxSplits ||
+        check_shape(B, H, N, d, 1.0f, 0, &empty) != FATTN_OK || empty)
+        return 0;
+    return split_ws_bytes(B, H, N, d, num_splits);
+}
+
+fattn_status_t attn_fwd_split(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int H, int N, int d, float scale, int causal, int num_splits,
+                              void *workspace, size_t workspace_bytes, struct CUstream_st *stream)
+{
+    return forward_split(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
+                         workspace_bytes, stream);
 }
 
 fattn_status_t attn_fwd_simt(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -94,37 +94,58 @@ struct Bars {
 struct Params {
     __nv_bfloat16 *o;
     float *lse;
-    int N;      // sequence length
-    int BH;     // batch * heads
-    int QT;     // query tiles per head = ceil(N / 128)
-    int KT;     // key tiles per head
-    int pairs;  // work units per head = ceil(QT / 2)
-    int units;  // BH * pairs
+    float *ws_o;   // split mode: fp32 partial O [splits][B*H*N][D]
+    float2 *ws_l;  // split mode: base-2 partial lse (exact sum, rounded sum) [splits][B*H*N]
+    int N;         // sequence length
+    int BH;        // batch * heads
+    int QT;        // query tiles per head = ceil(N / 128)
+    int KT;        // key tiles per head
+    int pairs;     // Q-tile pairs per head = ceil(QT / 2)
+    int splits;    // key-range splits per pair (1: no split, results go to o / lse)
+    int units;     // BH * pairs * splits
     int causal;
-    float sl2;  // scale * log2(e)
+    float sl2;     // scale * log2(e)
 };
 
+// A work unit: Q tiles qt[0], qt[1] of head bh, over key tiles [j0, j1[t]).
 struct Unit {
     int bh;
+    int split;
     int qt[2];
-    int nkv[2];  // key tiles visited by each Q tile (0: tile absent)
-    int nkv_max;
+    int j0;
+    int j1[2];  // j1[t] <= j0: tile t has no work in this unit
+    int n[2];   // key tiles of tile t: j1[t] - j0 (or 0)
+    int n_max;
 };
 
+// Key tiles visited by Q tile qt over the whole key range (0 past the end).
+__device__ __forceinline__ int key_tiles(const Params &p, int qt)
+{
+    if (qt >= p.QT)
+        return 0;
+    return p.causal ? min(qt + 1, p.KT) : p.KT;
+}
+
+// The split s of a pair covers key tiles [s*F/S, (s+1)*F/S) of the pair's
+// F = max over its two tiles; the combine kernel uses the same ranges.
 __device__ __forceinline__ Unit unit_at(const Params &p, int k)
 {
     Unit u;
-    const int pair = p.pairs - 1 - k / p.BH;  // heaviest pairs first
-    u.bh = k % p.BH;
+    u.split = k % p.splits;
+    const int rest = k / p.splits;
+    const int pair = p.pairs - 1 - rest / p.BH;  // heaviest pairs first
+    u.bh = rest % p.BH;
+    const int full0 = key_tiles(p, 2 * pair), full1 = key_tiles(p, 2 * pair + 1);
+    const int fmax = max(full0, full1);
+    u.j0 = u.split * fmax / p.splits;
+    const int je = (u.split + 1) * fmax / p.splits;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         u.qt[t] = 2 * pair + t;
-        if (u.qt[t] >= p.QT)
-            u.nkv[t] = 0;
-        else
-            u.nkv[t] = p.causal ? min(u.qt[t] + 1, p.KT) : p.KT;
+        u.j1[t] = min(je, t == 0 ? full0 : full1);
+        u.n[t] = max(u.j1[t] - u.j0, 0);
     }
-    u.nkv_max = max(u.nkv[0], u.nkv[1]);
+    u.n_max = max(u.n[0], u.n[1]);
     return u;
 }
 
@@ -177,7 +198,7 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
         const Unit u = unit_at(p, k);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-            if (!ok || u.nkv[t] == 0)
+            if (!ok || u.n[t] == 0)
                 continue;
             const uint32_t full = smem_addr(&b.q_full[t]);
             if (!warp_wait(smem_addr(&b.q_empty[t]), q_phase[t] ^ 1, abort)) {
@@ -194,7 +215,7 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
             last_q_parity[t] = q_phase[t];
             q_phase[t] ^= 1;
         }
-        for (int j = 0; ok && j < u.nkv_max; ++j) {
+        for (int j = u.j0; ok && j < u.j0 + u.n_max; ++j) {
 #pragma unroll
             for (int which = 0; which < 2; ++which, ++pos) {
                 const uint32_t stage = pos % C::kStages;
@@ -294,9 +315,11 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
         if (k >= p.units)
             break;
         const Unit u = unit_at(p, k);
-        const uint32_t base = pos;  // K_j at base + 2j, V_j at base + 2j + 1
+        const uint32_t base = pos;  // K_(j0+i) at base + 2i, V_(j0+i) at base + 2i + 1
+        if (u.n_max == 0)
+            continue;
         for (int t = 0; t < 2 && ok; ++t)
-            if (u.nkv[t] > 0) {
+            if (u.n[t] > 0) {
                 ok = warp_wait(smem_addr(&b.q_full[t]), q_phase[t], abort);
                 q_phase[t] ^= 1;
             }
@@ -305,29 +328,30 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
         if (!ok)
             break;
         tc_fence_after();
-        // Key tile 0: S for both Q tiles.
+        // First key tile: S for both Q tiles.
         for (int t = 0; t < 2; ++t) {
-            if (u.nkv[t] == 0)
+            if (u.n[t] == 0)
                 continue;
             if (leader)
                 issue_s<D>(tmem + (t == 0 ? 0u : 128u), smem_base + t * C::kTileBytes,
                            kv_smem(base));
             commit(b.s_full[t]);
-            if (u.nkv[t] == 1)
+            if (u.n[t] == 1)
                 commit(b.q_empty[t]);
         }
         commit(b.kv_empty[kv_stage(base)]);
 
-        // Key tiles 1..n-1: P V of the previous tile, then S of this one.
-        for (int j = 1; j <= u.nkv_max && ok; ++j) {
+        // Key tiles 1..n-1 of the unit: P V of the previous tile, then S of
+        // this one (j counts key tiles from j0).
+        for (int j = 1; j <= u.n_max && ok; ++j) {
             const uint32_t at_v = base + 2 * (j - 1) + 1;
             const uint32_t at_k = base + 2 * j;
-            const bool has_k = j < u.nkv_max;
+            const bool has_k = j < u.n_max;
             ok = kv_wait(at_v) && (!has_k || kv_wait(at_k));
             if (!ok)
                 break;
             for (int t = 0; t < 2 && ok; ++t) {
-                if (j - 1 >= u.nkv[t])
+                if (j - 1 >= u.n[t])
                     continue;  // tile t finished earlier (or is absent)
                 ok = warp_wait(smem_addr(&b.p_full[t]), p_phase[t], abort);
                 p_phase[t] ^= 1;
@@ -342,11 +366,11 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
                 const uint32_t col_o = t == 0 ? C::kColO0 : C::kColO1;
                 if (leader)
                     issue_pv<D>(tmem + col_o, tmem + col_s, kv_smem(at_v), j - 1 > 0);
-                if (j < u.nkv[t]) {
+                if (j < u.n[t]) {
                     if (leader)
                         issue_s<D>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
                     commit(b.s_full[t]);
-                    if (j == u.nkv[t] - 1)
+                    if (j == u.n[t] - 1)
                         commit(b.q_empty[t]);
                 } else {
                     commit(b.o_full[t]);
@@ -358,7 +382,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
             if (has_k)
                 commit(b.kv_empty[kv_stage(at_k)]);
         }
-        pos = base + 2 * u.nkv_max;
+        pos = base + 2 * u.n_max;
     }
     if (!ok && leader)
         record_failure(b, kRoleMma);
@@ -387,12 +411,13 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         if (k >= p.units)
             break;
         const Unit u = unit_at(p, k);
-        if (u.nkv[t] == 0)
+        if (u.n[t] == 0)
             continue;
         const int qt = u.qt[t];
         const int row = qt * kBM + r;
         float m = -INFINITY, l = 0.f, l_round = 0.f;
-        for (int j = 0; j < u.nkv[t]; ++j) {
+        for (int j = u.j0; j < u.j1[t]; ++j) {
+            const bool first = j == u.j0;
             ok = mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, abort);
             s_phase ^= 1;
             if (!ok)
@@ -431,7 +456,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                     mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
             }
             const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
-            const float m_new = (j == 0 || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
+            const float m_new = (first || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
             const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
             // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row
             // sums: of the fp32 p (for lse) and of the bf16-rounded p that
@@ -465,7 +490,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             f2_unpack(sum_round[1], r2, r3);
             l = l * alpha + ((e0 + e1) + (e2 + e3));
             l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
-            if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+            if (!first && __any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -486,7 +511,9 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         }
         if (!ok)
             break;
-        // Epilogue: O / l in bf16, lse = ln2 * (m + log2 l).
+        // Epilogue: O / l_round in bf16 and lse = ln2 * (m + log2 l); in
+        // split mode the fp32 partial O and the two base-2 partial lse go to
+        // the workspace instead, for the combine kernel.
         ok = mbar_wait(smem_addr(&b.o_full[t]), of_phase, kWaitLimitNs, abort);
         of_phase ^= 1;
         if (!ok)
@@ -494,27 +521,51 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         tc_fence_after();
         const float inv_l = 1.f / l_round;
         const bool live = row < p.N;
-        __nv_bfloat16 *orow = p.o + (static_cast<size_t>(u.bh) * p.N + row) * D;
+        const size_t grow = static_cast<size_t>(u.bh) * p.N + row;
+        if (p.splits == 1) {
+            __nv_bfloat16 *orow = p.o + grow * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            __syncwarp();
-            tmem_ld32(t_o + c * 32, o);
-            tmem_wait_ld();
-            uint32_t pk[16];
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(t_o + c * 32, o);
+                tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                    __uint_as_float(o[2 * i + 1]) * inv_l);
-            if (live) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                        __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (live) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
             }
+            if (live)
+                p.lse[grow] = (m + log2f(l)) * kLn2;
+        } else {
+            const size_t srow = static_cast<size_t>(u.split) * p.BH * p.N + grow;
+            float *orow = p.ws_o + srow * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(t_o + c * 32, o);
+                tmem_wait_ld();
+                if (live) {
+                    float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l,
+                                             __uint_as_float(o[4 * i + 1]) * inv_l,
+                                             __uint_as_float(o[4 * i + 2]) * inv_l,
+                                             __uint_as_float(o[4 * i + 3]) * inv_l);
+                }
+            }
+            if (live)
+                p.ws_l[srow] = make_float2(m + log2f(l), m + log2f(l_round));
         }
-        if (live)
-            p.lse[static_cast<size_t>(u.bh) * p.N + row] = (m + log2f(l)) * kLn2;
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -586,19 +637,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ combine
+// Merge of the key-range splits of each row (the blocked softmax statistics
+// merge: per-block maxima and sums combined into the global ones).  With
+// base-2 partial log-sum-exps le_s (exact sums) and lr_s (rounded sums) and
+// partial outputs O_s = acc_s / l_round_s:
+//   lse = ln2 * log2(sum_s 2^le_s)
+//   O   = sum_s w_s O_s,  w_s = 2^lr_s / sum_s' 2^lr_s'
+// Splits with no key tile for the row's Q tile are skipped (the same ranges
+// as unit_at).  One warp per row; lane l owns D/32 consecutive columns.
 template <int D>
-cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, int num_sms, cudaStream_t stream)
+__global__ void __launch_bounds__(256)
+    combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_l, const Params p)
+{
+    constexpr int kCols = D / 32;
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+    const long long rows = static_cast<long long>(p.BH) * p.N;
+    if (row >= rows)
+        return;
+    const int lane = threadIdx.x & 31;
+    const int i = static_cast<int>(row % p.N);
+    const int qt = i / kBM, pair = qt / 2;
+    const int full0 = key_tiles(p, 2 * pair), full1 = key_tiles(p, 2 * pair + 1);
+    const int fmax = max(full0, full1), fown = (qt & 1) ? full1 : full0;
+    float mx_e = -INFINITY, mx_r = -INFINITY;
+    for (int sp = 0; sp < p.splits; ++sp) {
+        const int j0 = sp * fmax / p.splits, je = (sp + 1) * fmax / p.splits;
+        if (min(je, fown) <= j0)
+            continue;
+        const float2 ll = ws_l[static_cast<size_t>(sp) * rows + row];
+        mx_e = fmaxf(mx_e, ll.x);
+        mx_r = fmaxf(mx_r, ll.y);
+    }
+    float se = 0.f, sr = 0.f;
+    float acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c)
+        acc[c] = 0.f;
+    for (int sp = 0; sp < p.splits; ++sp) {
+        const int j0 = sp * fmax / p.splits, je = (sp + 1) * fmax / p.splits;
+        if (min(je, fown) <= j0)
+            continue;
+        const size_t srow = static_cast<size_t>(sp) * rows + row;
+        const float2 ll = ws_l[srow];
+        se += ex2(ll.x - mx_e);
+        const float w = ex2(ll.y - mx_r);
+        sr += w;
+        const float *src = ws_o + srow * D + lane * kCols;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+            acc[c] = fmaf(w, src[c], acc[c]);
+    }
+    const float inv = 1.f / sr;
+    __nv_bfloat16 *dst = p.o + static_cast<size_t>(row) * D + lane * kCols;
+#pragma unroll
+    for (int c = 0; c < kCols; c += 2)
+        *reinterpret_cast<__nv_bfloat162 *>(dst + c) =
+            __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
+    if (lane == 0)
+        p.lse[row] = (mx_e + log2f(se)) * kLn2;
+}
+
+template <int D>
+cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split, int num_sms,
+                   cudaStream_t stream)
 {
     using C = Cfg<D>;
     Params p;
     p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
+    p.ws_o = split.ws_o;
+    p.ws_l = reinterpret_cast<float2 *>(split.ws_l);
     p.N = a.N;
     p.BH = a.B * a.H;
     p.QT = (a.N + kBM - 1) / kBM;
     p.KT = (a.N + kBN - 1) / kBN;
     p.pairs = (p.QT + 1) / 2;
-    const long long units = static_cast<long long>(p.BH) * p.pairs;
+    p.splits = split.splits < 1 ? 1 : split.splits;
+    const long long units = static_cast<long long>(p.BH) * p.pairs * p.splits;
     if (units == 0)
         return cudaSuccess;
     if (units > 0x7fffffffLL)
@@ -613,15 +729,23 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, int num_sms, cudaStrea
         return e;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
     fwd_kernel<D><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
+    if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
+        return e;
+    const long long rows = static_cast<long long>(p.BH) * p.N;
+    const long long blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    combine_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p.ws_o, p.ws_l, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, int num_sms,
-                             cudaStream_t stream)
+cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
+                             int num_sms, cudaStream_t stream)
 {
-    return a.d == 64 ? launch<64>(a, maps, num_sms, stream) : launch<128>(a, maps, num_sms, stream);
+    return a.d == 64 ? launch<64>(a, maps, split, num_sms, stream)
+                     : launch<128>(a, maps, split, num_sms, stream);
 }
 
 namespace {

@@ -25,6 +25,15 @@ struct FwdMaps {
     CUtensorMap q, k, v;
 };
 
+// Key-range split of the forward pass: splits > 1 sends fp32 partial O
+// ([splits][B*H*N][d]) and base-2 partial lse pairs ([splits][B*H*N] x 2
+// floats) to caller-provided scratch, then a combine kernel writes o / lse.
+struct FwdSplit {
+    int splits;
+    float *ws_o;
+    float *ws_l;
+};
+
 // Device status word codes (see fattn_get_device_status in fattn.h).
 enum DeviceRole : uint32_t {
     kRoleLoad = 1,
@@ -35,8 +44,8 @@ enum DeviceRole : uint32_t {
 };
 
 // tcgen05 / TMA kernel: one persistent CTA per SM.
-cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, int num_sms,
-                             cudaStream_t stream);
+cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
+                             int num_sms, cudaStream_t stream);
 // Failure-path self-test: a wait that nothing satisfies, limited to limit_ns.
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 // Reads (and clears) the device status word of the current device.

@@ -21,7 +21,8 @@ _LIB_PATH = os.path.join(_HERE, "_build", "libfattn.so")
 FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
                 3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
-EXPORTED = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "fattn_status_string",
+EXPORTED = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "attn_fwd_split",
+            "attn_fwd_split_count", "attn_fwd_split_workspace_size", "fattn_status_string",
             "fattn_last_cuda_error", "fattn_get_device_status", "fattn_selftest_wait_timeout",
             "fattn_version"]
 
@@ -63,6 +64,12 @@ def load():
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = fwd_args
+        lib.attn_fwd_split.restype = ctypes.c_int
+        lib.attn_fwd_split.argtypes = fwd_args[:-1] + [ip, vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_split_count.restype = ctypes.c_int
+        lib.attn_fwd_split_count.argtypes = [ip, ip, ip, ip, ip]
+        lib.attn_fwd_split_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_split_workspace_size.argtypes = [ip, ip, ip, ip, ip]
         lib.attn_fwd_host.restype = ctypes.c_int
         lib.attn_fwd_host.argtypes = [vp] * 10 + [ip, ip, ip, ip, fp, ip, vp]
         lib.fattn_status_string.restype = ctypes.c_char_p
@@ -147,6 +154,53 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     scale defaults to 1/sqrt(d).  ``out`` / ``lse`` may be preallocated.  The
     kernel is enqueued on ``stream`` (default: the current stream)."""
     return _forward("attn_fwd", q, k, v, causal, scale, out, lse, stream)
+
+
+def split_count(B: int, H: int, N: int, d: int, causal: bool, device=None) -> int:
+    """Key-range splits the library would use for this shape on the device."""
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        n = lib.attn_fwd_split_count(B, H, N, d, 1 if causal else 0)
+    if n < 1:
+        raise FattnError(1, "attn_fwd_split_count")
+    return n
+
+
+def split_workspace_size(B: int, H: int, N: int, d: int, num_splits: int) -> int:
+    return int(load().attn_fwd_split_workspace_size(B, H, N, d, num_splits))
+
+
+def attn_fwd_split(q, k, v, causal: bool = False, scale: float | None = None,
+                   num_splits: int | None = None, workspace=None, out=None, lse=None,
+                   stream=None):
+    """attn_fwd with the keys of every Q-tile pair split over num_splits CTAs
+    (default: the library's choice for the device) and merged by a combine
+    kernel.  ``workspace`` is a CUDA uint8 tensor of at least
+    split_workspace_size(...) bytes; when omitted, one is allocated here with
+    torch (the library itself never allocates)."""
+    _validate(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    if num_splits is None:
+        num_splits = split_count(B, H, N, d, causal, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = split_workspace_size(B, H, N, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if need > 0 else 0
+    lib = load()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, H, N, d, float(scale), 1 if causal else 0,
+                                int(num_splits), ws_ptr, workspace.numel(),
+                                _stream_handle(stream, q.device))
+    _check(st, "attn_fwd_split")
+    return out, lse
 
 
 def attn_fwd_simt(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
