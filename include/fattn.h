@@ -129,6 +129,33 @@ fattn_status_t attn_fwd_split(const void *q, const void *k, const void *v, void 
                               struct CUstream_st *stream);
 
 /*
+ * attn_fwd_split_noalloc -- attn_fwd_split for callers that cannot allocate
+ * device memory at the point of the call: for example a serving runtime that
+ * plans all of its device memory before it starts and forbids allocation on
+ * its execution path, or a plugin whose host framework owns every device
+ * allocation.  The pages have no counterpart of this call; it exists only for
+ * such callers.
+ *
+ * Same arguments and result as attn_fwd_split without the workspace: the
+ * scratch is a fixed 32 MiB array of device memory inside the library
+ * (every GPU that loads the library holds it until the process exits).  The
+ * call allocates nothing.  Its first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  A shape whose scratch
+ * (attn_fwd_split_workspace_size) exceeds 32 MiB returns
+ * FATTN_ERR_UNSUPPORTED without enqueuing anything: use attn_fwd_split with
+ * your own workspace then.  num_splits == 1 is exactly attn_fwd.  The array
+ * keeps the previous call's contents; nothing in it needs to start at zero,
+ * because every value the merge reads is written earlier by the same call.
+ * All calls in the process share the one array per device, so calls that
+ * overlap on the GPU (e.g. on two streams at once) race and corrupt each
+ * other's results: serialise them.
+ */
+fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, int B, int H, int N, int d, float scale,
+                                      int causal, int num_splits, struct CUstream_st *stream);
+
+/*
  * attn_fwd_simt -- the same operation and contract as attn_fwd, computed by a
  * plain fp32 SIMT kernel (no tensor cores, no 16-bit rounding of P).  It is
  * an independent second GPU implementation for cross-checking results at

@@ -290,6 +290,32 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
     return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream, split);
 }
 
+// ---------------------------------------------------------------- no-allocation split
+// Scratch for attn_fwd_split_noalloc: a fixed device array that lives as long
+// as the library is loaded, so that callers that may not allocate device
+// memory on their execution path still get the split kernel.  Its device
+// address is looked up once per device (cudaGetSymbolAddress, with that device
+// current); in host code the array's name is only a host-side stand-in.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+fattn_status_t noalloc_scratch(int dev, void **out)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr)
+            return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -329,6 +355,31 @@ fattn_status_t attn_fwd_split(const void *q, const void *k, const void *v, void 
 {
     return forward_split(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
                          workspace_bytes, stream);
+}
+
+fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *v, void *o,
+                                      float *lse, int B, int H, int N, int d, float scale,
+                                      int causal, int num_splits, struct CUstream_st *stream)
+{
+    if (num_splits < 1 || num_splits > kMaxSplits)
+        return FATTN_ERR_INVALID_ARG;
+    bool empty = false;
+    fattn_status_t s = check_shape(B, H, N, d, scale, causal, &empty);
+    if (s != FATTN_OK || empty)
+        return s;
+    if (num_splits == 1)  // no scratch needed: exactly attn_fwd
+        return forward(Kernel::kTcgen05, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+    if (split_ws_bytes(B, H, N, d, num_splits) > kNoAllocScratchBytes)
+        return FATTN_ERR_UNSUPPORTED;  // beyond the fixed scratch: use attn_fwd_split
+    int dev = 0;
+    DeviceInfo info;
+    if ((s = current_device(&dev, &info)) != FATTN_OK)
+        return s;
+    void *scratch = nullptr;
+    if ((s = noalloc_scratch(dev, &scratch)) != FATTN_OK)
+        return s;
+    return forward_split(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, scratch,
+                         kNoAllocScratchBytes, stream);
 }
 
 fattn_status_t attn_fwd_simt(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -22,7 +22,8 @@ FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
                 3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
 EXPORTED = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "attn_fwd_split",
-            "attn_fwd_split_count", "attn_fwd_split_workspace_size", "fattn_status_string",
+            "attn_fwd_split_count", "attn_fwd_split_noalloc", "attn_fwd_split_workspace_size",
+            "fattn_status_string",
             "fattn_last_cuda_error", "fattn_get_device_status", "fattn_selftest_wait_timeout",
             "fattn_version"]
 
@@ -66,6 +67,8 @@ def load():
             f.argtypes = fwd_args
         lib.attn_fwd_split.restype = ctypes.c_int
         lib.attn_fwd_split.argtypes = fwd_args[:-1] + [ip, vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_split_noalloc.restype = ctypes.c_int
+        lib.attn_fwd_split_noalloc.argtypes = fwd_args[:-1] + [ip, vp]
         lib.attn_fwd_split_count.restype = ctypes.c_int
         lib.attn_fwd_split_count.argtypes = [ip, ip, ip, ip, ip]
         lib.attn_fwd_split_workspace_size.restype = ctypes.c_size_t
