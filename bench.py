@@ -225,6 +225,69 @@ def run_reference(args, world, rank):
     return 0
 
 
+# ------------------------------------------------------------------ row ops
+ROWOP_WORKLOADS = {
+    "softmax_rows_M32768_N4096_f32": ("softmax_rows", 32768, 4096, torch.float32),
+    "softmax_rows_M2048_N65536_f32": ("softmax_rows", 2048, 65536, torch.float32),
+    "softmax_rows_M32768_N4096_bf16": ("softmax_rows", 32768, 4096, torch.bfloat16),
+    "row_sum_M32768_N4096_f32": ("row_sum", 32768, 4096, torch.float32),
+}
+
+
+def run_rowop(args, world, rank, local):
+    """Standalone row softmax / row sum: achieved GB/s of algorithmic traffic
+    (read x, write y or the sums; a second read of x for rows too long to keep
+    in registers is not counted) against the measured HBM copy bandwidth."""
+    import oracle
+    from tiled_online_softmax_fwd_gb300 import fattn
+    torch.cuda.set_device(local)
+    op, M, N, dt = ROWOP_WORKLOADS[args.op]
+    g = torch.Generator("cpu").manual_seed(7)
+    x = (torch.randn(M, N, generator=g) * 4.0).to(dt)
+    dx = x.cuda()
+    out = torch.empty_like(dx) if op == "softmax_rows" else torch.empty(M, device=dx.device)
+    fn = fattn.softmax_rows if op == "softmax_rows" else fattn.row_sum
+    esize = dx.element_size()
+    algo_bytes = M * N * esize + (M * N * esize if op == "softmax_rows" else M * 4)
+    for _ in range(max(3, args.warmup)):
+        fn(dx, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            fn(dx, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    try:
+        peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+        src = "measured copy (MEASURED_PEAKS.json)"
+    except Exception:
+        peak, src = 6800.0, "fallback 6.8 TB/s"
+    rows = min(M, 256)
+    t0 = time.perf_counter()
+    (oracle.softmax_rows if op == "softmax_rows" else oracle.row_sum)(x[:rows])
+    cpu_s = time.perf_counter() - t0
+    cpu_gbs = algo_bytes * rows / M / cpu_s / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "%s GB/s (HBM-bound, 1xGB300)" % op, "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if dt == torch.float32 else "bf16", "data": "synthetic",
+            "config": {"workload": args.op, "M": M, "N": N,
+                       "l2": "inputs larger than L2 (%d MB)" % (M * N * esize // 10**6)},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_source": src, "traffic": None,
+                         "algorithmic_bytes_per_launch": algo_bytes},
+            "gpu_launches": args.steps, "clocks": clocks.summary(),
+            "cpu_baseline": {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d of %d rows" % (rows, M)}}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args, world, rank, local):
     from tiled_online_softmax_fwd_gb300 import fattn
@@ -362,12 +425,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--op", default=None, choices=sorted(ROWOP_WORKLOADS),
+                    help="time a standalone row softmax / row sum workload instead")
     ap.add_argument("--split", default="auto", choices=["auto", "off"],
                     help="key-range split when the library recommends one (auto) or never")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.op:
+        return run_rowop(args, world, rank, local)
     return run_gpu(args, world, rank, local)
 
 

@@ -165,6 +165,25 @@ fattn_status_t attn_fwd_simt(const void *q, const void *k, const void *v, void *
                              int B, int H, int N, int d, float scale, int causal,
                              struct CUstream_st *stream);
 
+/*
+ * Standalone row softmax and row sum (HBM-bound), after the row softmax and
+ * row-sum examples of "CS336 lecture 6: kernels and Triton":
+ *   fattn_softmax_rows: y[i][j] = exp(x[i][j] - max_k x[i][k]) / sum_k exp(x[i][k] - max_k x[i][k])
+ *   fattn_row_sum:      out[i]  = sum_j x[i][j]
+ * x is a contiguous row-major [M][N] device matrix of dtype 0 = fp32 or
+ * 1 = bf16 (arithmetic in fp32); the softmax writes y with x's shape and type
+ * (y may equal x for an in-place softmax, but must not otherwise overlap it);
+ * the row sums go to fp32 out[M].  Pointers must be device pointers aligned
+ * to their element size.  Rows of up to 16384 elements are read from HBM
+ * once; longer rows twice (an online max/sum pass, then the output pass).
+ * Empty inputs are no-ops (an empty row sums to 0).  Asynchronous on
+ * `stream`; errors as for attn_fwd.
+ */
+fattn_status_t fattn_softmax_rows(const void *x, void *y, int M, int N, int dtype,
+                                  struct CUstream_st *stream);
+fattn_status_t fattn_row_sum(const void *x, float *out, int M, int N, int dtype,
+                             struct CUstream_st *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *fattn_status_string(fattn_status_t status);
 

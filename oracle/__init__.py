@@ -27,6 +27,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "rowops_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -38,11 +39,11 @@ def build(force: bool = False) -> str:
     """Compile attn_oracle.c into oracle/_build/liboracle.so with gcc."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
     cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-fPIC", "-shared",
-           "-pthread", "-o", tmp, _SRC, "-lm"]
+           "-pthread", "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -51,6 +52,11 @@ def build(force: bool = False) -> str:
 def _open(path: str):
     lib = ctypes.CDLL(path)
     dp = ctypes.POINTER(ctypes.c_double)
+    if hasattr(lib, "oracle_softmax_rows"):
+        for name in ("oracle_softmax_rows", "oracle_row_sum"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [dp, dp, ctypes.c_int64, ctypes.c_int64]
     lib.oracle_attn_fwd.restype = ctypes.c_int
     lib.oracle_attn_fwd.argtypes = [
         dp, dp, dp, dp, dp, dp,
@@ -141,3 +147,33 @@ def _run(lib, q, k, v, scale, causal, rows, threads, with_probs):
     if with_probs:
         return o, lse, probs
     return o, lse
+
+
+def softmax_rows(x):
+    """Exact fp64 softmax over the last axis of a 2-D array (rows).
+
+    Definition of the Triton softmax example in "CS336 lecture 6: kernels and
+    Triton": y = exp(x - rowmax) / sum exp(x - rowmax)."""
+    xd = _as_f64(x)
+    if xd.ndim != 2:
+        raise ValueError("x must be [M, N]")
+    M, N = xd.shape
+    y = np.zeros_like(xd)
+    rc = _load().oracle_softmax_rows(_ptr(xd), _ptr(y), M, N)
+    if rc != 0:
+        raise RuntimeError("oracle_softmax_rows failed")
+    return y
+
+
+def row_sum(x):
+    """Exact-as-fp64 sum of every row of a 2-D array (the row-sum example of
+    "CS336 lecture 6: kernels and Triton")."""
+    xd = _as_f64(x)
+    if xd.ndim != 2:
+        raise ValueError("x must be [M, N]")
+    M, N = xd.shape
+    out = np.zeros(M, dtype=np.float64)
+    rc = _load().oracle_row_sum(_ptr(xd), _ptr(out), M, N)
+    if rc != 0:
+        raise RuntimeError("oracle_row_sum failed")
+    return out

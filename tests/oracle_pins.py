@@ -260,3 +260,38 @@ def pin_row_selection(oracle):
 ALL_PINS = [pin_brute_force, pin_online_equals_two_pass, pin_rows_sum_to_one,
             pin_shift_invariance, pin_identical_values, pin_zero_queries,
             pin_single_key_rows, pin_permutations, pin_row_selection]
+
+
+# --------------------------------------------------------------------------- row ops
+def pin_softmax_rows(softmax_rows):
+    """Row softmax: matches torch.softmax in fp64, rows sum to 1, invariant to a
+    per-row shift, uniform for a constant row, one-hot in the large-gap limit."""
+    g = torch.Generator().manual_seed(101)
+    x = torch.randn(7, 33, generator=g, dtype=torch.float64) * 4
+    y = softmax_rows(x)
+    _close(y, torch.softmax(x, dim=1).numpy(), 1e-14, "softmax vs torch")
+    _close(y.sum(axis=1), np.ones(7), 1e-14, "softmax row sums")
+    shift = torch.tensor([[-3.5], [0.25], [100.0], [-1e3], [7.0], [0.0], [12.5]], dtype=torch.float64)
+    _close(softmax_rows(x + shift), y, 1e-13, "softmax shift invariance")
+    _close(softmax_rows(torch.full((2, 9), 3.0, dtype=torch.float64)), np.full((2, 9), 1 / 9), 1e-15,
+           "softmax of a constant row")
+    z = torch.zeros(1, 5, dtype=torch.float64)
+    z[0, 2] = 800.0
+    assert np.array_equal(softmax_rows(z), np.array([[0.0, 0.0, 1.0, 0.0, 0.0]])), "one-hot limit"
+    # direct definition without the max shift, exactly rounded sums
+    for row in x.tolist()[:3]:
+        e = [math.exp(a) for a in row]
+        zsum = math.fsum(e)
+        ref = [a / zsum for a in e]
+        _close(softmax_rows(torch.tensor([row], dtype=torch.float64))[0], ref, 1e-14, "softmax direct")
+
+
+def pin_row_sum(row_sum):
+    """Row sum: equals math.fsum of each row (exactly rounded), and is linear."""
+    g = torch.Generator().manual_seed(102)
+    x = torch.randn(6, 1000, generator=g, dtype=torch.float64)
+    s = row_sum(x)
+    ref = [math.fsum(r) for r in x.tolist()]
+    _close(s, ref, 1e-12, "row sum vs fsum")
+    _close(row_sum(2.0 * x + 1.0), 2.0 * np.asarray(ref) + 1000.0, 1e-12, "row sum linearity")
+    assert row_sum(torch.zeros(3, 0, dtype=torch.float64)).tolist() == [0.0, 0.0, 0.0]

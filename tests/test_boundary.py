@@ -147,3 +147,15 @@ def test_split_arguments_are_checked(lib):
     assert f(*base, 65, ws, 1 << 30, None) == INVALID
     assert f(*base[:5], 1, 1, 4096, 80, 0.125, 0, 4, ws, 1 << 30, None) == UNSUPPORTED
     assert f(*base[:5], 1, 1, 0, 64, 0.125, 0, 4, 0, 0, None) == OK   # empty: no-op
+
+
+def test_rowop_arguments_are_checked(lib):
+    for f in (lib.fattn_softmax_rows, lib.fattn_row_sum):
+        assert f(A, A + (1 << 24), -1, 4, 0, None) == INVALID      # negative M
+        assert f(A, A + (1 << 24), 4, -1, 0, None) == INVALID      # negative N
+        assert f(A, A + (1 << 24), 4, 4, 2, None) == INVALID       # unknown dtype
+        assert f(0, A, 4, 4, 0, None) == INVALID                   # null input
+        assert f(A + 2, A + (1 << 24), 4, 4, 0, None) == INVALID   # misaligned fp32
+        assert f(0, 0, 0, 16, 0, None) == OK                       # empty: no-op
+    assert lib.fattn_softmax_rows(A, A + 8, 4, 4, 0, None) == INVALID   # partial overlap
+    assert lib.fattn_row_sum(A, A + 8, 4, 4, 0, None) == INVALID        # sums inside input

@@ -60,6 +60,55 @@ def test_planted_mistake_is_caught(name, mutant_dir):
     assert failed, "planted mistake %s passed every pin" % name
 
 
+def test_rowops_oracle_meets_pins():
+    pins.pin_softmax_rows(oracle.softmax_rows)
+    pins.pin_row_sum(oracle.row_sum)
+
+
+ROWOPS_MUTANTS = {
+    "softmax_no_max_shift": ("yi[j] = exp(xi[j] - m);", "yi[j] = exp(xi[j] - m) * exp(m - 1.0);"),
+    "softmax_not_normalised": ("yi[j] /= z;", "yi[j] /= 1.0;"),
+    "softmax_exp_sign": ("yi[j] = exp(xi[j] - m);", "yi[j] = exp(m - xi[j]);"),
+    "row_sum_drops_last": ("for (int64_t j = 0; j < N; ++j)\n            acc += xi[j];",
+                           "for (int64_t j = 0; j + 1 < N; ++j)\n            acc += xi[j];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROWOPS_MUTANTS))
+def test_rowops_planted_mistake_is_caught(name, mutant_dir):
+    here = os.path.dirname(oracle.__file__)
+    src = open(os.path.join(here, "rowops_oracle.c")).read()
+    old, new = ROWOPS_MUTANTS[name]
+    assert src.count(old) >= 1, "mutation anchor vanished: %r" % old
+    c_path = os.path.join(mutant_dir, name + ".c")
+    so_path = os.path.join(mutant_dir, name + ".so")
+    with open(c_path, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", so_path,
+                    os.path.join(here, "attn_oracle.c"), c_path, "-lm"], check=True)
+    lib = oracle._open(so_path)
+
+    def softmax_rows(x):
+        xd = oracle._as_f64(x)
+        y = np.zeros_like(xd)
+        assert lib.oracle_softmax_rows(oracle._ptr(xd), oracle._ptr(y), *xd.shape) == 0
+        return y
+
+    def row_sum(x):
+        xd = oracle._as_f64(x)
+        out = np.zeros(xd.shape[0])
+        assert lib.oracle_row_sum(oracle._ptr(xd), oracle._ptr(out), *xd.shape) == 0
+        return out
+    failed = 0
+    with np.errstate(all="ignore"):
+        for pin, fn in ((pins.pin_softmax_rows, softmax_rows), (pins.pin_row_sum, row_sum)):
+            try:
+                pin(fn)
+            except AssertionError:
+                failed += 1
+    assert failed, "planted mistake %s passed every pin" % name
+
+
 def test_oracle_rejects_bad_arguments():
     q = torch.zeros(1, 1, 4, 2, dtype=torch.float64)
     with pytest.raises(RuntimeError):

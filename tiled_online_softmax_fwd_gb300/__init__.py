@@ -6,7 +6,8 @@ Importing the package does not load the library: the first call does, and it
 raises if the library has not been built (there is no CPU fallback).
 """
 __all__ = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "attn_fwd_split", "split_count",
-           "split_workspace_size", "FattnError", "device_status", "library_path", "version"]
+           "split_workspace_size", "softmax_rows", "row_sum", "FattnError", "device_status",
+           "library_path", "version"]
 
 
 def __getattr__(name):

@@ -382,6 +382,61 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
                          kNoAllocScratchBytes, stream);
 }
 
+static fattn_status_t rowop(bool softmax, const void *x, void *y, int M, int N, int dtype,
+                            cudaStream_t stream)
+{
+    if (M < 0 || N < 0 || (dtype != 0 && dtype != 1))
+        return FATTN_ERR_INVALID_ARG;
+    if (M == 0 || (N == 0 && softmax))
+        return FATTN_OK;
+    if (!y || (!x && N > 0))
+        return FATTN_ERR_INVALID_ARG;
+    if (N == 0) {  // row sums of empty rows are zero; x is not read
+        if (reinterpret_cast<uintptr_t>(y) % 4)
+            return FATTN_ERR_INVALID_ARG;
+        int dev = 0;
+        DeviceInfo info;
+        fattn_status_t s = current_device(&dev, &info);
+        if (s != FATTN_OK || (s = check_device_buffer(y, dev)) != FATTN_OK)
+            return s;
+        const cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M) * 4, stream);
+        return e == cudaSuccess ? FATTN_OK : cuda_fail(e);
+    }
+    const size_t elem = dtype == 0 ? 4 : 2;
+    const size_t in_bytes = static_cast<size_t>(M) * N * elem;
+    const size_t out_bytes = softmax ? in_bytes : static_cast<size_t>(M) * 4;
+    if (reinterpret_cast<uintptr_t>(x) % elem || reinterpret_cast<uintptr_t>(y) % 4 ||
+        (softmax && reinterpret_cast<uintptr_t>(y) % elem))
+        return FATTN_ERR_INVALID_ARG;
+    // The softmax may run in place (y == x) but not on partly overlapping
+    // buffers; the row sums must not overlap the input.
+    if ((!softmax || x != y) && overlap(x, in_bytes, y, out_bytes))
+        return FATTN_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceInfo info;
+    fattn_status_t s = current_device(&dev, &info);
+    if (s != FATTN_OK)
+        return s;
+    if ((s = check_device_buffer(x, dev)) != FATTN_OK || (s = check_device_buffer(y, dev)) != FATTN_OK)
+        return s;
+    const cudaError_t e =
+        softmax ? fattn::launch_softmax_rows(x, y, M, N, dtype, info.num_sms, stream)
+                : fattn::launch_row_sum(x, static_cast<float *>(y), M, N, dtype, info.num_sms, stream);
+    return e == cudaSuccess ? FATTN_OK : cuda_fail(e);
+}
+
+fattn_status_t fattn_softmax_rows(const void *x, void *y, int M, int N, int dtype,
+                                  struct CUstream_st *stream)
+{
+    return rowop(true, x, y, M, N, dtype, stream);
+}
+
+fattn_status_t fattn_row_sum(const void *x, float *out, int M, int N, int dtype,
+                             struct CUstream_st *stream)
+{
+    return rowop(false, x, out, M, N, dtype, stream);
+}
+
 fattn_status_t attn_fwd_simt(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int H, int N, int d, float scale, int causal,
                              struct CUstream_st *stream)

@@ -55,4 +55,11 @@ cudaError_t read_and_clear_status(uint32_t *out, cudaStream_t stream);
 // the tests as a cross-check.  Not used by attn_fwd.
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t stream);
 
+// Row softmax / row sum over a contiguous [M][N] matrix of fp32 (dtype 0) or
+// bf16 (dtype 1); the softmax output has the input's type, the sums are fp32.
+cudaError_t launch_softmax_rows(const void *x, void *y, int M, int N, int dtype, int num_sms,
+                                cudaStream_t stream);
+cudaError_t launch_row_sum(const void *x, float *out, int M, int N, int dtype, int num_sms,
+                           cudaStream_t stream);
+
 }  // namespace fattn

@@ -24,8 +24,8 @@ STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPO
 EXPORTED = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "attn_fwd_split",
             "attn_fwd_split_count", "attn_fwd_split_noalloc", "attn_fwd_split_workspace_size",
             "fattn_status_string",
-            "fattn_last_cuda_error", "fattn_get_device_status", "fattn_selftest_wait_timeout",
-            "fattn_version"]
+            "fattn_last_cuda_error", "fattn_get_device_status", "fattn_row_sum",
+            "fattn_selftest_wait_timeout", "fattn_softmax_rows", "fattn_version"]
 
 _lib = None
 _lock = threading.Lock()
@@ -83,6 +83,10 @@ def load():
         lib.fattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
         lib.fattn_selftest_wait_timeout.restype = ctypes.c_int
         lib.fattn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        for name in ("fattn_softmax_rows", "fattn_row_sum"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [vp, vp, ip, ip, ip, vp]
         lib.fattn_version.restype = ctypes.c_char_p
         lib.fattn_version.argtypes = []
         _lib = lib
@@ -260,6 +264,47 @@ def selftest_wait_timeout(limit_us: int = 20000, stream=None, device=None):
     with torch.cuda.device(dev):
         st = lib.fattn_selftest_wait_timeout(int(limit_us), _stream_handle(stream, dev))
     _check(st, "fattn_selftest_wait_timeout")
+
+
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+def _rowop_input(x):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [M, N] tensor")
+    if x.dtype not in _DTYPES:
+        raise ValueError("x must be float32 or bfloat16")
+    return x.shape[0], x.shape[1], _DTYPES[x.dtype]
+
+
+def softmax_rows(x, out=None, stream=None):
+    """Row softmax of a contiguous [M, N] fp32/bf16 CUDA tensor (out may be x)."""
+    M, N, dt = _rowop_input(x)
+    if out is None:
+        out = torch.empty_like(x)
+    if out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must match x")
+    with torch.cuda.device(x.device):
+        st = load().fattn_softmax_rows(x.data_ptr(), out.data_ptr(), M, N, dt,
+                                       _stream_handle(stream, x.device))
+    _check(st, "fattn_softmax_rows")
+    return out
+
+
+def row_sum(x, out=None, stream=None):
+    """fp32 sums of the rows of a contiguous [M, N] fp32/bf16 CUDA tensor."""
+    M, N, dt = _rowop_input(x)
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=x.device)
+    if out.shape != (M,) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 [M] tensor")
+    with torch.cuda.device(x.device):
+        st = load().fattn_row_sum(x.data_ptr(), out.data_ptr(), M, N, dt,
+                                  _stream_handle(stream, x.device))
+    _check(st, "fattn_row_sum")
+    return out
 
 
 def version() -> str:
