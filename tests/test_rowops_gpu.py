@@ -36,7 +36,10 @@ def test_softmax_rows_matches_oracle(M, N, dtype):
     err = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30)
     assert np.all(np.isfinite(got))
     assert np.all(np.abs(got - ref) <= rtol * np.abs(ref) + 1e-30), err.max()
-    np.testing.assert_allclose(got.sum(axis=1), 1.0, rtol=0, atol=max(1e-5, N * 2 ** -9 / N))
+    # rows sum to 1 up to the output rounding (one dominant bf16 element can
+    # be off by 2^-8 of itself)
+    np.testing.assert_allclose(got.sum(axis=1), 1.0, rtol=0,
+                               atol=1e-5 if dtype == torch.float32 else 2 ** -8)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])

@@ -114,19 +114,21 @@ __device__ __forceinline__ float block_sum(float v, float *red)
 // chunk that crosses N is handled element by element (never read past N).
 // x and y may be the same buffer (in place): every element is read and then
 // written by the same thread, and no thread reads another thread's elements.
-template <typename T>
+// kMaxChunks = 0 selects the two-pass path; otherwise chunks <= kMaxChunks and
+// the row stays in registers (instantiated for 1, 2, 4, ... so that short
+// rows use few registers and many rows are in flight per SM).
+template <typename T, int kMaxChunks>
 __global__ void __launch_bounds__(kThreads)
     softmax_rows_kernel(const T *x, T *y, int M, int N, int chunks, int vec_ok)
 {
     using Ck = Chunk<T>;
     constexpr int E = Ck::kElems;
-    constexpr int kMaxChunks = MaxChunks<T>::value;
     __shared__ float red[kThreads / 32];
     const int t = threadIdx.x;
     for (int row = blockIdx.x; row < M; row += gridDim.x) {
         const T *xr = x + static_cast<size_t>(row) * N;
         T *yr = y + static_cast<size_t>(row) * N;
-        if (chunks <= kMaxChunks) {
+        if constexpr (kMaxChunks > 0) {
             // One read: the row lives in registers.
             float v[kMaxChunks][E];
             float mx = -INFINITY;
@@ -261,6 +263,32 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Grid of (resident CTAs per SM) x SMs, rows dealt grid-stride.
+template <typename K>
+cudaError_t launch_grid(K kernel, int M, int num_sms, int *grid)
+{
+    int per_sm = 1;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+    if (e != cudaSuccess)
+        return e;
+    const long long slots = static_cast<long long>(num_sms) * (per_sm > 0 ? per_sm : 1);
+    *grid = static_cast<int>(M < slots ? M : slots);
+    return cudaSuccess;
+}
+
+template <typename T, int C>
+cudaError_t launch_softmax(const void *x, void *y, int M, int N, int chunks, int vec_ok,
+                           int num_sms, cudaStream_t stream)
+{
+    int grid = 0;
+    const cudaError_t e = launch_grid(softmax_rows_kernel<T, C>, M, num_sms, &grid);
+    if (e != cudaSuccess)
+        return e;
+    softmax_rows_kernel<T, C><<<grid, kThreads, 0, stream>>>(
+        static_cast<const T *>(x), static_cast<T *>(y), M, N, chunks, vec_ok);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_rowop(bool softmax, const void *x, void *y, int M, int N, int num_sms,
                          cudaStream_t stream)
@@ -270,23 +298,28 @@ cudaError_t launch_rowop(bool softmax, const void *x, void *y, int M, int N, int
     const int chunks = static_cast<int>((N + per_pass - 1) / per_pass);
     const int vec_ok = (N % E == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                        (!softmax || (reinterpret_cast<uintptr_t>(y) & 15u) == 0);
-    int per_sm = 1;
-    cudaError_t e = softmax ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                  &per_sm, softmax_rows_kernel<T>, kThreads, 0)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                  &per_sm, row_sum_kernel<T>, kThreads, 0);
-    if (e != cudaSuccess)
-        return e;
-    const long long slots = static_cast<long long>(num_sms) * (per_sm > 0 ? per_sm : 1);
-    const int grid = static_cast<int>(M < slots ? M : slots);
-    if (softmax)
-        softmax_rows_kernel<T><<<grid, kThreads, 0, stream>>>(
-            static_cast<const T *>(x), static_cast<T *>(y), M, N, chunks, vec_ok);
-    else
+    if (!softmax) {
+        int grid = 0;
+        const cudaError_t e = launch_grid(row_sum_kernel<T>, M, num_sms, &grid);
+        if (e != cudaSuccess)
+            return e;
         row_sum_kernel<T><<<grid, kThreads, 0, stream>>>(static_cast<const T *>(x),
                                                          static_cast<float *>(y), M, N, chunks,
                                                          vec_ok);
-    return cudaGetLastError();
+        return cudaGetLastError();
+    }
+    constexpr int kMax = MaxChunks<T>::value;
+    if (chunks <= 1)
+        return launch_softmax<T, 1>(x, y, M, N, chunks, vec_ok, num_sms, stream);
+    if (chunks <= 2)
+        return launch_softmax<T, 2>(x, y, M, N, chunks, vec_ok, num_sms, stream);
+    if (chunks <= 4)
+        return launch_softmax<T, 4>(x, y, M, N, chunks, vec_ok, num_sms, stream);
+    if (chunks <= 8)
+        return launch_softmax<T, 8>(x, y, M, N, chunks, vec_ok, num_sms, stream);
+    if (chunks <= kMax)
+        return launch_softmax<T, kMax>(x, y, M, N, chunks, vec_ok, num_sms, stream);
+    return launch_softmax<T, 0>(x, y, M, N, chunks, vec_ok, num_sms, stream);
 }
 
 }  // namespace
