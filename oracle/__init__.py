@@ -27,7 +27,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
-_SRCS = [_SRC, os.path.join(_HERE, "rowops_oracle.c")]
+_SRCS = [_SRC, os.path.join(_HERE, "rowops_oracle.c"), os.path.join(_HERE, "attn_bwd_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
@@ -52,6 +52,14 @@ def build(force: bool = False) -> str:
 def _open(path: str):
     lib = ctypes.CDLL(path)
     dp = ctypes.POINTER(ctypes.c_double)
+    if hasattr(lib, "oracle_attn_bwd"):
+        i64 = ctypes.c_int64
+        lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = [dp] * 7 + [i64] * 4 + [ctypes.c_double, ctypes.c_int,
+                                                                ctypes.c_int]
+        lib.oracle_attn_bwd_dq_rows.restype = ctypes.c_int
+        lib.oracle_attn_bwd_dq_rows.argtypes = [dp] * 5 + [i64] * 4 + [
+            ctypes.c_double, ctypes.c_int, ctypes.POINTER(i64), i64, ctypes.c_int]
     if hasattr(lib, "oracle_softmax_rows"):
         for name in ("oracle_softmax_rows", "oracle_row_sum"):
             f = getattr(lib, name)
@@ -176,4 +184,35 @@ def row_sum(x):
     rc = _load().oracle_row_sum(_ptr(xd), _ptr(out), M, N)
     if rc != 0:
         raise RuntimeError("oracle_row_sum failed")
+    return out
+
+
+def attn_bwd(q, k, v, dout, scale: float, causal: bool, threads: int | None = None):
+    """Exact fp64 gradients (dq, dk, dv), each [B, H, N, d], of the attention
+    forward O = softmax(scale Q K^T [causal]) V for the upstream gradient dout."""
+    qd, kd, vd, dd = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    if qd.ndim != 4 or not (qd.shape == kd.shape == vd.shape == dd.shape):
+        raise ValueError("q, k, v, dout must share one [B, H, N, d] shape")
+    B, H, N, d = qd.shape
+    dq, dk, dv = (np.zeros_like(qd) for _ in range(3))
+    rc = _load().oracle_attn_bwd(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(dd), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, H, N, d, float(scale), 1 if causal else 0,
+                                 int(threads) if threads else default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd failed with code %d" % rc)
+    return dq, dk, dv
+
+
+def attn_bwd_dq_rows(q, k, v, dout, scale: float, causal: bool, rows, threads: int | None = None):
+    """Exact fp64 dq for the given global rows (b*H + h)*N + i: [R, d]."""
+    qd, kd, vd, dd = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    B, H, N, d = qd.shape
+    rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    out = np.zeros((rows_arr.size, d))
+    rc = _load().oracle_attn_bwd_dq_rows(
+        _ptr(qd), _ptr(kd), _ptr(vd), _ptr(dd), _ptr(out), B, H, N, d, float(scale),
+        1 if causal else 0, rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        rows_arr.size, int(threads) if threads else default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd_dq_rows failed with code %d" % rc)
     return out

@@ -295,3 +295,71 @@ def pin_row_sum(row_sum):
     _close(s, ref, 1e-12, "row sum vs fsum")
     _close(row_sum(2.0 * x + 1.0), 2.0 * np.asarray(ref) + 1000.0, 1e-12, "row sum linearity")
     assert row_sum(torch.zeros(3, 0, dtype=torch.float64)).tolist() == [0.0, 0.0, 0.0]
+
+
+# --------------------------------------------------------------------------- backward
+def _torch_attn(q, k, v, scale, causal):
+    s = torch.einsum("bhic,bhjc->bhij", q, k) * scale
+    if causal:
+        N = q.shape[2]
+        s = s.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+    return torch.softmax(s, dim=-1) @ v
+
+
+def pin_bwd_autograd(attn_bwd):
+    """Gradients equal torch.autograd of the standard attention in fp64."""
+    for (B, H, N, d, causal, seed) in [(1, 1, 1, 2, False, 1), (1, 2, 6, 3, False, 2),
+                                       (2, 1, 9, 4, True, 3), (1, 1, 17, 8, True, 4)]:
+        q = _bf16_exact((B, H, N, d), seed, 2.0).requires_grad_()
+        k = _bf16_exact((B, H, N, d), seed + 10, 2.0).requires_grad_()
+        v = _bf16_exact((B, H, N, d), seed + 20).requires_grad_()
+        g = _bf16_exact((B, H, N, d), seed + 30)
+        _torch_attn(q, k, v, 0.6, causal).backward(g)
+        dq, dk, dv = attn_bwd(q.detach(), k.detach(), v.detach(), g, 0.6, causal)
+        _close(dq, q.grad.numpy(), 1e-12, "bwd dq vs autograd")
+        _close(dk, k.grad.numpy(), 1e-12, "bwd dk vs autograd")
+        _close(dv, v.grad.numpy(), 1e-12, "bwd dv vs autograd")
+
+
+def pin_bwd_finite_difference(attn_bwd, attn_fwd):
+    """Central differences of L = sum(O * g) through the forward oracle."""
+    B, H, N, d = 1, 1, 5, 3
+    q = _bf16_exact((B, H, N, d), 41)
+    k = _bf16_exact((B, H, N, d), 42)
+    v = _bf16_exact((B, H, N, d), 43)
+    g = _bf16_exact((B, H, N, d), 44)
+    for causal in (False, True):
+        grads = dict(zip("qkv", attn_bwd(q, k, v, g, 0.8, causal)))
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            for idx in [(0, 0, 0, 0), (0, 0, 2, 1), (0, 0, 4, 2)]:
+                eps = 1e-5
+                tp, tm = t.clone(), t.clone()
+                tp[idx] += eps
+                tm[idx] -= eps
+                args_p = {"q": q, "k": k, "v": v, name: tp}
+                args_m = {"q": q, "k": k, "v": v, name: tm}
+                lp = (attn_fwd(args_p["q"], args_p["k"], args_p["v"], 0.8, causal)[0] *
+                      g.reshape(-1, d).numpy()).sum()
+                lm = (attn_fwd(args_m["q"], args_m["k"], args_m["v"], 0.8, causal)[0] *
+                      g.reshape(-1, d).numpy()).sum()
+                fd = (lp - lm) / (2 * eps)
+                assert abs(fd - grads[name][idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd,
+                                                                                 grads[name][idx])
+
+
+def pin_bwd_invariants(attn_bwd, attn_bwd_dq_rows):
+    """Each row of dS sums to zero, so the key gradients sum to zero over the
+    keys; the value gradients sum to the sum of dO over the rows (rows of P
+    sum to one); and the dq rows mode equals the full dq rows."""
+    for causal in (False, True):
+        B, H, N, d = 2, 2, 23, 4
+        q = _bf16_exact((B, H, N, d), 51, 2.0)
+        k = _bf16_exact((B, H, N, d), 52, 2.0)
+        v = _bf16_exact((B, H, N, d), 53)
+        g = _bf16_exact((B, H, N, d), 54)
+        dq, dk, dv = attn_bwd(q, k, v, g, 0.4, causal)
+        assert np.max(np.abs(dk.sum(axis=2))) <= 1e-12, "sum_j dK_j != 0"
+        _close(dv.sum(axis=2), g.sum(dim=2).numpy(), 1e-12, "sum_j dV_j")
+        rows = np.array([0, 7, 22, 23, 50, 91], dtype=np.int64)
+        _close(attn_bwd_dq_rows(q, k, v, g, 0.4, causal, rows), dq.reshape(-1, d)[rows], 1e-13,
+               "dq rows mode")

@@ -1,5 +1,6 @@
 """CPU tests: the fp64 oracle against its pins, and planted mistakes in copies
 of the oracle that the pins must catch."""
+import ctypes
 import os
 import subprocess
 
@@ -57,6 +58,70 @@ def test_planted_mistake_is_caught(name, mutant_dir):
                 pin(fn)
             except AssertionError:
                 failed.append(pin.__name__)
+    assert failed, "planted mistake %s passed every pin" % name
+
+
+def test_bwd_oracle_meets_pins():
+    pins.pin_bwd_autograd(oracle.attn_bwd)
+    pins.pin_bwd_finite_difference(oracle.attn_bwd, oracle.attn_fwd)
+    pins.pin_bwd_invariants(oracle.attn_bwd, oracle.attn_bwd_dq_rows)
+
+
+BWD_MUTANTS = {
+    "dq_without_scale": ("dqh[i * d + c] += jb->scale * ds * kh[j * d + c];",
+                         "dqh[i * d + c] += ds * kh[j * d + c];"),
+    "ds_without_D": ("const double ds = p[j] * (dp[j] - D);\n                for",
+                     "const double ds = p[j] * dp[j];\n                for"),
+    "dk_uses_k": ("dkh[j * d + c] += jb->scale * ds * qh[i * d + c];",
+                  "dkh[j * d + c] += jb->scale * ds * kh[i * d + c];"),
+    "dv_uses_ds": ("dvh[j * d + c] += p[j] * doh[i * d + c];",
+                   "dvh[j * d + c] += (p[j] - 0.5 * p[j] * p[j]) * doh[i * d + c];"),
+    "dp_wrong_operand": ("dot += doi[c] * vh[j * d + c];", "dot += doi[c] * kh[j * d + c];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_bwd_planted_mistake_is_caught(name, mutant_dir):
+    here = os.path.dirname(oracle.__file__)
+    src = open(os.path.join(here, "attn_bwd_oracle.c")).read()
+    old, new = BWD_MUTANTS[name]
+    assert src.count(old) >= 1, "mutation anchor vanished: %r" % old
+    c_path = os.path.join(mutant_dir, "bwd_" + name + ".c")
+    so_path = os.path.join(mutant_dir, "bwd_" + name + ".so")
+    with open(c_path, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", so_path,
+                    os.path.join(here, "attn_oracle.c"), os.path.join(here, "rowops_oracle.c"),
+                    c_path, "-lm"], check=True)
+    lib = oracle._open(so_path)
+
+    def attn_bwd(q, k, v, dout, scale, causal):
+        qd, kd, vd, dd = (oracle._as_f64(t) for t in (q, k, v, dout))
+        B, H, N, d = qd.shape
+        outs = [np.zeros_like(qd) for _ in range(3)]
+        assert lib.oracle_attn_bwd(*(oracle._ptr(t) for t in (qd, kd, vd, dd, *outs)), B, H, N, d,
+                                   float(scale), int(causal), 1) == 0
+        return outs
+
+    def dq_rows(q, k, v, dout, scale, causal, rows):
+        qd, kd, vd, dd = (oracle._as_f64(t) for t in (q, k, v, dout))
+        B, H, N, d = qd.shape
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        out = np.zeros((r.size, d))
+        assert lib.oracle_attn_bwd_dq_rows(*(oracle._ptr(t) for t in (qd, kd, vd, dd, out)), B, H,
+                                           N, d, float(scale), int(causal),
+                                           r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                           r.size, 1) == 0
+        return out
+    failed = 0
+    with np.errstate(all="ignore"):
+        for run in (lambda: pins.pin_bwd_autograd(attn_bwd),
+                    lambda: pins.pin_bwd_finite_difference(attn_bwd, oracle.attn_fwd),
+                    lambda: pins.pin_bwd_invariants(attn_bwd, dq_rows)):
+            try:
+                run()
+            except AssertionError:
+                failed += 1
     assert failed, "planted mistake %s passed every pin" % name
 
 
