@@ -226,6 +226,8 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ row ops
+BWD_WORKLOADS = ["bwd_" + n for n in WORKLOADS]
+
 ROWOP_WORKLOADS = {
     "softmax_rows_M32768_N4096_f32": ("softmax_rows", 32768, 4096, torch.float32),
     "softmax_rows_M2048_N65536_f32": ("softmax_rows", 2048, 65536, torch.float32),
@@ -285,6 +287,53 @@ def run_rowop(args, world, rank, local):
             "gpu_launches": args.steps, "clocks": clocks.summary(),
             "cpu_baseline": {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": "%d of %d rows" % (rows, M)}}), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ backward
+def run_bwd(args, world, rank, local):
+    """attn_bwd on one of the forward workloads: TFLOP/s of the method's
+    algorithmic work (five products, 10*B*H*N^2*d, halved under the causal
+    mask; the kernels recompute S and dP once more, which is not counted)."""
+    from tiled_online_softmax_fwd_gb300 import fattn
+    torch.cuda.set_device(local)
+    w = WORKLOADS[args.op[len("bwd_"):]]
+    q, k, v, _ = make_workload(w)
+    g = torch.Generator("cpu").manual_seed(77)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).cuda()
+    dq_, dk_, dv_ = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fattn.attn_fwd(dq_, dk_, dv_, causal=w.causal, scale=w.scale)
+    gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
+    ws = torch.empty(w.B * w.H * w.N * 4, dtype=torch.uint8, device=dq_.device)
+
+    def step():
+        fattn.attn_bwd(dq_, dk_, dv_, o, lse, dout, causal=w.causal, scale=w.scale, workspace=ws,
+                       dq=gq, dk=gk, dv=gv)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 2.5 * w.flops
+    value = flops / (ms * 1e-3) / 1e12
+    peak, peak_src = measured_peak()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "attention bwd TFLOP/s (bf16, 1xGB300)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": args.op, **w.describe()},
+            "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                         "frac": value / peak, "peak_source": peak_src, "traffic": None,
+                         "algorithmic_flops_per_launch": flops,
+                         "executed_flops_per_launch": 3.5 * w.flops},
+            "gpu_launches": 3 * args.steps, "clocks": clocks.summary()}), flush=True)
     return 0
 
 
@@ -425,7 +474,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
-    ap.add_argument("--op", default=None, choices=sorted(ROWOP_WORKLOADS),
+    ap.add_argument("--op", default=None, choices=sorted(ROWOP_WORKLOADS) + BWD_WORKLOADS,
                     help="time a standalone row softmax / row sum workload instead")
     ap.add_argument("--split", default="auto", choices=["auto", "off"],
                     help="key-range split when the library recommends one (auto) or never")
@@ -433,6 +482,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.op and args.op.startswith("bwd_"):
+        return run_bwd(args, world, rank, local)
     if args.op:
         return run_rowop(args, world, rank, local)
     return run_gpu(args, world, rank, local)

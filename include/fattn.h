@@ -166,6 +166,27 @@ fattn_status_t attn_fwd_simt(const void *q, const void *k, const void *v, void *
                              struct CUstream_st *stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd: dq, dk, dv (bf16 [B][H][N][d]) for the
+ * upstream gradient dout (bf16 [B][H][N][d]), from the forward's inputs and
+ * its saved outputs o (bf16) and lse (fp32 [B][H][N]), as the autograd
+ * wrapper of "OpenAI Triton: from introduction to model practice", section
+ * 6, saves and passes them.  The scores are recomputed from q, k and lse:
+ *   P = exp(scale Q K^T - lse) (masked entries 0),  D_i = dO_i . O_i,
+ *   dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ * P and dS are rounded to bf16 for the products that use them; accumulation
+ * is fp32.  Same B, H, N, d, scale, causal rules as attn_fwd.  workspace is
+ * caller-owned device scratch of at least attn_bwd_workspace_size(...) bytes
+ * (B*H*N*4; contents ignored on entry, undefined on exit), 16-byte aligned.
+ * dq, dk, dv and the workspace must not overlap each other or any input.
+ * Three kernels are enqueued on `stream`.  Errors as for attn_fwd.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+fattn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                        int H, int N, int d, float scale, int causal, void *workspace,
+                        size_t workspace_bytes, struct CUstream_st *stream);
+
+/*
  * Standalone row softmax and row sum (HBM-bound), after the row softmax and
  * row-sum examples of "CS336 lecture 6: kernels and Triton":
  *   fattn_softmax_rows: y[i][j] = exp(x[i][j] - max_k x[i][k]) / sum_k exp(x[i][k] - max_k x[i][k])

@@ -22,9 +22,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfattn.so")
 
-SOURCES = ["fattn_api.cu", "fattn_fwd_sm103.cu", "fattn_fwd_simt.cu", "fattn_rowops.cu"]
+SOURCES = ["fattn_api.cu", "fattn_fwd_sm103.cu", "fattn_bwd_sm103.cu", "fattn_fwd_simt.cu",
+           "fattn_rowops.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
-EXPORTS = "{ global: attn_fwd*; fattn_*; local: *; };\n"
+EXPORTS = "{ global: attn_fwd*; attn_bwd*; fattn_*; local: *; };\n"
 
 
 def nvcc() -> str:

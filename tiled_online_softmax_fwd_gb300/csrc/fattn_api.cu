@@ -382,6 +382,77 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
                          kNoAllocScratchBytes, stream);
 }
 
+size_t attn_bwd_workspace_size(int B, int H, int N, int d)
+{
+    bool empty = false;
+    if (check_shape(B, H, N, d, 1.0f, 0, &empty) != FATTN_OK || empty)
+        return 0;
+    return static_cast<size_t>(B) * H * N * sizeof(float);
+}
+
+fattn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                        const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                        int H, int N, int d, float scale, int causal, void *workspace,
+                        size_t workspace_bytes, struct CUstream_st *stream)
+{
+    bool empty = false;
+    fattn_status_t s = check_shape(B, H, N, d, scale, causal, &empty);
+    if (s != FATTN_OK || empty)
+        return s;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    const size_t tb = rows * d * 2, lb = rows * 4;
+    const void *ins[6] = {q, k, v, o, lse, dout};
+    const size_t in_bytes[6] = {tb, tb, tb, tb, lb, tb};
+    void *outs[4] = {dq, dk, dv, workspace};
+    const size_t out_bytes[4] = {tb, tb, tb, lb};
+    for (const void *p : ins)
+        if (!p || !aligned16(p))
+            return FATTN_ERR_INVALID_ARG;
+    for (void *p : outs)
+        if (!p || !aligned16(p))
+            return FATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < lb)
+        return FATTN_ERR_INVALID_ARG;
+    // Outputs (and the scratch) overlap neither each other nor any input.
+    for (int a = 0; a < 4; ++a) {
+        for (int i = 0; i < 6; ++i)
+            if (overlap(outs[a], out_bytes[a], ins[i], in_bytes[i]))
+                return FATTN_ERR_INVALID_ARG;
+        for (int c = a + 1; c < 4; ++c)
+            if (overlap(outs[a], out_bytes[a], outs[c], out_bytes[c]))
+                return FATTN_ERR_INVALID_ARG;
+    }
+    int dev = 0;
+    DeviceInfo info;
+    if ((s = current_device(&dev, &info)) != FATTN_OK)
+        return s;
+    for (const void *p : ins)
+        if ((s = check_device_buffer(p, dev)) != FATTN_OK)
+            return s;
+    for (void *p : outs)
+        if ((s = check_device_buffer(p, dev)) != FATTN_OK)
+            return s;
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    if ((s = get_encoder(&encode)) != FATTN_OK)
+        return s;
+    fattn::FwdMaps maps;
+    fattn::BwdMaps bmaps;
+    const long long BH = static_cast<long long>(B) * H;
+    if ((s = make_map(encode, &maps.q, q, N, d, BH)) != FATTN_OK ||
+        (s = make_map(encode, &maps.k, k, N, d, BH)) != FATTN_OK ||
+        (s = make_map(encode, &maps.v, v, N, d, BH)) != FATTN_OK ||
+        (s = make_map(encode, &bmaps.dout, dout, N, d, BH)) != FATTN_OK)
+        return s;
+    uint32_t *status = nullptr;
+    cudaError_t e = fattn::status_word_address(&status);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    fattn::BwdArgs a{q, k, v, o, dout, lse, dq, dk, dv, static_cast<float *>(workspace), status,
+                     B, H, N, d, scale, causal};
+    e = fattn::launch_bwd_sm103(a, maps, bmaps, info.num_sms, stream);
+    return e == cudaSuccess ? FATTN_OK : cuda_fail(e);
+}
+
 static fattn_status_t rowop(bool softmax, const void *x, void *y, int M, int N, int dtype,
                             cudaStream_t stream)
 {

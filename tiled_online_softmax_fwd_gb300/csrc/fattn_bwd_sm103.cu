@@ -1,0 +1,564 @@
+// fattn_bwd_sm103.cu -- gradients of the attention forward pass on GB300.
+//
+// The backward that "OpenAI Triton: from introduction to model practice"
+// (section 6) wraps around the forward, from the saved q, k, v, o and lse:
+// the scores are recomputed, never stored.  With P = exp(scale*Q K^T - lse)
+// (masked entries 0) and D_i = dO_i . O_i:
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,
+//   dK = scale dS^T Q.
+// Three kernels:
+//   prep_kernel    D_i = dO_i . O_i into the caller's scratch (fp32).
+//   dkdv_kernel    one CTA per 128-row key tile j (persistent, heaviest
+//                  first): for every query tile i it computes S^T = K_j Q_i^T
+//                  and dP^T = V_j dO_i^T on the tensor cores (keys on TMEM
+//                  lanes), one thread per key row forms P^T and dS^T in bf16
+//                  back into TMEM, and the tensor cores accumulate
+//                  dV_j += P^T dO_i and dK_j += dS^T Q_i in TMEM.
+//   dq_kernel      one CTA per 128-row query tile i: for every key tile j,
+//                  S = Q_i K_j^T and dP = dO_i V_j^T, one thread per query
+//                  row forms dS in bf16, and dQ_i += dS K_j.
+// S and dP are computed twice (once per kernel) so that neither kernel needs
+// atomics or an fp32 dQ accumulator in memory.  The roles are those of the
+// forward kernel: a TMA producer warp, a warp-converged MMA warp with one
+// elected issuing lane, and one warpgroup for the elementwise work, with every
+// wait bounded.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fattn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace fattn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kTile = 128;
+constexpr int kThreads = 192;  // warps 0-3 elementwise, 4 producer, 5 MMA
+constexpr int kWarpLoad = 4;
+constexpr int kWarpMma = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kChunkBytes = kTile * 64 * 2;
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256;
+
+template <int D>
+struct BCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;  // one [128][D] bf16 tile
+    // smem: two resident tiles + 2 stages of two streamed tiles.
+    static constexpr uint32_t kTilesBytes = 6 * kTileBytes;
+    static constexpr uint32_t kColAcc1 = kColAcc0 + D;
+};
+
+struct BBars {
+    uint64_t res_full, res_empty;  // the CTA's resident pair (K_j,V_j or Q_i,dO_i)
+    uint64_t st_full[2], st_empty[2];
+    uint64_t s_full, p_full, o_full, o_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    float lse2[2][kTile];  // dkdv: per query tile, lse * log2(e) and D
+    float dd[2][kTile];
+};
+
+struct BParams {
+    const __nv_bfloat16 *o, *dout;
+    const float *lse;
+    float *dvec;  // D = rowsum(dO * O), fp32 [B*H*N]
+    __nv_bfloat16 *g0, *g1;  // dkdv: dK, dV   dq: dQ, unused
+    uint32_t *status;
+    int N, BH, T;  // T = tiles per head
+    int units;
+    int causal;
+    float scale, sl2;
+};
+
+__device__ __forceinline__ void fail(const BParams &p, BBars &b, uint32_t role)
+{
+    const uint32_t code = 4u | (role << 8) | ((blockIdx.x & 0xffffu) << 16);
+    atomicCAS(p.status, 0u, code);
+    *reinterpret_cast<volatile int *>(&b.abort) = 1;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int *abort)
+{
+    const bool ok = mbar_wait(bar, parity, kWaitLimitNs, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ int deal(int round, int cta, int grid)
+{
+    return round * grid + ((round & 1) ? grid - 1 - cta : cta);
+}
+
+// Tiles that interact with resident tile `own` (the loop range of the CTA):
+// dkdv (key tile own): query tiles [causal ? own : 0, T); dq (query tile own):
+// key tiles [0, causal ? own + 1 : T).
+template <bool kDkDv>
+__device__ __forceinline__ void loop_range(const BParams &p, int own, int &lo, int &hi)
+{
+    if (kDkDv) {
+        lo = p.causal ? own : 0;
+        hi = p.T;
+    } else {
+        lo = 0;
+        hi = p.causal ? own + 1 : p.T;
+    }
+}
+
+// Unit k -> (head, resident tile), heaviest first.
+template <bool kDkDv>
+__device__ __forceinline__ void unit_of(const BParams &p, int k, int &bh, int &own)
+{
+    bh = k % p.BH;
+    own = kDkDv ? k / p.BH : p.T - 1 - k / p.BH;
+}
+
+// ------------------------------------------------------------------ MMA helpers
+// [128 x D] x [128 x D]^T, both K-major 128-byte-swizzled tiles, into 128
+// fp32 TMEM columns.
+template <int D>
+__device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint32_t a_smem, uint32_t b_smem)
+{
+    constexpr uint32_t idesc = idesc_bf16_f32(kTile, kTile, false);
+    constexpr uint32_t hi = smem_desc_hi(1024);
+    const uint32_t a_lo = smem_desc_lo(a_smem, 16), b_lo = smem_desc_lo(b_smem, 16);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss_w(tmem_d, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// TMEM [128 x 128] (bf16 pairs) x smem tile [128 x D] (D contiguous, i.e.
+// MN-major B) into D fp32 TMEM columns.
+template <int D>
+__device__ __forceinline__ void mma_tn(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_smem,
+                                       bool accumulate)
+{
+    constexpr uint32_t idesc = idesc_bf16_f32(kTile, D, true);
+    constexpr uint32_t lbo = D == 128 ? kChunkBytes : 1024;
+    constexpr uint32_t hi = smem_desc_hi(1024);
+    const uint32_t b_lo = smem_desc_lo(b_smem, lbo);
+    const uint32_t acc0 = accumulate ? 1u : 0u;
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ts_w(tmem_d, tmem_a + kk * 8, b_lo + ((kk * 16 * 128) >> 4), hi, idesc,
+                 kk > 0 ? 1u : acc0);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ------------------------------------------------------------------ roles
+// Producer: the resident pair (A0, A1) once per unit, then the streamed pairs
+// (B0, B1) of every tile of the loop range into a two-stage ring.
+template <int D, bool kDkDv>
+__device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtensorMap *ra0,
+                         const CUtensorMap *ra1, const CUtensorMap *sb0, const CUtensorMap *sb1)
+{
+    using C = BCfg<D>;
+    const volatile int *abort = &b.abort;
+    const bool leader = elect_one();
+    uint32_t res_phase = 0, pos = 0;
+    bool ok = true;
+    int res_issued = 0;
+    for (int r = 0; ok; ++r) {
+        const int k = deal(r, blockIdx.x, gridDim.x);
+        if (k >= p.units)
+            break;
+        int bh, own, lo, hi;
+        unit_of<kDkDv>(p, k, bh, own);
+        loop_range<kDkDv>(p, own, lo, hi);
+        if (!warp_wait(smem_addr(&b.res_empty), res_phase ^ 1, abort)) {
+            ok = false;
+            break;
+        }
+        res_phase ^= 1;
+        if (leader) {
+            const uint32_t full = smem_addr(&b.res_full);
+            mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(smem + c * kChunkBytes, ra0, full, 64 * c, own * kTile, bh);
+                tma_load_3d(smem + C::kTileBytes + c * kChunkBytes, ra1, full, 64 * c, own * kTile,
+                            bh);
+            }
+        }
+        ++res_issued;
+        for (int t = lo; ok && t < hi; ++t, ++pos) {
+            const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
+            if (!warp_wait(smem_addr(&b.st_empty[stage]), phase ^ 1, abort)) {
+                ok = false;
+                break;
+            }
+            if (leader) {
+                const uint32_t full = smem_addr(&b.st_full[stage]);
+                const uint32_t dst = smem + (2 + 2 * stage) * C::kTileBytes;
+                mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(dst + c * kChunkBytes, sb0, full, 64 * c, t * kTile, bh);
+                    tma_load_3d(dst + C::kTileBytes + c * kChunkBytes, sb1, full, 64 * c, t * kTile,
+                                bh);
+                }
+            }
+        }
+    }
+    if (!ok) {
+        if (leader)
+            fail(p, b, kRoleLoad);
+        for (uint32_t q = pos > 2 ? pos - 2 : 0; q < pos; ++q)
+            mbar_wait(smem_addr(&b.st_full[q & 1]), (q >> 1) & 1, kWaitLimitNs / 8, nullptr);
+        if (res_issued > 0)
+            mbar_wait(smem_addr(&b.res_full), res_phase ^ 1, kWaitLimitNs / 8, nullptr);
+    }
+}
+
+// MMA issuer.  dkdv: S^T = K Q^T (cols 0-127), dP^T = V dO^T (128-255); then
+// dV += P^T dO (acc0), dK += dS^T Q (acc1).  dq: S = Q K^T, dP = dO V^T; then
+// dQ += dS K (acc0).
+template <int D, bool kDkDv>
+__device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem)
+{
+    using C = BCfg<D>;
+    const volatile int *abort = &b.abort;
+    const bool leader = elect_one();
+    uint32_t res_phase = 0, s_phase = 0, oe_phase = 0, pos = 0;
+    bool ok = true;
+    auto commit = [&](uint64_t &bar) {
+        if (leader)
+            mma_commit(smem_addr(&bar));
+    };
+    const uint32_t a0 = smem, a1 = smem + C::kTileBytes;  // resident pair
+    for (int r = 0; ok; ++r) {
+        const int k = deal(r, blockIdx.x, gridDim.x);
+        if (k >= p.units)
+            break;
+        int bh, own, lo, hi;
+        unit_of<kDkDv>(p, k, bh, own);
+        loop_range<kDkDv>(p, own, lo, hi);
+        ok = warp_wait(smem_addr(&b.res_full), res_phase, abort);
+        res_phase ^= 1;
+        if (ok)
+            ok = warp_wait(smem_addr(&b.o_empty), oe_phase ^ 1, abort);
+        oe_phase ^= 1;
+        if (!ok)
+            break;
+        for (int t = lo; ok && t < hi; ++t, ++pos) {
+            const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
+            ok = warp_wait(smem_addr(&b.st_full[stage]), phase, abort);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t b0 = smem + (2 + 2 * stage) * C::kTileBytes, b1 = b0 + C::kTileBytes;
+            if (leader) {
+                mma_nt<D>(tmem + kColS, a0, b0);   // S^T = K Q^T  |  S = Q K^T
+                mma_nt<D>(tmem + kColDP, a1, b1);  // dP^T = V dO^T | dP = dO V^T
+            }
+            commit(b.s_full);
+            if (t == hi - 1)
+                commit(b.res_empty);  // resident pair no longer read
+            ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
+            s_phase ^= 1;
+            if (!ok)
+                break;
+            tc_fence_after();
+            if (leader) {
+                if (kDkDv) {
+                    mma_tn<D>(tmem + kColAcc0, tmem + kColS, b1, t > lo);          // dV += P^T dO
+                    mma_tn<D>(tmem + C::kColAcc1, tmem + kColDP, b0, t > lo);      // dK += dS^T Q
+                } else {
+                    mma_tn<D>(tmem + kColAcc0, tmem + kColS, b0, t > lo);          // dQ += dS K
+                }
+            }
+            commit(b.st_empty[stage]);
+            if (t == hi - 1)
+                commit(b.o_full);
+        }
+    }
+    if (!ok && leader)
+        fail(p, b, kRoleMma);
+    commit(b.drain);
+    mbar_wait(smem_addr(&b.drain), 0, kWaitLimitNs, nullptr);
+}
+
+// Elementwise warpgroup: thread r owns TMEM lane r = row `own*128 + r` of the
+// resident tile (a key in dkdv, a query in dq).
+template <int D, bool kDkDv>
+__device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
+{
+    using C = BCfg<D>;
+    const volatile int *abort = &b.abort;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int r = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t s_phase = 0, of_phase = 0;
+    int xbuf = 0;
+    bool ok = true;
+    for (int rr = 0; ok; ++rr) {
+        const int k = deal(rr, blockIdx.x, gridDim.x);
+        if (k >= p.units)
+            break;
+        int bh, own, lo, hi;
+        unit_of<kDkDv>(p, k, bh, own);
+        loop_range<kDkDv>(p, own, lo, hi);
+        const int row = own * kTile + r;                    // this thread's row
+        const size_t head = static_cast<size_t>(bh) * p.N;
+        float my_lse2 = 0.f, my_d = 0.f;
+        if (!kDkDv && row < p.N) {
+            my_lse2 = p.lse[head + row] * kLog2e;
+            my_d = p.dvec[head + row];
+        }
+        for (int t = lo; ok && t < hi; ++t) {
+            if (kDkDv) {
+                // lse and D of the 128 queries of tile t, shared through smem
+                // (double-buffered; a 128-thread barrier publishes them).
+                const int qrow = t * kTile + r;
+                b.lse2[xbuf][r] = qrow < p.N ? p.lse[head + qrow] * kLog2e : 0.f;
+                b.dd[xbuf][r] = qrow < p.N ? p.dvec[head + qrow] : 0.f;
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+            ok = mbar_wait(smem_addr(&b.s_full), s_phase, kWaitLimitNs, abort);
+            s_phase ^= 1;
+            if (!ok)
+                break;
+            tc_fence_after();
+            // Column c of this row pairs row `row` of the resident tile with
+            // row t*128+c of the streamed one.  Valid: inside N and, under the
+            // causal mask, query >= key.
+            const int col0 = t * kTile;
+            int c_lo = 0, c_hi = kTile - 1;  // valid columns [c_lo, c_hi]
+            if (kDkDv) {
+                if (p.causal && t == own)
+                    c_lo = r;  // query t*128+c >= key own*128+r
+            } else {
+                if (p.causal && t == own)
+                    c_hi = r;  // key t*128+c <= query own*128+r
+            }
+            c_hi = min(c_hi, p.N - 1 - col0);
+#pragma unroll 1
+            for (int ch = 0; ch < kTile / 32; ++ch) {
+                uint32_t sr[32], dr[32];
+                __syncwarp();
+                tmem_ld32(tmem + lane_off + kColS + ch * 32, sr);
+                tmem_ld32(tmem + lane_off + kColDP + ch * 32, dr);
+                tmem_wait_ld();
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = ch * 32 + 2 * i + h;
+                        const float l2 = kDkDv ? b.lse2[xbuf][c] : my_lse2;
+                        const float dd = kDkDv ? b.dd[xbuf][c] : my_d;
+                        const bool valid = c >= c_lo && c <= c_hi;
+                        const float pe = valid ? ex2(fmaf(__uint_as_float(sr[2 * i + h]), p.sl2, -l2))
+                                               : 0.f;
+                        pv[h] = pe;
+                        dsv[h] = pe * (__uint_as_float(dr[2 * i + h]) - dd);
+                    }
+                    pk[i] = pack2(pv[0], pv[1]);
+                    dk[i] = pack2(dsv[0], dsv[1]);
+                }
+                if (kDkDv) {  // P^T over S, dS^T over dP
+                    tmem_st16(tmem + lane_off + kColS + ch * 16, pk);
+                    tmem_st16(tmem + lane_off + kColDP + ch * 16, dk);
+                } else {      // dS over S
+                    tmem_st16(tmem + lane_off + kColS + ch * 16, dk);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&b.p_full));
+            xbuf ^= 1;
+        }
+        if (!ok)
+            break;
+        // Epilogue: the accumulators -> bf16 rows (dK and dQ times scale).
+        ok = mbar_wait(smem_addr(&b.o_full), of_phase, kWaitLimitNs, abort);
+        of_phase ^= 1;
+        if (!ok)
+            break;
+        tc_fence_after();
+        const bool live = row < p.N;
+#pragma unroll 1
+        for (int which = 0; which < (kDkDv ? 2 : 1); ++which) {
+            // dkdv: which 0 = dV (acc0, unscaled) -> g1, which 1 = dK (acc1) -> g0
+            const uint32_t col = which == 0 ? kColAcc0 : C::kColAcc1;
+            const float f = (kDkDv && which == 0) ? 1.f : p.scale;
+            __nv_bfloat16 *dst = ((kDkDv && which == 0) ? p.g1 : p.g0) + (head + row) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(tmem + lane_off + col + c * 32, o);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack2(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
+                if (live) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&b.o_empty));
+    }
+    if (!ok)
+        fail(p, b, kRoleSoftmax);
+}
+
+template <int D, bool kDkDv>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap ra0, const __grid_constant__ CUtensorMap ra1,
+               const __grid_constant__ CUtensorMap sb0, const __grid_constant__ CUtensorMap sb1,
+               const BParams p)
+{
+    using C = BCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t smem = (raw + 1023u) & ~1023u;
+    BBars &b = *reinterpret_cast<BBars *>(smem_raw + (smem - raw) + C::kTilesBytes);
+    const int warp = threadIdx.x / 32;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&b.res_full), 1);
+        mbar_init(smem_addr(&b.res_empty), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_addr(&b.st_full[s]), 1);
+            mbar_init(smem_addr(&b.st_empty[s]), 1);
+        }
+        mbar_init(smem_addr(&b.s_full), 1);
+        mbar_init(smem_addr(&b.p_full), 4);
+        mbar_init(smem_addr(&b.o_full), 1);
+        mbar_init(smem_addr(&b.o_empty), 4);
+        mbar_init(smem_addr(&b.drain), 1);
+        b.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_addr(&b.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = b.tmem_base;
+    if (warp < 4)
+        bwd_elem<D, kDkDv>(p, b, tmem);
+    else if (warp == kWarpLoad)
+        bwd_load<D, kDkDv>(p, b, smem, &ra0, &ra1, &sb0, &sb1);
+    else
+        bwd_mma<D, kDkDv>(p, b, smem, tmem);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// D_i = dO_i . O_i (fp32), one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+    prep_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
+                float *__restrict__ dvec, long long rows)
+{
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+    if (row >= rows)
+        return;
+    const int lane = threadIdx.x & 31;
+    constexpr int kPer = D / 32;  // 2 or 4 elements per lane
+    const __nv_bfloat16 *orow = o + row * D + lane * kPer;
+    const __nv_bfloat16 *drow = dout + row * D + lane * kPer;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        acc = fmaf(__bfloat162float(orow[i]), __bfloat162float(drow[i]), acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0)
+        dvec[row] = acc;
+}
+
+template <int D, bool kDkDv>
+cudaError_t launch_one(const CUtensorMap &ra0, const CUtensorMap &ra1, const CUtensorMap &sb0,
+                       const CUtensorMap &sb1, const BParams &p, int num_sms, cudaStream_t stream)
+{
+    using C = BCfg<D>;
+    const size_t smem = C::kTilesBytes + sizeof(BBars) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kDkDv>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    const int grid = p.units < num_sms ? p.units : num_sms;
+    bwd_kernel<D, kDkDv><<<grid, kThreads, smem, stream>>>(ra0, ra1, sb0, sb1, p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd(const BwdArgs &a, const FwdMaps &m, const BwdMaps &mb, int num_sms,
+                       cudaStream_t stream)
+{
+    BParams p;
+    p.o = static_cast<const __nv_bfloat16 *>(a.o);
+    p.dout = static_cast<const __nv_bfloat16 *>(a.dout);
+    p.lse = a.lse;
+    p.dvec = a.dvec;
+    p.status = a.status;
+    p.N = a.N;
+    p.BH = a.B * a.H;
+    p.T = (a.N + kTile - 1) / kTile;
+    const long long units = static_cast<long long>(p.BH) * p.T;
+    if (units == 0)
+        return cudaSuccess;
+    if (units > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    p.units = static_cast<int>(units);
+    p.causal = a.causal;
+    p.scale = a.scale;
+    p.sl2 = a.scale * kLog2e;
+    const long long rows = static_cast<long long>(p.BH) * p.N;
+    prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p.o, p.dout, p.dvec,
+                                                                              rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    // dK, dV: resident (K, V), streamed (Q, dO).
+    p.g0 = static_cast<__nv_bfloat16 *>(a.dk);
+    p.g1 = static_cast<__nv_bfloat16 *>(a.dv);
+    if ((e = launch_one<D, true>(m.k, m.v, m.q, mb.dout, p, num_sms, stream)) != cudaSuccess)
+        return e;
+    // dQ: resident (Q, dO), streamed (K, V).
+    p.g0 = static_cast<__nv_bfloat16 *>(a.dq);
+    p.g1 = nullptr;
+    return launch_one<D, false>(m.q, mb.dout, m.k, m.v, p, num_sms, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_sm103(const BwdArgs &a, const FwdMaps &m, const BwdMaps &mb, int num_sms,
+                             cudaStream_t stream)
+{
+    return a.d == 64 ? launch_bwd<64>(a, m, mb, num_sms, stream)
+                     : launch_bwd<128>(a, m, mb, num_sms, stream);
+}
+
+}  // namespace fattn

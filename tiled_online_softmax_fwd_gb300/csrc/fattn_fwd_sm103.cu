@@ -779,6 +779,14 @@ cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+cudaError_t status_word_address(uint32_t **out)
+{
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_fattn_status);
+    *out = static_cast<uint32_t *>(ptr);
+    return e;
+}
+
 cudaError_t read_and_clear_status(uint32_t *out, cudaStream_t stream)
 {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fattn_status, sizeof(uint32_t), 0,

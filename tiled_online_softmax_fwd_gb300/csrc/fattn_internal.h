@@ -55,6 +55,26 @@ cudaError_t read_and_clear_status(uint32_t *out, cudaStream_t stream);
 // the tests as a cross-check.  Not used by attn_fwd.
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t stream);
 
+// Backward pass (dQ, dK, dV) of the forward above.  dvec is scratch for
+// D = rowsum(dO * O) (fp32, B*H*N); status is the device status word.
+struct BwdArgs {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    float *dvec;
+    uint32_t *status;
+    int B, H, N, d;
+    float scale;
+    int causal;
+};
+struct BwdMaps {
+    CUtensorMap dout;  // same geometry as FwdMaps
+};
+cudaError_t launch_bwd_sm103(const BwdArgs &a, const FwdMaps &m, const BwdMaps &mb, int num_sms,
+                             cudaStream_t stream);
+// Device address of the status word on the current device.
+cudaError_t status_word_address(uint32_t **out);
+
 // Row softmax / row sum over a contiguous [M][N] matrix of fp32 (dtype 0) or
 // bf16 (dtype 1); the softmax output has the input's type, the sums are fp32.
 cudaError_t launch_softmax_rows(const void *x, void *y, int M, int N, int dtype, int num_sms,

@@ -21,7 +21,8 @@ _LIB_PATH = os.path.join(_HERE, "_build", "libfattn.so")
 FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
                 3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
-EXPORTED = ["attn_fwd", "attn_fwd_host", "attn_fwd_simt", "attn_fwd_split",
+EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_host", "attn_fwd_simt",
+            "attn_fwd_split",
             "attn_fwd_split_count", "attn_fwd_split_noalloc", "attn_fwd_split_workspace_size",
             "fattn_status_string",
             "fattn_last_cuda_error", "fattn_get_device_status", "fattn_row_sum",
@@ -73,6 +74,10 @@ def load():
         lib.attn_fwd_split_count.argtypes = [ip, ip, ip, ip, ip]
         lib.attn_fwd_split_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_split_workspace_size.argtypes = [ip, ip, ip, ip, ip]
+        lib.attn_bwd.restype = ctypes.c_int
+        lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, fp, ip, vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.attn_bwd_workspace_size.argtypes = [ip, ip, ip, ip]
         lib.attn_fwd_host.restype = ctypes.c_int
         lib.attn_fwd_host.argtypes = [vp] * 10 + [ip, ip, ip, ip, fp, ip, vp]
         lib.fattn_status_string.restype = ctypes.c_char_p
@@ -208,6 +213,38 @@ def attn_fwd_split(q, k, v, causal: bool = False, scale: float | None = None,
                                 _stream_handle(stream, q.device))
     _check(st, "attn_fwd_split")
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+             workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for the upstream gradient dout, from
+    the forward's inputs and saved outputs o, lse (libfattn attn_bwd).  The
+    scratch for D = rowsum(dO * O) is allocated here with torch when not
+    given (the library itself never allocates)."""
+    _validate(q, k, v)
+    B, H, N, d = q.shape
+    for name, t in (("o", o), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() \
+                or t.device != q.device:
+            raise ValueError("%s must be a contiguous bf16 tensor shaped like q" % name)
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if scale is None:
+        scale = default_scale(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(load().attn_bwd_workspace_size(B, H, N, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                             dv.data_ptr(), B, H, N, d, float(scale), 1 if causal else 0,
+                             workspace.data_ptr(), workspace.numel(),
+                             _stream_handle(stream, q.device))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_simt(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
