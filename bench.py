@@ -344,7 +344,7 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     fattn.load()
     w = WORKLOADS[args.workload]
-    q, k, v, rows_all = make_workload(w)
+    q, k, v, rows_all = make_workload(w, dtype=torch.float16 if args.fp16 else torch.bfloat16)
     in_digest = digest(q, k, v)
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
     do = torch.empty_like(dq)
@@ -352,8 +352,10 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     big = w.io_bytes > L2_BYTES
     flush = None if big else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    # Key-range split when the library recommends it (few work units per SM).
-    splits = 1 if args.split == "off" else fattn.split_count(w.B, w.H, w.N, w.d, w.causal, dev)
+    # Key-range split when the library recommends it (few work units per SM;
+    # bf16 only).
+    splits = 1 if (args.split == "off" or args.fp16) else fattn.split_count(w.B, w.H, w.N, w.d,
+                                                                           w.causal, dev)
     ws = None
     if splits > 1:
         ws = torch.empty(fattn.split_workspace_size(w.B, w.H, w.N, w.d, splits), dtype=torch.uint8,
@@ -363,6 +365,9 @@ def run_gpu(args, world, rank, local):
         if splits > 1:
             fattn.attn_fwd_split(dq, dk, dv, causal=w.causal, scale=w.scale, num_splits=splits,
                                  workspace=ws, out=do, lse=dl, stream=stream)
+        elif args.fp16:
+            fattn.attn_fwd_fp16(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, lse=dl,
+                                stream=stream)
         else:
             fattn.attn_fwd(dq, dk, dv, causal=w.causal, scale=w.scale, out=do, lse=dl,
                            stream=stream)
@@ -406,7 +411,7 @@ def run_gpu(args, world, rank, local):
 
     # End to end through the C ABI with host buffers (pinned), copies timed.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.fp16:
         hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
         ho = torch.empty_like(q).pin_memory()
         hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
@@ -434,8 +439,8 @@ def run_gpu(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, **w.describe(), "parallelism": "replicas" if world > 1 else "single",
+        "dtype": "f16" if args.fp16 else "bf16", "data": "synthetic",
+        "config": {"workload": w.name + ("_fp16" if args.fp16 else ""), **w.describe(), "parallelism": "replicas" if world > 1 else "single",
                    "splits": splits,
                    "l2": ("inputs larger than L2 (%d MB)" % (w.io_bytes // 10**6)) if big
                          else "L2 flushed (256 MiB write) before every step, outside the timed events",
@@ -476,6 +481,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--op", default=None, choices=sorted(ROWOP_WORKLOADS) + BWD_WORKLOADS,
                     help="time a standalone row softmax / row sum workload instead")
+    ap.add_argument("--fp16", action="store_true", help="fp16 inputs through attn_fwd_fp16")
     ap.add_argument("--split", default="auto", choices=["auto", "off"],
                     help="key-range split when the library recommends one (auto) or never")
     args = ap.parse_args()

@@ -81,6 +81,18 @@ fattn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, fl
                         struct CUstream_st *stream);
 
 /*
+ * attn_fwd_fp16 -- attn_fwd for fp16 q, k, v and o (lse stays fp32): the
+ * element type of the page-1 kernel of "Triton hand-written kernels: vector
+ * add -> tiled GEMM -> FlashAttention core" (section 4, fp16 inputs and P
+ * cast to fp16 before the second product).  P is rounded to fp16 and O is
+ * normalised by the fp32 row sum.  Same arguments, rules and errors as
+ * attn_fwd.
+ */
+fattn_status_t attn_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             struct CUstream_st *stream);
+
+/*
  * attn_fwd_host -- the same operation on HOST buffers, end to end.
  *
  * Copies q_host, k_host, v_host to the caller's device buffers dq, dk, dv,

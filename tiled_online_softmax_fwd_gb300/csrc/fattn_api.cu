@@ -142,7 +142,7 @@ fattn_status_t check_device_buffer(const void *p, int dev)
 }
 
 fattn_status_t make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m, const void *ptr,
-                        int N, int d, long long BH)
+                        int N, int d, long long BH, bool f16 = false)
 {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
@@ -150,7 +150,8 @@ fattn_status_t make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
                                    static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
     const cuuint32_t box[3] = {64, 128, 1};
     const cuuint32_t elem_strides[3] = {1, 1, 1};
-    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+    const CUresult r = encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              3, const_cast<void *>(ptr), dims,
                               strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -161,7 +162,7 @@ fattn_status_t make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
     return FATTN_OK;
 }
 
-enum class Kernel { kTcgen05, kSimt };
+enum class Kernel { kTcgen05, kTcgen05F16, kSimt };
 
 // Every check of a forward call.  On FATTN_OK, *empty tells whether there is
 // any work, and (when there is) *dev / *info describe the current device.
@@ -192,6 +193,8 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
                       const fattn::FwdSplit &split = fattn::FwdSplit{1, nullptr, nullptr})
 {
     fattn::FwdArgs a{q, k, v, o, lse, B, H, N, d, scale, causal};
+    const bool f16 = which == Kernel::kTcgen05F16;
+    a.f16 = f16 ? 1 : 0;
     cudaError_t e;
     if (which == Kernel::kSimt) {
         e = fattn::launch_fwd_simt(a, stream);
@@ -202,9 +205,9 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
             return s;
         fattn::FwdMaps maps;
         const long long BH = static_cast<long long>(B) * H;
-        if ((s = make_map(encode, &maps.q, q, N, d, BH)) != FATTN_OK ||
-            (s = make_map(encode, &maps.k, k, N, d, BH)) != FATTN_OK ||
-            (s = make_map(encode, &maps.v, v, N, d, BH)) != FATTN_OK)
+        if ((s = make_map(encode, &maps.q, q, N, d, BH, f16)) != FATTN_OK ||
+            (s = make_map(encode, &maps.k, k, N, d, BH, f16)) != FATTN_OK ||
+            (s = make_map(encode, &maps.v, v, N, d, BH, f16)) != FATTN_OK)
             return s;
         e = fattn::launch_fwd_sm103(a, maps, split, info.num_sms, stream);
     }
@@ -324,6 +327,13 @@ fattn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, fl
                         int H, int N, int d, float scale, int causal, struct CUstream_st *stream)
 {
     return forward(Kernel::kTcgen05, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+}
+
+fattn_status_t attn_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             struct CUstream_st *stream)
+{
+    return forward(Kernel::kTcgen05F16, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
 }
 
 int attn_fwd_split_count(int B, int H, int N, int d, int causal)

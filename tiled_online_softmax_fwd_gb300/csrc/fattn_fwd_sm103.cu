@@ -44,6 +44,7 @@
 // that actually enter P V, which normalises O, so that the weights applied to
 // V sum to one exactly (the rounding of a dominant p cancels in O / l_round).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "fattn_internal.h"
@@ -92,7 +93,7 @@ struct Bars {
 };
 
 struct Params {
-    __nv_bfloat16 *o;
+    void *o;       // bf16 or fp16 [B*H*N][D]
     float *lse;
     float *ws_o;   // split mode: fp32 partial O [splits][B*H*N][D]
     float2 *ws_l;  // split mode: base-2 partial lse (exact sum, rounded sum) [splits][B*H*N]
@@ -167,6 +168,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Two floats rounded to the 16-bit element type (bf16, or fp16 when kF16),
+// low half first.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if constexpr (kF16) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    } else {
+        return pack_bf16x2(lo, hi);
+    }
 }
 
 // ------------------------------------------------------------------ producer
@@ -257,10 +271,10 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
 // 64-column box, or to the next 16 KB box.  The start address occupies the
 // low 14 bits of the descriptor's low word and never carries out of them
 // (shared memory is below 256 KB), so a step is one 32-bit add.
-template <int D>
+template <int D, bool kF16>
 __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem)
 {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, kBN, false, kF16);
     constexpr uint32_t hi = smem_desc_hi(1024);
     const uint32_t a_lo = smem_desc_lo(q_smem, 16), b_lo = smem_desc_lo(k_smem, 16);
 #pragma unroll
@@ -275,11 +289,11 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32
 // halves of d = 128 is one 16 KB box (LBO; with d = 64 there is one half and
 // the value is irrelevant, so it is kept inside the tile).  P is read from
 // tensor memory, 8 columns (16 keys of bf16 pairs) per K = 16 step.
-template <int D>
+template <int D, bool kF16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_smem,
                                          bool accumulate)
 {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, D, true, kF16);
     constexpr uint32_t kVLbo = D == 128 ? kChunkBytes : 1024;
     constexpr uint32_t hi = smem_desc_hi(1024);
     const uint32_t b_lo = smem_desc_lo(v_smem, kVLbo);
@@ -290,7 +304,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint3
                  kk > 0 ? 1u : acc0);
 }
 
-template <int D>
+template <int D, bool kF16>
 __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t tmem)
 {
     using C = Cfg<D>;
@@ -333,7 +347,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
             if (u.n[t] == 0)
                 continue;
             if (leader)
-                issue_s<D>(tmem + (t == 0 ? 0u : 128u), smem_base + t * C::kTileBytes,
+                issue_s<D, kF16>(tmem + (t == 0 ? 0u : 128u), smem_base + t * C::kTileBytes,
                            kv_smem(base));
             commit(b.s_full[t]);
             if (u.n[t] == 1)
@@ -365,10 +379,10 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
                 const uint32_t col_s = t == 0 ? 0u : 128u;
                 const uint32_t col_o = t == 0 ? C::kColO0 : C::kColO1;
                 if (leader)
-                    issue_pv<D>(tmem + col_o, tmem + col_s, kv_smem(at_v), j - 1 > 0);
+                    issue_pv<D, kF16>(tmem + col_o, tmem + col_s, kv_smem(at_v), j - 1 > 0);
                 if (j < u.n[t]) {
                     if (leader)
-                        issue_s<D>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
+                        issue_s<D, kF16>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
                     commit(b.s_full[t]);
                     if (j == u.n[t] - 1)
                         commit(b.q_empty[t]);
@@ -392,7 +406,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D>
+template <int D, bool kF16>
 __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 {
     using C = Cfg<D>;
@@ -475,11 +489,12 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                     f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm),
                               x0, x1);
                     const float p0 = ex2(x0), p1 = ex2(x1);
-                    pk[i] = pack_bf16x2(p0, p1);
+                    pk[i] = pack2<kF16>(p0, p1);
                     sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
-                    sum_round[i & 1] =
-                        f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                         __uint_as_float(pk[i] & 0xffff0000u)));
+                    if constexpr (!kF16)
+                        sum_round[i & 1] =
+                            f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                             __uint_as_float(pk[i] & 0xffff0000u)));
                 }
                 tmem_st16(t_s + c * 16, pk);
             }
@@ -519,11 +534,13 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         if (!ok)
             break;
         tc_fence_after();
-        const float inv_l = 1.f / l_round;
+        // fp16 P is rounded 8x more finely than bf16 P: O is normalised by
+        // the exact sum there.
+        const float inv_l = 1.f / (kF16 ? l : l_round);
         const bool live = row < p.N;
         const size_t grow = static_cast<size_t>(u.bh) * p.N + row;
         if (p.splits == 1) {
-            __nv_bfloat16 *orow = p.o + grow * D;
+            uint16_t *orow = static_cast<uint16_t *>(p.o) + grow * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -533,7 +550,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                    pk[i] = pack2<kF16>(__uint_as_float(o[2 * i]) * inv_l,
                                         __uint_as_float(o[2 * i + 1]) * inv_l);
                 if (live) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
@@ -576,7 +593,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const Params p)
@@ -621,11 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = b.tmem_base;
 
     if (warp < 8) {
-        run_softmax<D>(p, b, tmem, warp / 4);
+        run_softmax<D, kF16>(p, b, tmem, warp / 4);
     } else if (warp == kWarpLoad) {
         run_load<D>(p, b, smem_base, &mq, &mk, &mv);
     } else if (warp == kWarpMma) {
-        run_mma<D>(p, b, smem_base, tmem);
+        run_mma<D, kF16>(p, b, smem_base, tmem);
     }
 
     tc_fence_before();
@@ -646,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   O   = sum_s w_s O_s,  w_s = 2^lr_s / sum_s' 2^lr_s'
 // Splits with no key tile for the row's Q tile are skipped (the same ranges
 // as unit_at).  One warp per row; lane l owns D/32 consecutive columns.
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_l, const Params p)
 {
@@ -689,22 +706,21 @@ __global__ void __launch_bounds__(256)
             acc[c] = fmaf(w, src[c], acc[c]);
     }
     const float inv = 1.f / sr;
-    __nv_bfloat16 *dst = p.o + static_cast<size_t>(row) * D + lane * kCols;
+    uint16_t *dst = static_cast<uint16_t *>(p.o) + static_cast<size_t>(row) * D + lane * kCols;
 #pragma unroll
     for (int c = 0; c < kCols; c += 2)
-        *reinterpret_cast<__nv_bfloat162 *>(dst + c) =
-            __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
+        *reinterpret_cast<uint32_t *>(dst + c) = pack2<kF16>(acc[c] * inv, acc[c + 1] * inv);
     if (lane == 0)
         p.lse[row] = (mx_e + log2f(se)) * kLn2;
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split, int num_sms,
                    cudaStream_t stream)
 {
     using C = Cfg<D>;
     Params p;
-    p.o = static_cast<__nv_bfloat16 *>(a.o);
+    p.o = a.o;
     p.lse = a.lse;
     p.ws_o = split.ws_o;
     p.ws_l = reinterpret_cast<float2 *>(split.ws_l);
@@ -723,19 +739,20 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     p.causal = a.causal;
     p.sl2 = a.scale * kLog2e;
     const size_t smem = C::kTilesBytes + sizeof(Bars) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-    fwd_kernel<D><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
+    fwd_kernel<D, kF16><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
         return e;
     const long long rows = static_cast<long long>(p.BH) * p.N;
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    combine_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p.ws_o, p.ws_l, p);
+    combine_kernel<D, kF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p.ws_o, p.ws_l, p);
     return cudaGetLastError();
 }
 
@@ -744,8 +761,11 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
 cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
                              int num_sms, cudaStream_t stream)
 {
-    return a.d == 64 ? launch<64>(a, maps, split, num_sms, stream)
-                     : launch<128>(a, maps, split, num_sms, stream);
+    if (a.f16)
+        return a.d == 64 ? launch<64, true>(a, maps, split, num_sms, stream)
+                         : launch<128, true>(a, maps, split, num_sms, stream);
+    return a.d == 64 ? launch<64, false>(a, maps, split, num_sms, stream)
+                     : launch<128, false>(a, maps, split, num_sms, stream);
 }
 
 namespace {

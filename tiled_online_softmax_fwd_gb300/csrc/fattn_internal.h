@@ -17,6 +17,7 @@ struct FwdArgs {
     int B, H, N, d;
     float scale;
     int causal;
+    int f16 = 0;  // 1: fp16 q, k, v, o (P in fp16); 0: bf16
 };
 
 // Tensor maps over Q, K, V viewed as 3-D bf16 arrays (d, N, B*H), box

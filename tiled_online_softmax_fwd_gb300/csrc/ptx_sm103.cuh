@@ -349,14 +349,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
     return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5  D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format
-//   bit 15    A major (0 = K-major); bit 16 B major (1 = MN-major)
-//   bits 17-22 N >> 3; bits 24-28 M >> 4
+// Instruction descriptor for kind::f16 with 16-bit A/B and fp32 D.
+//   bits 4-5  D format (1 = f32); 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B always the same); bit 15 A major (0 = K-major);
+//   bit 16 B major (1 = MN-major); bits 17-22 N >> 3; bits 24-28 M >> 4
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn_major, bool f16)
+{
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+    return idesc_f32acc(M, N, b_mn_major, false);
 }
 
 }  // namespace ptx

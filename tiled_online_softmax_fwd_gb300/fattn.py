@@ -21,7 +21,8 @@ _LIB_PATH = os.path.join(_HERE, "_build", "libfattn.so")
 FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
                 3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
-EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_host", "attn_fwd_simt",
+EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_fp16", "attn_fwd_host",
+            "attn_fwd_simt",
             "attn_fwd_split",
             "attn_fwd_split_count", "attn_fwd_split_noalloc", "attn_fwd_split_workspace_size",
             "fattn_status_string",
@@ -62,7 +63,7 @@ def load():
         lib = ctypes.CDLL(_LIB_PATH)
         vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         fwd_args = [vp, vp, vp, vp, vp, ip, ip, ip, ip, fp, ip, vp]
-        for name in ("attn_fwd", "attn_fwd_simt"):
+        for name in ("attn_fwd", "attn_fwd_fp16", "attn_fwd_simt"):
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = fwd_args
@@ -115,14 +116,14 @@ def _stream_handle(stream, device) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _validate(q, k, v):
+def _validate(q, k, v, dtype=torch.bfloat16):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor):
             raise TypeError("%s must be a torch.Tensor" % name)
         if not t.is_cuda:
             raise ValueError("%s must be a CUDA tensor" % name)
-        if t.dtype != torch.bfloat16:
-            raise ValueError("%s must be bfloat16, got %s" % (name, t.dtype))
+        if t.dtype != dtype:
+            raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
         if t.dim() != 4:
             raise ValueError("%s must be [B, H, N, d]" % name)
         if not t.is_contiguous():
@@ -136,7 +137,8 @@ def _validate(q, k, v):
 
 
 def _forward(entry: str, q, k, v, causal, scale, out, lse, stream):
-    _validate(q, k, v)
+    dtype = torch.float16 if entry == "attn_fwd_fp16" else torch.bfloat16
+    _validate(q, k, v, dtype)
     B, H, N, d = q.shape
     if scale is None:
         scale = default_scale(d)
@@ -144,9 +146,9 @@ def _forward(entry: str, q, k, v, causal, scale, out, lse, stream):
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+    if out.shape != q.shape or out.dtype != dtype or not out.is_contiguous() \
             or out.device != q.device:
-        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+        raise ValueError("out must be a contiguous tensor of q's type and shape on q's device")
     if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() \
             or lse.device != q.device:
         raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor on q's device")
@@ -245,6 +247,12 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
                              _stream_handle(stream, q.device))
     _check(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_fwd_fp16(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                  stream=None):
+    """attn_fwd for fp16 [B, H, N, d] CUDA tensors (libfattn attn_fwd_fp16)."""
+    return _forward("attn_fwd_fp16", q, k, v, causal, scale, out, lse, stream)
 
 
 def attn_fwd_simt(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

@@ -73,13 +73,14 @@ WORKLOAD_ORDER = list(WORKLOADS)
 
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int, sigma_qk: float = 1.0,
-             generator: torch.Generator | None = None):
-    """Return bf16 CPU tensors q, k, v of shape [B, H, N, d] (contiguous)."""
+             generator: torch.Generator | None = None, dtype=torch.bfloat16):
+    """Return CPU tensors q, k, v of shape [B, H, N, d] (contiguous), rounded
+    to ``dtype`` (bf16 by default, fp16 for the fp16 variant)."""
     g = generator if generator is not None else torch.Generator("cpu").manual_seed(seed)
     shape = (B, H, N, d)
-    q = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma_qk).to(torch.bfloat16)
-    k = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma_qk).to(torch.bfloat16)
-    v = torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    q = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma_qk).to(dtype)
+    k = (torch.randn(shape, generator=g, dtype=torch.float32) * sigma_qk).to(dtype)
+    v = torch.randn(shape, generator=g, dtype=torch.float32).to(dtype)
     return q.contiguous(), k.contiguous(), v.contiguous()
 
 
@@ -93,10 +94,11 @@ def sample_rows(B: int, H: int, N: int, per_head: int, generator: torch.Generato
     return torch.cat(out) if out else torch.zeros(0, dtype=torch.int64)
 
 
-def make_workload(w: Workload):
-    """q, k, v (bf16, CPU) and the checked row ids (None when all rows are checked)."""
+def make_workload(w: Workload, dtype=torch.bfloat16):
+    """q, k, v (bf16 unless ``dtype`` says otherwise, CPU) and the checked row
+    ids (None when all rows are checked)."""
     g = torch.Generator("cpu").manual_seed(w.seed)
-    q, k, v = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, generator=g)
+    q, k, v = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, generator=g, dtype=dtype)
     rows = None
     if w.rows_per_head is not None:
         rows = sample_rows(w.B, w.H, w.N, w.rows_per_head, g)
