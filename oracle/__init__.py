@@ -52,6 +52,11 @@ def build(force: bool = False) -> str:
 def _open(path: str):
     lib = ctypes.CDLL(path)
     dp = ctypes.POINTER(ctypes.c_double)
+    if hasattr(lib, "oracle_attn_fwd_kv"):
+        i64 = ctypes.c_int64
+        lib.oracle_attn_fwd_kv.restype = ctypes.c_int
+        lib.oracle_attn_fwd_kv.argtypes = [dp] * 5 + [i64] * 5 + [
+            ctypes.c_double, ctypes.c_int, ctypes.POINTER(i64), i64, ctypes.c_int]
     if hasattr(lib, "oracle_attn_bwd"):
         i64 = ctypes.c_int64
         lib.oracle_attn_bwd.restype = ctypes.c_int
@@ -216,3 +221,32 @@ def attn_bwd_dq_rows(q, k, v, dout, scale: float, causal: bool, rows, threads: i
     if rc != 0:
         raise RuntimeError("oracle_attn_bwd_dq_rows failed with code %d" % rc)
     return out
+
+
+def attn_fwd_kv(q, k, v, scale: float, causal: bool, rows=None, threads: int | None = None):
+    """Exact fp64 forward for queries [B, H, Nq, d] against keys and values
+    [B, H, Nk, d].  The queries are the last Nq positions of the key sequence:
+    under the causal mask query i sees keys j <= i + (Nk - Nq) (Nq <= Nk).
+    rows: None for all B*H*Nq rows, else global ids (b*H + h)*Nq + i.
+    Returns (o [R, d], lse [R])."""
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    if qd.ndim != 4 or kd.shape != vd.shape or qd.shape[:2] != kd.shape[:2] \
+            or qd.shape[3] != kd.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] do not match")
+    B, H, Nq, d = qd.shape
+    Nk = kd.shape[2]
+    if rows is None:
+        rows_arr, n_rows = None, B * H * Nq
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        n_rows = rows_arr.size
+    o = np.zeros((n_rows, d))
+    lse = np.zeros(n_rows)
+    rc = _load().oracle_attn_fwd_kv(
+        _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(scale),
+        1 if causal else 0,
+        rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if rows_arr is not None else None,
+        n_rows, int(threads) if threads else default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_attn_fwd_kv failed with code %d" % rc)
+    return o, lse

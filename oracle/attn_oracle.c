@@ -177,3 +177,124 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v, double *o
     free(running);
     return status;
 }
+
+/*
+ * oracle_attn_fwd_kv: queries and keys of different lengths.
+ *   q      : double [B][H][Nq][d]      k, v : double [B][H][Nk][d]
+ *   o      : double [n_rows][d]        lse  : double [n_rows]
+ *   rows   : global query rows (b*H + h)*Nq + i, or NULL for all B*H*Nq
+ * The queries are the last Nq positions of the key sequence: under the
+ * causal mask query i sees keys j <= i + (Nk - Nq) (requires Nq <= Nk);
+ * without it, all Nk keys.  With Nq == Nk this is oracle_attn_fwd.
+ * Same two-pass definition per row, in double.
+ */
+typedef struct {
+    const double *q, *k, *v;
+    double *o, *lse;
+    int64_t Nq, Nk, d;
+    double scale;
+    int causal;
+    const int64_t *rows;
+    int64_t row_begin, row_end;
+    int status;
+} oracle_kv_job;
+
+static void *run_kv_job(void *arg)
+{
+    oracle_kv_job *jb = (oracle_kv_job *)arg;
+    const int64_t Nq = jb->Nq, Nk = jb->Nk, d = jb->d;
+    double *s = (double *)malloc((size_t)(Nk > 0 ? Nk : 1) * sizeof(double));
+    if (!s) {
+        jb->status = ORACLE_NO_MEM;
+        return NULL;
+    }
+    for (int64_t r = jb->row_begin; r < jb->row_end; ++r) {
+        const int64_t grow = jb->rows ? jb->rows[r] : r;
+        const int64_t head = grow / Nq, i = grow % Nq;
+        const double *qi = jb->q + grow * d;
+        const double *kh = jb->k + head * Nk * d;
+        const double *vh = jb->v + head * Nk * d;
+        const int64_t n_keys = jb->causal ? i + (Nk - Nq) + 1 : Nk;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < n_keys; ++j) {
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dot += qi[c] * kh[j * d + c];
+            s[j] = jb->scale * dot;
+            if (s[j] > m)
+                m = s[j];
+        }
+        double *oi = jb->o + r * d;
+        for (int64_t c = 0; c < d; ++c)
+            oi[c] = 0.0;
+        double l = 0.0;
+        for (int64_t j = 0; j < n_keys; ++j) {
+            const double e = exp(s[j] - m);
+            l += e;
+            for (int64_t c = 0; c < d; ++c)
+                oi[c] += e * vh[j * d + c];
+        }
+        for (int64_t c = 0; c < d; ++c)
+            oi[c] /= l;
+        jb->lse[r] = m + log(l);
+    }
+    free(s);
+    jb->status = ORACLE_OK;
+    return NULL;
+}
+
+int oracle_attn_fwd_kv(const double *q, const double *k, const double *v, double *o, double *lse,
+                       int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale,
+                       int causal, const int64_t *rows, int64_t n_rows, int threads)
+{
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0 || n_rows < 0 || threads < 1)
+        return ORACLE_BAD_ARG;
+    if (causal && Nq > Nk)
+        return ORACLE_BAD_ARG;
+    if (n_rows == 0)
+        return ORACLE_OK;
+    if (!q || !k || !v || !o || !lse || Nk == 0)
+        return ORACLE_BAD_ARG;
+    const int64_t total = B * H * Nq;
+    if (!rows && n_rows != total)
+        return ORACLE_BAD_ARG;
+    if (rows)
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= total)
+                return ORACLE_BAD_ARG;
+    if (threads > n_rows)
+        threads = (int)n_rows;
+    oracle_kv_job *jobs = (oracle_kv_job *)calloc((size_t)threads, sizeof(oracle_kv_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)threads, sizeof(pthread_t));
+    char *running = (char *)calloc((size_t)threads, 1);
+    if (!jobs || !tid || !running) {
+        free(jobs);
+        free(tid);
+        free(running);
+        return ORACLE_NO_MEM;
+    }
+    int status = ORACLE_OK;
+    for (int t = 0; t < threads; ++t) {
+        oracle_kv_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->o = o; jb->lse = lse;
+        jb->Nq = Nq; jb->Nk = Nk; jb->d = d; jb->scale = scale; jb->causal = causal;
+        jb->rows = rows;
+        jb->row_begin = n_rows * t / threads;
+        jb->row_end = n_rows * (t + 1) / threads;
+        jb->status = ORACLE_BAD_ARG;
+        if (threads > 1 && pthread_create(&tid[t], NULL, run_kv_job, jb) == 0)
+            running[t] = 1;
+        else
+            run_kv_job(jb);
+    }
+    for (int t = 0; t < threads; ++t)
+        if (running[t])
+            pthread_join(tid[t], NULL);
+    for (int t = 0; t < threads; ++t)
+        if (jobs[t].status != ORACLE_OK)
+            status = jobs[t].status;
+    free(jobs);
+    free(tid);
+    free(running);
+    return status;
+}

@@ -363,3 +363,37 @@ def pin_bwd_invariants(attn_bwd, attn_bwd_dq_rows):
         rows = np.array([0, 7, 22, 23, 50, 91], dtype=np.int64)
         _close(attn_bwd_dq_rows(q, k, v, g, 0.4, causal, rows), dq.reshape(-1, d)[rows], 1e-13,
                "dq rows mode")
+
+
+# --------------------------------------------------------------------------- Nq != Nk
+def pin_fwd_kv(attn_fwd_kv, attn_fwd):
+    """Queries against a longer key sequence: brute force against torch.softmax
+    with the bottom-right causal mask; the square case equals the main oracle;
+    a single query (decode) sees every key with or without the mask; a query
+    block at the end of the sequence equals those rows of the square problem."""
+    for (B, H, Nq, Nk, d, causal, seed) in [(1, 2, 3, 7, 4, True, 1), (2, 1, 5, 5, 3, True, 2),
+                                            (1, 1, 4, 9, 2, False, 3), (1, 1, 1, 6, 4, True, 4)]:
+        q = _bf16_exact((B, H, Nq, d), seed, 2.0)
+        k = _bf16_exact((B, H, Nk, d), seed + 50, 2.0)
+        v = _bf16_exact((B, H, Nk, d), seed + 60)
+        o, lse = attn_fwd_kv(q, k, v, 0.5, causal)
+        s = torch.einsum("bhic,bhjc->bhij", q, k) * 0.5
+        if causal:
+            i = torch.arange(Nq)[:, None]
+            j = torch.arange(Nk)[None, :]
+            s = s.masked_fill(j > i + (Nk - Nq), float("-inf"))
+        _close(o, (torch.softmax(s, -1) @ v).reshape(-1, d).numpy(), 1e-13, "kv vs torch")
+        _close(lse, torch.logsumexp(s, -1).reshape(-1).numpy(), 1e-13, "kv lse vs torch")
+    q = _bf16_exact((2, 2, 11, 4), 7)
+    k = _bf16_exact((2, 2, 11, 4), 8)
+    v = _bf16_exact((2, 2, 11, 4), 9)
+    for causal in (False, True):
+        a = attn_fwd_kv(q, k, v, 0.3, causal)
+        b = attn_fwd(q, k, v, 0.3, causal)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), "square case"
+        tail = attn_fwd_kv(q[:, :, 8:].contiguous(), k, v, 0.3, causal)
+        rows = np.array([h * 11 + i for h in range(4) for i in range(8, 11)])
+        _close(tail[0], b[0][rows], 1e-14, "query block at the end")
+    one_q = q[:, :, -1:].contiguous()
+    assert np.array_equal(attn_fwd_kv(one_q, k, v, 0.3, True)[0],
+                          attn_fwd_kv(one_q, k, v, 0.3, False)[0]), "decode row sees all keys"

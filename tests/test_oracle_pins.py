@@ -20,6 +20,9 @@ def test_oracle_meets_pin(pin):
 # Each planted mistake is a one-line edit of the oracle's C source (built into
 # a temporary library on the CPU); at least one pin must reject it.
 MUTANTS = {
+    "kv_causal_offset_dropped": ("jb->causal ? i + (Nk - Nq) + 1 : Nk", "jb->causal ? i + 1 : Nk"),
+    "kv_values_of_wrong_head": ("const double *vh = jb->v + head * Nk * d;",
+                                "const double *vh = jb->v;"),
     "dropped_scale": ("s[j] = job->scale * dot;", "s[j] = dot;"),
     "causal_excludes_diagonal": ("job->causal ? i + 1 : N", "job->causal ? i : N"),
     "exp_sign_flipped": ("exp(s[j] - m)", "exp(m - s[j])"),
@@ -52,13 +55,32 @@ def test_planted_mistake_is_caught(name, mutant_dir):
                     c_path, "-lm"], check=True)
     fn = oracle.bind(so_path)
     failed = []
+    lib = oracle._open(so_path)
+
+    def fwd_kv(q, k, v, scale, causal, rows=None):
+        qd, kd, vd = (oracle._as_f64(t) for t in (q, k, v))
+        B, H, Nq, d = qd.shape
+        o = np.zeros((B * H * Nq, d))
+        lse = np.zeros(B * H * Nq)
+        rc = lib.oracle_attn_fwd_kv(*(oracle._ptr(t) for t in (qd, kd, vd, o, lse)), B, H, Nq,
+                                    kd.shape[2], d, float(scale), int(causal), None, B * H * Nq, 1)
+        assert rc == 0
+        return o, lse
     with np.errstate(all="ignore"):
         for pin in pins.ALL_PINS:
             try:
                 pin(fn)
             except AssertionError:
                 failed.append(pin.__name__)
+        try:
+            pins.pin_fwd_kv(fwd_kv, fn)
+        except AssertionError:
+            failed.append("pin_fwd_kv")
     assert failed, "planted mistake %s passed every pin" % name
+
+
+def test_fwd_kv_oracle_meets_pins():
+    pins.pin_fwd_kv(oracle.attn_fwd_kv, oracle.attn_fwd)
 
 
 def test_bwd_oracle_meets_pins():
