@@ -35,7 +35,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from tiled_online_softmax_fwd_gb300.inputs import WORKLOADS, digest, make_workload  # noqa: E402
+from tiled_online_softmax_fwd_gb300.inputs import (KV_WORKLOADS, WORKLOADS, digest,  # noqa: E402
+                                                   make_qkv_kv, make_workload)
 
 DEFAULT_WORKLOAD = "B1_H32_N16384_d128_causal_sigma3"
 METRIC = "attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
@@ -337,6 +338,121 @@ def run_bwd(args, world, rank, local):
     return 0
 
 
+# ------------------------------------------------------------------ decode shapes
+def peak_hbm():
+    try:
+        return (float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"]),
+                "measured copy (MEASURED_PEAKS.json)")
+    except Exception:
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+def run_kv(args, world, rank, local):
+    """attn_fwd_kv on a decode-shaped workload (Nq queries per head against Nk
+    cached keys): GB/s of algorithmic traffic (K, V, Q read once, O and lse
+    written once) against the measured HBM copy bandwidth, and TFLOP/s of the
+    visible (query, key) pairs against the bf16 peak."""
+    import oracle
+    from tiled_online_softmax_fwd_gb300 import fattn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = KV_WORKLOADS[args.op]
+    q, k, v = make_qkv_kv(w.B, w.H, w.Nq, w.Nk, w.d, w.seed, w.sigma_qk)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    do = torch.empty_like(dq)
+    dl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    need = fattn.kv_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, 0)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    splits = 1 if need == 0 else None  # the library's choice; reported below when known
+
+    def step():
+        fattn.attn_fwd_kv(dq, dk, dv, causal=w.causal, scale=w.scale, num_splits=0, workspace=ws,
+                          out=do, lse=dl, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    kernel_ms = e0.elapsed_time(e1) / args.steps
+    barrier(world)
+    status = fattn.device_status()
+    ms = max_over_ranks(world, kernel_ms)
+    gbs = w.io_bytes / (kernel_ms * 1e-3) / 1e9
+    tflops = w.flops / (kernel_ms * 1e-3) / 1e12
+    hbm, hbm_src = peak_hbm()
+    tc, tc_src = measured_peak()
+    bound = "hbm" if gbs / hbm >= tflops / tc else "tensor"
+    if need > 0:
+        rows = w.B * w.H * w.Nq
+        per_split = (w.d * 4 + 8) * rows
+        splits = max(2, round(need / per_split))
+
+    # End to end: q, k, v from pinned host memory, o and lse back, all timed.
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.empty_like(q).pin_memory()
+    hl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
+    n_e2e = max(3, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+
+    if rank != 0:
+        return 0
+    # The oracle on this host over whole heads' rows until the budget is spent.
+    qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+    threads = oracle.default_threads()
+    t_cpu, done_bytes, heads = 0.0, 0.0, 0
+    per_head_rows = w.Nq
+    while t_cpu < args.cpu_budget and heads < w.B * w.H:
+        take = torch.arange(heads * per_head_rows, (heads + 1) * per_head_rows)
+        t1 = time.perf_counter()
+        oracle.attn_fwd_kv(qd, kd, vd, w.scale, w.causal, rows=take.numpy(), threads=threads)
+        t_cpu += time.perf_counter() - t1
+        done_bytes += w.io_bytes / (w.B * w.H)
+        heads += 1
+    print(json.dumps({
+        "metric": "attention fwd GB/s, decode shape (bf16, 1xGB300)", "value": world * gbs,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, **w.describe(), "splits": splits,
+                   "l2": "inputs larger than L2 (%d MB)" % (w.io_bytes // 10**6)},
+        "tflops": tflops,
+        "roofline": {"bound": bound, "achieved": gbs if bound == "hbm" else tflops,
+                     "peak": hbm if bound == "hbm" else tc,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                     "frac": gbs / hbm if bound == "hbm" else tflops / tc,
+                     "peak_source": hbm_src if bound == "hbm" else tc_src, "traffic": None,
+                     "hbm_frac": gbs / hbm, "tensor_frac": tflops / tc,
+                     "algorithmic_bytes_per_launch": w.io_bytes,
+                     "algorithmic_flops_per_launch": w.flops},
+        "gpu_launches": args.steps * (2 if need > 0 else 1),
+        "e2e": {"value": w.io_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "steps": n_e2e,
+                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+                "d2h_bytes_per_step": q.numel() * 2 + w.B * w.H * w.Nq * 4},
+        "clocks": clocks.summary(), "device_status": status,
+        "cpu_baseline": {"value": done_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "%d of %d heads (all their query rows and keys), %.1f s"
+                                   % (heads, w.B * w.H, t_cpu)}}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args, world, rank, local):
     from tiled_online_softmax_fwd_gb300 import fattn
@@ -479,8 +595,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
-    ap.add_argument("--op", default=None, choices=sorted(ROWOP_WORKLOADS) + BWD_WORKLOADS,
-                    help="time a standalone row softmax / row sum workload instead")
+    ap.add_argument("--op", default=None,
+                    choices=sorted(ROWOP_WORKLOADS) + BWD_WORKLOADS + sorted(KV_WORKLOADS),
+                    help="time a row softmax / row sum, backward or decode-shape workload instead")
     ap.add_argument("--fp16", action="store_true", help="fp16 inputs through attn_fwd_fp16")
     ap.add_argument("--split", default="auto", choices=["auto", "off"],
                     help="key-range split when the library recommends one (auto) or never")
@@ -490,6 +607,8 @@ def main():
         return run_reference(args, world, rank)
     if args.op and args.op.startswith("bwd_"):
         return run_bwd(args, world, rank, local)
+    if args.op in KV_WORKLOADS:
+        return run_kv(args, world, rank, local)
     if args.op:
         return run_rowop(args, world, rank, local)
     return run_gpu(args, world, rank, local)

@@ -168,6 +168,40 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
                                       int causal, int num_splits, struct CUstream_st *stream);
 
 /*
+ * attn_fwd_kv -- queries and keys of different lengths: the decode step of
+ * autoregressive generation, where a few new query rows attend to a long,
+ * growing cache of keys and values and every step reads the whole cache
+ * ("OpenAI Triton: from introduction to model practice", section 4, the note
+ * on why attention is the bottleneck: 1 x seq_len scores per generated token,
+ * bound by memory bandwidth).
+ *
+ *   q     : bf16 [B][H][Nq][d]      k, v : bf16 [B][H][Nk][d]
+ *   o     : bf16 [B][H][Nq][d]      lse  : fp32 [B][H][Nq]
+ * All contiguous, device memory, 16-byte aligned; d in {64, 128}.
+ * Without the mask every query sees all Nk keys.  With causal = 1 the Nq
+ * queries are the LAST Nq positions of the key sequence: query i sees keys
+ * j <= i + (Nk - Nq), so Nq <= Nk is required; Nq == Nk is attn_fwd's causal
+ * mask.  Nk >= 1 whenever B*H*Nq > 0; B*H*Nq == 0 enqueues nothing.
+ *
+ * num_splits: 0 = the library's choice for the current device (key ranges
+ * spread over the SMs when B*H*ceil(Nq/256) is smaller than the SM count, as
+ * attn_fwd_split); 1..64 = that many key ranges (1: one kernel, the
+ * workspace is ignored and may be NULL).  The workspace rules are
+ * attn_fwd_split's; attn_fwd_kv_workspace_size gives the bytes for the same
+ * (B, H, Nq, Nk, d, num_splits) on the current device (0 when none is
+ * needed or on invalid arguments).  Errors: FATTN_ERR_INVALID_ARG for bad
+ * shapes, pointers, Nq > Nk under the mask, Nk == 0 with queries, or a
+ * workspace that is missing, too small, misaligned or overlapping;
+ * FATTN_ERR_UNSUPPORTED for other d or tensors beyond 2^39 bytes; nothing is
+ * enqueued on an error.
+ */
+size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+fattn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                           int num_splits, void *workspace, size_t workspace_bytes,
+                           struct CUstream_st *stream);
+
+/*
  * attn_fwd_simt -- the same operation and contract as attn_fwd, computed by a
  * plain fp32 SIMT kernel (no tensor cores, no 16-bit rounding of P).  It is
  * an independent second GPU implementation for cross-checking results at

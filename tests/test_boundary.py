@@ -149,6 +149,40 @@ def test_split_arguments_are_checked(lib):
     assert f(*base[:5], 1, 1, 0, 64, 0.125, 0, 4, 0, 0, None) == OK   # empty: no-op
 
 
+def test_kv_workspace_size(lib):
+    f = lib.attn_fwd_kv_workspace_size
+    rows = 2 * 3 * 5                                   # B*H*Nq: the scratch follows the queries
+    o_bytes = 7 * rows * 128 * 4
+    assert f(2, 3, 5, 9000, 128, 7) == (o_bytes + 255) // 256 * 256 + 7 * rows * 8
+    assert f(2, 3, 5, 9000, 128, 1) == 0
+    assert f(2, 3, 5, 9000, 96, 7) == 0 and f(2, 3, 5, 9000, 128, 65) == 0
+    assert f(2, 3, 5, 9000, 128, -1) == 0 and f(2, 3, 5, 0, 128, 7) == 0   # no keys
+    assert f(2, 3, 5, -1, 128, 7) == 0
+
+
+def test_kv_arguments_are_checked(lib):
+    f = lib.attn_fwd_kv
+    ptrs = [A, A + (1 << 24), A + (2 << 24), A + (3 << 24), A + (4 << 24)]
+    ws = A + (8 << 24)
+
+    def call(B, H, Nq, Nk, d, causal=0, splits=1, scale=0.125, p=ptrs):
+        return f(*p, B, H, Nq, Nk, d, scale, causal, splits, ws, 1 << 30, None)
+    assert call(1, 1, 10, 5, 64, causal=1) == INVALID      # more queries than keys under the mask
+    assert call(1, 1, 10, 0, 64) == INVALID                # queries without keys
+    assert call(1, 1, 10, -3, 64) == INVALID
+    assert call(1, 1, 4, 8, 64, splits=-1) == INVALID
+    assert call(1, 1, 4, 8, 64, splits=65) == INVALID
+    assert call(1, 1, 4, 8, 64, causal=2) == INVALID
+    assert call(1, 1, 4, 8, 64, scale=0.0) == INVALID
+    assert call(1, 1, 4, 8, 80) == UNSUPPORTED
+    assert call(1, 1, 4, 8, 64, p=[0] + ptrs[1:]) == INVALID
+    assert call(1, 1, 4, 8, 64, p=ptrs[:3] + [A + 8] + ptrs[4:]) == INVALID   # misaligned o
+    # o (4 rows) overlapping the end of k (8 rows of 64 bf16) is caught with k's own size
+    assert call(1, 1, 4, 8, 64, p=ptrs[:3] + [ptrs[1] + 8 * 64 * 2 - 16] + ptrs[4:]) == INVALID
+    assert call(1, 1, 0, 8, 64) == OK                      # no queries: no-op
+    assert call(1, 1, 0, 0, 64, causal=1) == OK
+
+
 def test_rowop_arguments_are_checked(lib):
     for f in (lib.fattn_softmax_rows, lib.fattn_row_sum):
         assert f(A, A + (1 << 24), -1, 4, 0, None) == INVALID      # negative M

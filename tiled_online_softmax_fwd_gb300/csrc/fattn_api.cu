@@ -108,19 +108,37 @@ fattn_status_t check_shape(int B, int H, int N, int d, float scale, int causal, 
     return FATTN_OK;
 }
 
+// Key-length checks of a call whose keys (Nk) may differ from its queries
+// (Nq): Nk >= 0, at least one key when there are queries, Nq <= Nk under the
+// causal mask (the queries are the last Nq key positions), and K, V within the
+// same size limit as Q.
+fattn_status_t check_keys(int B, int H, int Nq, int Nk, int d, int causal)
+{
+    if (Nk < 0)
+        return FATTN_ERR_INVALID_ARG;
+    const long long q_rows = static_cast<long long>(B) * H * Nq;
+    if (q_rows > 0 && Nk == 0)
+        return FATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk)
+        return FATTN_ERR_INVALID_ARG;
+    if (q_rows > 0 && static_cast<long long>(B) * H * Nk > (1LL << 39) / (2LL * d))
+        return FATTN_ERR_UNSUPPORTED;
+    return FATTN_OK;
+}
+
 // Pointer checks: non-null, 16-byte aligned, no output overlapping an input or
-// the other output.
+// the other output.  q_bytes covers q and o, kv_bytes each of k and v.
 fattn_status_t check_pointers(const void *q, const void *k, const void *v, const void *o,
-                              const float *lse, size_t tensor_bytes, size_t lse_bytes)
+                              const float *lse, size_t q_bytes, size_t kv_bytes, size_t lse_bytes)
 {
     if (!q || !k || !v || !o || !lse)
         return FATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FATTN_ERR_INVALID_ARG;
-    if (overlap(o, tensor_bytes, q, tensor_bytes) || overlap(o, tensor_bytes, k, tensor_bytes) ||
-        overlap(o, tensor_bytes, v, tensor_bytes) || overlap(o, tensor_bytes, lse, lse_bytes) ||
-        overlap(lse, lse_bytes, q, tensor_bytes) || overlap(lse, lse_bytes, k, tensor_bytes) ||
-        overlap(lse, lse_bytes, v, tensor_bytes))
+    if (overlap(o, q_bytes, q, q_bytes) || overlap(o, q_bytes, k, kv_bytes) ||
+        overlap(o, q_bytes, v, kv_bytes) || overlap(o, q_bytes, lse, lse_bytes) ||
+        overlap(lse, lse_bytes, q, q_bytes) || overlap(lse, lse_bytes, k, kv_bytes) ||
+        overlap(lse, lse_bytes, v, kv_bytes))
         return FATTN_ERR_INVALID_ARG;
     return FATTN_OK;
 }
@@ -164,17 +182,21 @@ fattn_status_t make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
 
 enum class Kernel { kTcgen05, kTcgen05F16, kSimt };
 
-// Every check of a forward call.  On FATTN_OK, *empty tells whether there is
-// any work, and (when there is) *dev / *info describe the current device.
+// Every check of a forward call with N queries and Nk keys per head.  On
+// FATTN_OK, *empty tells whether there is any work, and (when there is)
+// *dev / *info describe the current device.
 fattn_status_t validate(const void *q, const void *k, const void *v, const void *o,
-                        const float *lse, int B, int H, int N, int d, float scale, int causal,
-                        bool *empty, int *dev, DeviceInfo *info)
+                        const float *lse, int B, int H, int N, int Nk, int d, float scale,
+                        int causal, bool *empty, int *dev, DeviceInfo *info)
 {
     fattn_status_t s = check_shape(B, H, N, d, scale, causal, empty);
-    if (s != FATTN_OK || *empty)
+    if (s != FATTN_OK)
+        return s;
+    if ((s = check_keys(B, H, N, Nk, d, causal)) != FATTN_OK || *empty)
         return s;
     const size_t rows = static_cast<size_t>(B) * H * N;
-    if ((s = check_pointers(q, k, v, o, lse, rows * d * 2, rows * 4)) != FATTN_OK)
+    const size_t kv_bytes = static_cast<size_t>(B) * H * Nk * d * 2;
+    if ((s = check_pointers(q, k, v, o, lse, rows * d * 2, kv_bytes, rows * 4)) != FATTN_OK)
         return s;
     if ((s = current_device(dev, info)) != FATTN_OK)
         return s;
@@ -185,18 +207,21 @@ fattn_status_t validate(const void *q, const void *k, const void *v, const void 
     return FATTN_OK;
 }
 
-// Enqueue one validated forward call (split.splits > 1: key-range split with
-// the caller's scratch).
+// Enqueue one validated forward call with N queries and Nk keys per head
+// (split.splits > 1: key-range split with the caller's scratch).
 fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const void *k,
-                      const void *v, void *o, float *lse, int B, int H, int N, int d, float scale,
-                      int causal, cudaStream_t stream,
+                      const void *v, void *o, float *lse, int B, int H, int N, int Nk, int d,
+                      float scale, int causal, cudaStream_t stream,
                       const fattn::FwdSplit &split = fattn::FwdSplit{1, nullptr, nullptr})
 {
     fattn::FwdArgs a{q, k, v, o, lse, B, H, N, d, scale, causal};
     const bool f16 = which == Kernel::kTcgen05F16;
     a.f16 = f16 ? 1 : 0;
+    a.Nk = Nk;
     cudaError_t e;
     if (which == Kernel::kSimt) {
+        if (Nk != N)
+            return FATTN_ERR_UNSUPPORTED;
         e = fattn::launch_fwd_simt(a, stream);
     } else {
         PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -206,8 +231,8 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
         fattn::FwdMaps maps;
         const long long BH = static_cast<long long>(B) * H;
         if ((s = make_map(encode, &maps.q, q, N, d, BH, f16)) != FATTN_OK ||
-            (s = make_map(encode, &maps.k, k, N, d, BH, f16)) != FATTN_OK ||
-            (s = make_map(encode, &maps.v, v, N, d, BH, f16)) != FATTN_OK)
+            (s = make_map(encode, &maps.k, k, Nk, d, BH, f16)) != FATTN_OK ||
+            (s = make_map(encode, &maps.v, v, Nk, d, BH, f16)) != FATTN_OK)
             return s;
         e = fattn::launch_fwd_sm103(a, maps, split, info.num_sms, stream);
     }
@@ -221,10 +246,11 @@ fattn_status_t forward(Kernel which, const void *q, const void *k, const void *v
     bool empty = false;
     int dev = 0;
     DeviceInfo info;
-    fattn_status_t s = validate(q, k, v, o, lse, B, H, N, d, scale, causal, &empty, &dev, &info);
+    fattn_status_t s =
+        validate(q, k, v, o, lse, B, H, N, N, d, scale, causal, &empty, &dev, &info);
     if (s != FATTN_OK || empty)
         return s;
-    return launch(which, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+    return launch(which, info, q, k, v, o, lse, B, H, N, N, d, scale, causal, stream);
 }
 
 constexpr int kMaxSplits = 64;
@@ -247,41 +273,48 @@ size_t split_ws_bytes(int B, int H, int N, int d, int splits)
 }
 
 // Splits that fill the device: ceil(#SMs / units) for a grid of fewer work
-// units than SMs, at most one split per two key tiles and at most 16.
-int choose_splits(int B, int H, int N, int num_sms)
+// units than SMs, at most one split per two key tiles and at most kMaxSplits.
+int choose_splits(int B, int H, int Nq, int Nk, int num_sms)
 {
-    const long long pairs = ((static_cast<long long>(N) + 127) / 128 + 1) / 2;
+    const long long pairs = ((static_cast<long long>(Nq) + 127) / 128 + 1) / 2;
     const long long units = static_cast<long long>(B) * H * pairs;
-    const long long key_tiles = (static_cast<long long>(N) + 127) / 128;
+    const long long key_tiles = (static_cast<long long>(Nk) + 127) / 128;
     if (units <= 0 || units >= num_sms)
         return 1;
     long long s = (num_sms + units - 1) / units;
-    s = s > 16 ? 16 : s;
+    s = s > kMaxSplits ? kMaxSplits : s;
     s = s > key_tiles / 2 ? key_tiles / 2 : s;
     return s < 1 ? 1 : static_cast<int>(s);
 }
 
+// num_splits == 0: the choice of choose_splits for the current device.
 fattn_status_t forward_split(const void *q, const void *k, const void *v, void *o, float *lse,
-                             int B, int H, int N, int d, float scale, int causal, int num_splits,
-                             void *workspace, size_t workspace_bytes, cudaStream_t stream)
+                             int B, int H, int N, int Nk, int d, float scale, int causal,
+                             int num_splits, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream)
 {
-    if (num_splits < 1 || num_splits > kMaxSplits)
+    if (num_splits < 0 || num_splits > kMaxSplits)
         return FATTN_ERR_INVALID_ARG;
     bool empty = false;
     int dev = 0;
     DeviceInfo info;
-    fattn_status_t s = validate(q, k, v, o, lse, B, H, N, d, scale, causal, &empty, &dev, &info);
+    fattn_status_t s =
+        validate(q, k, v, o, lse, B, H, N, Nk, d, scale, causal, &empty, &dev, &info);
     if (s != FATTN_OK || empty)
         return s;
+    if (num_splits == 0)
+        num_splits = choose_splits(B, H, N, Nk, info.num_sms);
     if (num_splits == 1)
-        return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+        return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal,
+                      stream);
     const size_t need = split_ws_bytes(B, H, N, d, num_splits);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return FATTN_ERR_INVALID_ARG;
     const size_t rows = static_cast<size_t>(B) * H * N;
     const size_t tb = rows * d * 2, lb = rows * 4;
-    if (overlap(workspace, need, q, tb) || overlap(workspace, need, k, tb) ||
-        overlap(workspace, need, v, tb) || overlap(workspace, need, o, tb) ||
+    const size_t kvb = static_cast<size_t>(B) * H * Nk * d * 2;
+    if (overlap(workspace, need, q, tb) || overlap(workspace, need, k, kvb) ||
+        overlap(workspace, need, v, kvb) || overlap(workspace, need, o, tb) ||
         overlap(workspace, need, lse, lb))
         return FATTN_ERR_INVALID_ARG;
     if ((s = check_device_buffer(workspace, dev)) != FATTN_OK)
@@ -290,7 +323,8 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
     const fattn::FwdSplit split{
         num_splits, reinterpret_cast<float *>(ws),
         reinterpret_cast<float *>(ws + align_up(split_ws_o_bytes(B, H, N, d, num_splits), kWsAlign))};
-    return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, d, scale, causal, stream, split);
+    return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream,
+                  split);
 }
 
 // ---------------------------------------------------------------- no-allocation split
@@ -347,7 +381,7 @@ int attn_fwd_split_count(int B, int H, int N, int d, int causal)
     DeviceInfo info;
     if (current_device(&dev, &info) != FATTN_OK)
         return 0;
-    return choose_splits(B, H, N, info.num_sms);
+    return choose_splits(B, H, N, N, info.num_sms);
 }
 
 size_t attn_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits)
@@ -363,7 +397,35 @@ fattn_status_t attn_fwd_split(const void *q, const void *k, const void *v, void 
                               int B, int H, int N, int d, float scale, int causal, int num_splits,
                               void *workspace, size_t workspace_bytes, struct CUstream_st *stream)
 {
-    return forward_split(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
+    if (num_splits < 1)
+        return FATTN_ERR_INVALID_ARG;
+    return forward_split(q, k, v, o, lse, B, H, N, N, d, scale, causal, num_splits, workspace,
+                         workspace_bytes, stream);
+}
+
+size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits)
+{
+    bool empty = false;
+    if (num_splits < 0 || num_splits > kMaxSplits ||
+        check_shape(B, H, Nq, d, 1.0f, 0, &empty) != FATTN_OK ||
+        check_keys(B, H, Nq, Nk, d, 0) != FATTN_OK || empty)
+        return 0;
+    if (num_splits == 0) {
+        int dev = 0;
+        DeviceInfo info;
+        if (current_device(&dev, &info) != FATTN_OK)
+            return 0;
+        num_splits = choose_splits(B, H, Nq, Nk, info.num_sms);
+    }
+    return split_ws_bytes(B, H, Nq, d, num_splits);
+}
+
+fattn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                           int num_splits, void *workspace, size_t workspace_bytes,
+                           struct CUstream_st *stream)
+{
+    return forward_split(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, workspace,
                          workspace_bytes, stream);
 }
 
@@ -388,7 +450,7 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
     void *scratch = nullptr;
     if ((s = noalloc_scratch(dev, &scratch)) != FATTN_OK)
         return s;
-    return forward_split(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, scratch,
+    return forward_split(q, k, v, o, lse, B, H, N, N, d, scale, causal, num_splits, scratch,
                          kNoAllocScratchBytes, stream);
 }
 
@@ -533,7 +595,7 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
     bool empty = false;
     int dev = 0;
     DeviceInfo info;
-    fattn_status_t s = validate(dq, dk, dv, do_, dlse, B, H, N, d, scale, causal, &empty, &dev,
+    fattn_status_t s = validate(dq, dk, dv, do_, dlse, B, H, N, N, d, scale, causal, &empty, &dev,
                                 &info);
     if (s != FATTN_OK || empty)
         return s;
@@ -546,7 +608,7 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
         (e = cudaMemcpyAsync(dk, k_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
         (e = cudaMemcpyAsync(dv, v_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
         return cuda_fail(e);
-    if ((s = launch(Kernel::kTcgen05, info, dq, dk, dv, do_, dlse, B, H, N, d, scale, causal,
+    if ((s = launch(Kernel::kTcgen05, info, dq, dk, dv, do_, dlse, B, H, N, N, d, scale, causal,
                     stream)) != FATTN_OK)
         return s;
     if ((e = cudaMemcpyAsync(o_host, do_, tensor_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||

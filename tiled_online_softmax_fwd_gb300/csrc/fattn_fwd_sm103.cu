@@ -45,6 +45,7 @@
 // V sum to one exactly (the rounding of a dominant p cancels in O / l_round).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <float.h>
 #include <stdint.h>
 
 #include "fattn_internal.h"
@@ -93,14 +94,17 @@ struct Bars {
 };
 
 struct Params {
-    void *o;       // bf16 or fp16 [B*H*N][D]
+    void *o;       // bf16 or fp16 [B*H*Nq][D]
     float *lse;
-    float *ws_o;   // split mode: fp32 partial O [splits][B*H*N][D]
-    float2 *ws_l;  // split mode: base-2 partial lse (exact sum, rounded sum) [splits][B*H*N]
-    int N;         // sequence length
+    float *ws_o;   // split mode: fp32 partial O [splits][B*H*Nq][D]
+    float2 *ws_l;  // split mode: base-2 partial lse (exact sum, rounded sum) [splits][B*H*Nq]
+    int Nq;        // query rows per head
+    int Nk;        // keys per head
+    int off;       // Nk - Nq: query i sits at key position i + off (causal mask)
+    int extra;     // ceil(off / 128): key tiles past the diagonal (causal mask)
     int BH;        // batch * heads
-    int QT;        // query tiles per head = ceil(N / 128)
-    int KT;        // key tiles per head
+    int QT;        // query tiles per head = ceil(Nq / 128)
+    int KT;        // key tiles per head = ceil(Nk / 128)
     int pairs;     // Q-tile pairs per head = ceil(QT / 2)
     int splits;    // key-range splits per pair (1: no split, results go to o / lse)
     int units;     // BH * pairs * splits
@@ -119,12 +123,16 @@ struct Unit {
     int n_max;
 };
 
-// Key tiles visited by Q tile qt over the whole key range (0 past the end).
+// Key tiles visited by Q tile qt over the whole key range (0 past the end):
+// under the causal mask, up to the tile holding the last visible key of the
+// tile's last row, min(128 qt + 127, Nq - 1) + off.  For every tile but the
+// last that is tile qt + ceil(off / 128); for the last one it is the last
+// key tile, which the min with KT gives.
 __device__ __forceinline__ int key_tiles(const Params &p, int qt)
 {
     if (qt >= p.QT)
         return 0;
-    return p.causal ? min(qt + 1, p.KT) : p.KT;
+    return p.causal ? min(qt + 1 + p.extra, p.KT) : p.KT;
 }
 
 // The split s of a pair covers key tiles [s*F/S, (s+1)*F/S) of the pair's
@@ -429,8 +437,14 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             continue;
         const int qt = u.qt[t];
         const int row = qt * kBM + r;
-        float m = -INFINITY, l = 0.f, l_round = 0.f;
-        for (int j = u.j0; j < u.j1[t]; ++j) {
+        // m starts at -FLT_MAX, not -inf: a row can see no key of a tile
+        // only on its last tile (when Nk - Nq is not a multiple of 128), and
+        // when that tile is also its first in this unit, m - m_new and the
+        // exponents stay -inf or 0 instead of NaN (l = 0, lse = -inf).
+        float m = -FLT_MAX, l = 0.f, l_round = 0.f;
+        // Last visible column of row 0 in key tile j (causal mask).
+        int first_vis = qt * kBM + p.off - u.j0 * kBN;
+        for (int j = u.j0; j < u.j1[t]; ++j, first_vis -= kBN) {
             const bool first = j == u.j0;
             ok = mbar_wait(smem_addr(&b.s_full[t]), s_phase, kWaitLimitNs, abort);
             s_phase ^= 1;
@@ -448,15 +462,16 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 #pragma unroll
             for (int i = 0; i < kBN; ++i)
                 s[i] = __uint_as_float(sraw[i / 32][i % 32]);
-            // Mask (only on the diagonal tile and the ragged last tile; the
-            // branch is uniform across the warp): keys above the diagonal
-            // and keys past N get -inf, i.e. weight exactly 0.
-            const bool diag = p.causal && j == qt;
-            const bool tail = (j + 1) * kBN > p.N;
+            // Mask (only on tiles that cross the diagonal and on the ragged
+            // last tile; the branch is uniform across the warp): keys past
+            // row position + off and keys past Nk get -inf, i.e. weight
+            // exactly 0.
+            const bool diag = p.causal && first_vis < kBN - 1;
+            const bool tail = (j + 1) * kBN > p.Nk;
             if (diag || tail) {
-                int limit = diag ? r : kBN - 1;
+                int limit = diag ? first_vis + r : kBN - 1;
                 if (tail)
-                    limit = min(limit, p.N - 1 - j * kBN);
+                    limit = min(limit, p.Nk - 1 - j * kBN);
 #pragma unroll
                 for (int i = 0; i < kBN; ++i)
                     s[i] = i > limit ? -INFINITY : s[i];
@@ -536,9 +551,11 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         tc_fence_after();
         // fp16 P is rounded 8x more finely than bf16 P: O is normalised by
         // the exact sum there.
-        const float inv_l = 1.f / (kF16 ? l : l_round);
-        const bool live = row < p.N;
-        const size_t grow = static_cast<size_t>(u.bh) * p.N + row;
+        // l is 0 only for a split that saw no key of this row.
+        const float l_norm = kF16 ? l : l_round;
+        const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
+        const bool live = row < p.Nq;
+        const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
         if (p.splits == 1) {
             uint16_t *orow = static_cast<uint16_t *>(p.o) + grow * D;
 #pragma unroll 1
@@ -562,7 +579,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             if (live)
                 p.lse[grow] = (m + log2f(l)) * kLn2;
         } else {
-            const size_t srow = static_cast<size_t>(u.split) * p.BH * p.N + grow;
+            const size_t srow = static_cast<size_t>(u.split) * p.BH * p.Nq + grow;
             float *orow = p.ws_o + srow * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -669,11 +686,11 @@ __global__ void __launch_bounds__(256)
 {
     constexpr int kCols = D / 32;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
-    const long long rows = static_cast<long long>(p.BH) * p.N;
+    const long long rows = static_cast<long long>(p.BH) * p.Nq;
     if (row >= rows)
         return;
     const int lane = threadIdx.x & 31;
-    const int i = static_cast<int>(row % p.N);
+    const int i = static_cast<int>(row % p.Nq);
     const int qt = i / kBM, pair = qt / 2;
     const int full0 = key_tiles(p, 2 * pair), full1 = key_tiles(p, 2 * pair + 1);
     const int fmax = max(full0, full1), fown = (qt & 1) ? full1 : full0;
@@ -724,10 +741,13 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     p.lse = a.lse;
     p.ws_o = split.ws_o;
     p.ws_l = reinterpret_cast<float2 *>(split.ws_l);
-    p.N = a.N;
+    p.Nq = a.N;
+    p.Nk = a.Nk;
+    p.off = a.Nk - a.N;
+    p.extra = p.off > 0 ? (p.off + kBN - 1) / kBN : 0;
     p.BH = a.B * a.H;
     p.QT = (a.N + kBM - 1) / kBM;
-    p.KT = (a.N + kBN - 1) / kBN;
+    p.KT = (a.Nk + kBN - 1) / kBN;
     p.pairs = (p.QT + 1) / 2;
     p.splits = split.splits < 1 ? 1 : split.splits;
     const long long units = static_cast<long long>(p.BH) * p.pairs * p.splits;
@@ -748,7 +768,7 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     fwd_kernel<D, kF16><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
         return e;
-    const long long rows = static_cast<long long>(p.BH) * p.N;
+    const long long rows = static_cast<long long>(p.BH) * p.Nq;
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;

@@ -18,10 +18,12 @@ struct FwdArgs {
     float scale;
     int causal;
     int f16 = 0;  // 1: fp16 q, k, v, o (P in fp16); 0: bf16
+    int Nk = 0;   // keys per head (N: queries per head); the queries are the
+                  // last N key positions under the causal mask
 };
 
-// Tensor maps over Q, K, V viewed as 3-D bf16 arrays (d, N, B*H), box
-// (64, 128, 1), 128-byte swizzle, zero fill outside N.
+// Tensor maps over Q, K, V viewed as 3-D bf16 arrays (d, N or Nk, B*H), box
+// (64, 128, 1), 128-byte swizzle, zero fill outside the sequence.
 struct FwdMaps {
     CUtensorMap q, k, v;
 };

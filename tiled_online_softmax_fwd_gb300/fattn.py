@@ -22,7 +22,7 @@ FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
                 3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
 EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_fp16", "attn_fwd_host",
-            "attn_fwd_simt",
+            "attn_fwd_kv", "attn_fwd_kv_workspace_size", "attn_fwd_simt",
             "attn_fwd_split",
             "attn_fwd_split_count", "attn_fwd_split_noalloc", "attn_fwd_split_workspace_size",
             "fattn_status_string",
@@ -75,6 +75,10 @@ def load():
         lib.attn_fwd_split_count.argtypes = [ip, ip, ip, ip, ip]
         lib.attn_fwd_split_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_split_workspace_size.argtypes = [ip, ip, ip, ip, ip]
+        lib.attn_fwd_kv.restype = ctypes.c_int
+        lib.attn_fwd_kv.argtypes = [vp] * 5 + [ip] * 5 + [fp, ip, ip, vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_kv_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_kv_workspace_size.argtypes = [ip] * 6
         lib.attn_bwd.restype = ctypes.c_int
         lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, fp, ip, vp, ctypes.c_size_t, vp]
         lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
@@ -214,6 +218,47 @@ def attn_fwd_split(q, k, v, causal: bool = False, scale: float | None = None,
                                 int(num_splits), ws_ptr, workspace.numel(),
                                 _stream_handle(stream, q.device))
     _check(st, "attn_fwd_split")
+    return out, lse
+
+
+def kv_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    """Scratch bytes attn_fwd_kv needs (num_splits 0: the library's choice on
+    the current device)."""
+    return int(load().attn_fwd_kv_workspace_size(B, H, Nq, Nk, d, num_splits))
+
+
+def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None,
+                num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
+    """Queries q [B, H, Nq, d] against keys and values k, v [B, H, Nk, d]
+    (libfattn attn_fwd_kv).  Under the causal mask the queries are the last Nq
+    key positions.  num_splits 0 lets the library choose the key-range split;
+    the scratch is allocated here with torch when not given."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 \
+                or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous 4-D bf16 CUDA tensor" % name)
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] do not match: %s %s %s"
+                         % (q.shape, k.shape, v.shape))
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v are on different devices")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = default_scale(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        need = kv_workspace_size(B, H, Nq, Nk, d, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        st = load().attn_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, H, Nq, Nk, d, float(scale), 1 if causal else 0,
+                                int(num_splits), workspace.data_ptr() if need > 0 else 0,
+                                workspace.numel(), _stream_handle(stream, q.device))
+    _check(st, "attn_fwd_kv")
     return out, lse
 
 

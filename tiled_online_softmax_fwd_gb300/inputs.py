@@ -84,6 +84,67 @@ def make_qkv(B: int, H: int, N: int, d: int, seed: int, sigma_qk: float = 1.0,
     return q.contiguous(), k.contiguous(), v.contiguous()
 
 
+@dataclasses.dataclass(frozen=True)
+class KvWorkload:
+    """Queries against a longer key sequence (the decode shape): Nq query rows
+    per head, Nk keys per head; under the causal mask the queries are the last
+    Nq key positions."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+    sigma_qk: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    @property
+    def flops(self) -> float:
+        """4*d per visible (query, key) pair."""
+        off = self.Nk - self.Nq
+        if self.causal:
+            pairs = sum(min(i + off + 1, self.Nk) for i in range(self.Nq))
+        else:
+            pairs = self.Nq * self.Nk
+        return 4.0 * self.B * self.H * pairs * self.d
+
+    @property
+    def io_bytes(self) -> int:
+        """Bytes of K, V and Q read and O written (bf16) plus LSE (fp32)."""
+        bh = self.B * self.H
+        return 2 * bh * self.Nk * self.d * 2 + 2 * bh * self.Nq * self.d * 2 + bh * self.Nq * 4
+
+    def describe(self) -> dict:
+        return {"B": self.B, "H": self.H, "Nq": self.Nq, "Nk": self.Nk, "d": self.d,
+                "causal": self.causal, "seed": self.seed, "sigma_qk": self.sigma_qk}
+
+
+# Decode-shaped workloads: one new query row per head against a 32K-key
+# cache, and a 256-row chunk of new queries against a 16K-key cache.
+KV_WORKLOADS = {
+    "decode_B8_H32_Nq1_Nk32768_d128": KvWorkload("decode_B8_H32_Nq1_Nk32768_d128", 8, 32, 1,
+                                                 32768, 128, True, 11),
+    "chunk_B4_H32_Nq256_Nk16384_d128_causal": KvWorkload(
+        "chunk_B4_H32_Nq256_Nk16384_d128_causal", 4, 32, 256, 16384, 128, True, 12),
+}
+
+
+def make_qkv_kv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int, sigma_qk: float = 1.0,
+                dtype=torch.bfloat16):
+    """CPU tensors q [B, H, Nq, d] and k, v [B, H, Nk, d], drawn in that order
+    from one generator seeded with ``seed`` (same distributions as make_qkv)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = (torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32) * sigma_qk).to(dtype)
+    k = (torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32) * sigma_qk).to(dtype)
+    v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32).to(dtype)
+    return q.contiguous(), k.contiguous(), v.contiguous()
+
+
 def sample_rows(B: int, H: int, N: int, per_head: int, generator: torch.Generator):
     """Global row ids (b*H + h)*N + i: ``per_head`` distinct rows of every head."""
     out = []
