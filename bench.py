@@ -362,7 +362,7 @@ def run_kv(args, world, rank, local):
     do = torch.empty_like(dq)
     dl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    need = fattn.kv_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, 0)
+    need = fattn.kv_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, w.causal, 0)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     splits = 1 if need == 0 else None  # the library's choice; reported below when known
 
@@ -395,36 +395,47 @@ def run_kv(args, world, rank, local):
         splits = max(2, round(need / per_split))
 
     # End to end: q, k, v from pinned host memory, o and lse back, all timed.
-    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    ho = torch.empty_like(q).pin_memory()
-    hl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
-    n_e2e = max(3, min(args.steps, 10))
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        step()
-        ho.copy_(do, non_blocking=True)
-        hl.copy_(dl, non_blocking=True)
-        torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        ho = torch.empty_like(q).pin_memory()
+        hl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
+        n_e2e = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            step()
+            ho.copy_(do, non_blocking=True)
+            hl.copy_(dl, non_blocking=True)
+            torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        e2e = {"value": w.io_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms, "steps": n_e2e,
+               "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+               "d2h_bytes_per_step": q.numel() * 2 + w.B * w.H * w.Nq * 4}
 
     if rank != 0:
         return 0
     # The oracle on this host over whole heads' rows until the budget is spent.
-    qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
-    threads = oracle.default_threads()
-    t_cpu, done_bytes, heads = 0.0, 0.0, 0
-    per_head_rows = w.Nq
-    while t_cpu < args.cpu_budget and heads < w.B * w.H:
-        take = torch.arange(heads * per_head_rows, (heads + 1) * per_head_rows)
-        t1 = time.perf_counter()
-        oracle.attn_fwd_kv(qd, kd, vd, w.scale, w.causal, rows=take.numpy(), threads=threads)
-        t_cpu += time.perf_counter() - t1
-        done_bytes += w.io_bytes / (w.B * w.H)
-        heads += 1
-    print(json.dumps({
+    cpu = None
+    if not args.no_cpu_baseline:
+        qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+        threads = oracle.default_threads()
+        t_cpu, done_bytes, heads = 0.0, 0.0, 0
+        while heads == 0 or (t_cpu < args.cpu_budget and heads < w.B * w.H):
+            take = torch.arange(heads * w.Nq, (heads + 1) * w.Nq)
+            t1 = time.perf_counter()
+            oracle.attn_fwd_kv(qd, kd, vd, w.scale, w.causal, rows=take.numpy(), threads=threads)
+            t_cpu += time.perf_counter() - t1
+            done_bytes += w.io_bytes / (w.B * w.H)
+            heads += 1
+        cpu = {"value": done_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": "%d of %d heads (all their query rows and keys), %.1f s"
+                         % (heads, w.B * w.H, t_cpu)}
+    line = {
         "metric": "attention fwd GB/s, decode shape (bf16, 1xGB300)", "value": world * gbs,
         "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -441,15 +452,12 @@ def run_kv(args, world, rank, local):
                      "algorithmic_bytes_per_launch": w.io_bytes,
                      "algorithmic_flops_per_launch": w.flops},
         "gpu_launches": args.steps * (2 if need > 0 else 1),
-        "e2e": {"value": w.io_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "ms_per_step": e2e_ms, "steps": n_e2e,
-                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
-                "d2h_bytes_per_step": q.numel() * 2 + w.B * w.H * w.Nq * 4},
-        "clocks": clocks.summary(), "device_status": status,
-        "cpu_baseline": {"value": done_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": threads,
-                         "kind": "oracle",
-                         "sample": "%d of %d heads (all their query rows and keys), %.1f s"
-                                   % (heads, w.B * w.H, t_cpu)}}), flush=True)
+        "clocks": clocks.summary(), "device_status": status}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
     return 0
 
 

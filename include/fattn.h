@@ -183,19 +183,25 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
  * j <= i + (Nk - Nq), so Nq <= Nk is required; Nq == Nk is attn_fwd's causal
  * mask.  Nk >= 1 whenever B*H*Nq > 0; B*H*Nq == 0 enqueues nothing.
  *
- * num_splits: 0 = the library's choice for the current device (key ranges
- * spread over the SMs when B*H*ceil(Nq/256) is smaller than the SM count, as
- * attn_fwd_split); 1..64 = that many key ranges (1: one kernel, the
- * workspace is ignored and may be NULL).  The workspace rules are
- * attn_fwd_split's; attn_fwd_kv_workspace_size gives the bytes for the same
- * (B, H, Nq, Nk, d, num_splits) on the current device (0 when none is
- * needed or on invalid arguments).  Errors: FATTN_ERR_INVALID_ARG for bad
+ * num_splits: 0 = the library's schedule for the current device; 1..64 =
+ * that many equal key ranges per pair of 128-row query tiles, as
+ * attn_fwd_split (1: one kernel, the workspace is ignored and may be NULL).
+ * The automatic schedule, for Nq <= 256 (one pair of query tiles per head)
+ * when whole heads per SM would leave SMs idle, deals the B*H*(key tiles)
+ * steps evenly over the SMs in contiguous head-major ranges (a head may be
+ * shared by several SMs, each producing a partial result) and merges the
+ * partials as attn_fwd_split does; otherwise it is attn_fwd_split_count's
+ * choice.  The workspace rules are attn_fwd_split's;
+ * attn_fwd_kv_workspace_size gives the bytes for the same (B, H, Nq, Nk, d,
+ * causal, num_splits) on the current device (0 when none is needed or on
+ * invalid arguments).  Errors: FATTN_ERR_INVALID_ARG for bad
  * shapes, pointers, Nq > Nk under the mask, Nk == 0 with queries, or a
  * workspace that is missing, too small, misaligned or overlapping;
  * FATTN_ERR_UNSUPPORTED for other d or tensors beyond 2^39 bytes; nothing is
  * enqueued on an error.
  */
-size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal,
+                                  int num_splits);
 fattn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
                            int num_splits, void *workspace, size_t workspace_bytes,

@@ -153,11 +153,11 @@ def test_kv_workspace_size(lib):
     f = lib.attn_fwd_kv_workspace_size
     rows = 2 * 3 * 5                                   # B*H*Nq: the scratch follows the queries
     o_bytes = 7 * rows * 128 * 4
-    assert f(2, 3, 5, 9000, 128, 7) == (o_bytes + 255) // 256 * 256 + 7 * rows * 8
-    assert f(2, 3, 5, 9000, 128, 1) == 0
-    assert f(2, 3, 5, 9000, 96, 7) == 0 and f(2, 3, 5, 9000, 128, 65) == 0
-    assert f(2, 3, 5, 9000, 128, -1) == 0 and f(2, 3, 5, 0, 128, 7) == 0   # no keys
-    assert f(2, 3, 5, -1, 128, 7) == 0
+    assert f(2, 3, 5, 9000, 128, 1, 7) == (o_bytes + 255) // 256 * 256 + 7 * rows * 8
+    assert f(2, 3, 5, 9000, 128, 0, 1) == 0
+    assert f(2, 3, 5, 9000, 96, 0, 7) == 0 and f(2, 3, 5, 9000, 128, 0, 65) == 0
+    assert f(2, 3, 5, 9000, 128, 0, -1) == 0 and f(2, 3, 5, 0, 128, 0, 7) == 0   # no keys
+    assert f(2, 3, 5, -1, 128, 0, 7) == 0 and f(1, 1, 9, 5, 64, 1, 2) == 0   # Nq > Nk, causal
 
 
 def test_kv_arguments_are_checked(lib):

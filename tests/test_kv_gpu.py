@@ -38,6 +38,13 @@ KV_CASES = [
     (1, 1, 64, 448, 128, True, 1), (1, 3, 1, 16384, 128, True, 0), (1, 1, 255, 256, 64, True, 2),
     (1, 1, 256, 320, 64, True, 3), (1, 1, 256, 320, 128, True, 3), (1, 1, 130, 2000, 64, True, 16),
     (1, 1, 16, 5000, 128, False, 64), (3, 1, 2, 129, 64, True, 2),
+    # The automatic schedule deals (head, key tile) steps over the SMs
+    # (stream-K) for these: one or two query tiles per head, few heads, long
+    # keys; the last one has ranges of two key tiles, some starting on a key
+    # tile that rows 0..63 of the first query tile cannot see.
+    (1, 5, 200, 9000, 64, True, 0), (2, 3, 256, 20000, 128, True, 0),
+    (1, 1, 1, 50000, 128, False, 0), (1, 2, 256, 19520, 64, True, 0),
+    (1, 2, 256, 19520, 128, True, 0),
 ]
 
 
@@ -95,11 +102,11 @@ def test_splits_agree():
 
 
 def test_kv_workspace_query_matches_the_auto_choice():
-    need = fattn.kv_workspace_size(8, 32, 1, 32768, 128, 0)
+    need = fattn.kv_workspace_size(8, 32, 1, 32768, 128, True, 0)
     assert need >= 0
     q, k, v = make_qkv_kv(1, 1, 1, 256, 64, seed=2)
-    ws = torch.empty(max(fattn.kv_workspace_size(1, 1, 1, 256, 64, 0), 1), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.empty(max(fattn.kv_workspace_size(1, 1, 1, 256, 64, True, 0), 1),
+                     dtype=torch.uint8, device="cuda")
     o, _ = fattn.attn_fwd_kv(q.cuda(), k.cuda(), v.cuda(), causal=True, workspace=ws)
     torch.cuda.synchronize()
     assert torch.isfinite(o.float()).all()

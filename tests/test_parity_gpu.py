@@ -283,9 +283,16 @@ def test_split_matches_oracle(B, H, N, d, causal, splits):
 
 
 def test_split_count_fills_the_device():
+    """The split count minimises the estimated time in key-tile steps:
+    ceil(units * s / SMs) rounds of ceil(key tiles / s) + 3 steps, plus 6
+    steps for the partials and their merge when s > 1."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    units, tiles = 16, 32                      # B=1, H=1, N=4096: 16 pairs, 32 key tiles
+
+    def est(s):
+        return -(-units * s // n_sm) * (-(-tiles // s) + 3) + (6 if s > 1 else 0)
     s = fattn.split_count(1, 1, 4096, 64, False)
-    assert 1 < s <= 16 and 16 * s >= min(n_sm, 16 * 16)
+    assert 1 < s <= 16 and est(s) == min(est(x) for x in range(1, 17))
     assert fattn.split_count(1, 32, 16384, 128, True) == 1   # already more units than SMs
 
 

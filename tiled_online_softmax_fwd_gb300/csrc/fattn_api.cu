@@ -272,8 +272,14 @@ size_t split_ws_bytes(int B, int H, int N, int d, int splits)
            static_cast<size_t>(splits) * B * H * N * 2 * sizeof(float);
 }
 
-// Splits that fill the device: ceil(#SMs / units) for a grid of fewer work
-// units than SMs, at most one split per two key tiles and at most kMaxSplits.
+// Splits for a grid of fewer work units than SMs: the s (at most one split
+// per two key tiles, at most kMaxSplits) that minimises the estimated time in
+// key-tile steps: ceil(units * s / SMs) rounds of ceil(KT / s) steps plus
+// kUnitCost steps per unit (Q load, pipeline fill, epilogue), plus
+// kMergeCost steps for the partial outputs and their merge when s > 1 (both
+// measured on one and four splits of 16 pairs x 32 key tiles, d = 64).  Ties
+// go to the smaller s.
+constexpr long long kUnitCost = 3, kMergeCost = 6;
 int choose_splits(int B, int H, int Nq, int Nk, int num_sms)
 {
     const long long pairs = ((static_cast<long long>(Nq) + 127) / 128 + 1) / 2;
@@ -281,13 +287,30 @@ int choose_splits(int B, int H, int Nq, int Nk, int num_sms)
     const long long key_tiles = (static_cast<long long>(Nk) + 127) / 128;
     if (units <= 0 || units >= num_sms)
         return 1;
-    long long s = (num_sms + units - 1) / units;
-    s = s > kMaxSplits ? kMaxSplits : s;
-    s = s > key_tiles / 2 ? key_tiles / 2 : s;
-    return s < 1 ? 1 : static_cast<int>(s);
+    long long best_s = 1, best = key_tiles + kUnitCost;
+    const long long s_max = key_tiles / 2 < kMaxSplits ? key_tiles / 2 : kMaxSplits;
+    for (long long s = 2; s <= s_max; ++s) {
+        const long long rounds = (units * s + num_sms - 1) / num_sms;
+        const long long est = rounds * ((key_tiles + s - 1) / s + kUnitCost) + kMergeCost;
+        if (est < best) {
+            best = est;
+            best_s = s;
+        }
+    }
+    return static_cast<int>(best_s);
 }
 
-// num_splits == 0: the choice of choose_splits for the current device.
+// The automatic schedule of attn_fwd_kv: stream-K for one Q-tile pair per
+// head when whole heads would leave SMs idle, else choose_splits.  Returns
+// the partial slots per head (1: no split).
+int auto_slots(int B, int H, int Nq, int Nk, int causal, int num_sms, int *streamk)
+{
+    const fattn::FwdPlan plan = fattn::plan_fwd_streamk(B, H, Nq, Nk, causal, num_sms);
+    *streamk = plan.streamk;
+    return plan.streamk ? plan.slots : choose_splits(B, H, Nq, Nk, num_sms);
+}
+
+// num_splits == 0: the automatic schedule for the current device.
 fattn_status_t forward_split(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int H, int N, int Nk, int d, float scale, int causal,
                              int num_splits, void *workspace, size_t workspace_bytes,
@@ -302,8 +325,9 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
         validate(q, k, v, o, lse, B, H, N, Nk, d, scale, causal, &empty, &dev, &info);
     if (s != FATTN_OK || empty)
         return s;
+    int streamk = 0;
     if (num_splits == 0)
-        num_splits = choose_splits(B, H, N, Nk, info.num_sms);
+        num_splits = auto_slots(B, H, N, Nk, causal, info.num_sms, &streamk);
     if (num_splits == 1)
         return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal,
                       stream);
@@ -322,7 +346,8 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const fattn::FwdSplit split{
         num_splits, reinterpret_cast<float *>(ws),
-        reinterpret_cast<float *>(ws + align_up(split_ws_o_bytes(B, H, N, d, num_splits), kWsAlign))};
+        reinterpret_cast<float *>(ws + align_up(split_ws_o_bytes(B, H, N, d, num_splits), kWsAlign)),
+        streamk};
     return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream,
                   split);
 }
@@ -403,19 +428,20 @@ fattn_status_t attn_fwd_split(const void *q, const void *k, const void *v, void 
                          workspace_bytes, stream);
 }
 
-size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits)
+size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal,
+                                  int num_splits)
 {
     bool empty = false;
     if (num_splits < 0 || num_splits > kMaxSplits ||
-        check_shape(B, H, Nq, d, 1.0f, 0, &empty) != FATTN_OK ||
-        check_keys(B, H, Nq, Nk, d, 0) != FATTN_OK || empty)
+        check_shape(B, H, Nq, d, 1.0f, causal, &empty) != FATTN_OK ||
+        check_keys(B, H, Nq, Nk, d, causal) != FATTN_OK || empty)
         return 0;
     if (num_splits == 0) {
-        int dev = 0;
+        int dev = 0, streamk = 0;
         DeviceInfo info;
         if (current_device(&dev, &info) != FATTN_OK)
             return 0;
-        num_splits = choose_splits(B, H, Nq, Nk, info.num_sms);
+        num_splits = auto_slots(B, H, Nq, Nk, causal, info.num_sms, &streamk);
     }
     return split_ws_bytes(B, H, Nq, d, num_splits);
 }

@@ -89,6 +89,10 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    // Stream-K range of this CTA (see cta_unit): first head, its first key
+    // tile and partial slot, and the end of the range.
+    int sk_h0, sk_j0, sk_slot0;
+    long long sk_hi;
     float xmax[2][2 * kBM];  // row-half exchange (double-buffered): partial max / l_round
     float xsum[2][2 * kBM];  // row-half exchange: partial l
 };
@@ -106,9 +110,14 @@ struct Params {
     int QT;        // query tiles per head = ceil(Nq / 128)
     int KT;        // key tiles per head = ceil(Nk / 128)
     int pairs;     // Q-tile pairs per head = ceil(QT / 2)
-    int splits;    // key-range splits per pair (1: no split, results go to o / lse)
+    int splits;    // key-range splits per pair (1: no split, results go to o / lse);
+                   // stream-K: partial slots per head
     int units;     // BH * pairs * splits
     int causal;
+    int streamk;   // 1: one Q-tile pair per head, key tiles dealt evenly over CTAs
+    int grid;      // CTAs of the launch (stream-K ranges)
+    int F;         // key tiles of the pair (stream-K)
+    long long W;   // BH * F: stream-K work in key tiles
     float sl2;     // scale * log2(e)
 };
 
@@ -128,34 +137,59 @@ struct Unit {
 // tile's last row, min(128 qt + 127, Nq - 1) + off.  For every tile but the
 // last that is tile qt + ceil(off / 128); for the last one it is the last
 // key tile, which the min with KT gives.
+__host__ __device__ __forceinline__ int key_tiles(int QT, int KT, int extra, int causal, int qt)
+{
+    if (qt >= QT)
+        return 0;
+    return causal ? min(qt + 1 + extra, KT) : KT;
+}
 __device__ __forceinline__ int key_tiles(const Params &p, int qt)
 {
-    if (qt >= p.QT)
-        return 0;
-    return p.causal ? min(qt + 1 + p.extra, p.KT) : p.KT;
+    return key_tiles(p.QT, p.KT, p.extra, p.causal, qt);
+}
+
+// Tile t of the pair works on key tiles [j0, min(je, its own count)).
+__device__ __forceinline__ Unit make_unit(const Params &p, int bh, int split, int pair, int j0,
+                                          int je)
+{
+    Unit u;
+    u.bh = bh;
+    u.split = split;
+    u.j0 = j0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        u.qt[t] = 2 * pair + t;
+        u.j1[t] = min(je, key_tiles(p, u.qt[t]));
+        u.n[t] = max(u.j1[t] - u.j0, 0);
+    }
+    u.n_max = max(u.n[0], u.n[1]);
+    return u;
 }
 
 // The split s of a pair covers key tiles [s*F/S, (s+1)*F/S) of the pair's
 // F = max over its two tiles; the combine kernel uses the same ranges.
 __device__ __forceinline__ Unit unit_at(const Params &p, int k)
 {
-    Unit u;
-    u.split = k % p.splits;
+    const int split = k % p.splits;
     const int rest = k / p.splits;
     const int pair = p.pairs - 1 - rest / p.BH;  // heaviest pairs first
-    u.bh = rest % p.BH;
-    const int full0 = key_tiles(p, 2 * pair), full1 = key_tiles(p, 2 * pair + 1);
-    const int fmax = max(full0, full1);
-    u.j0 = u.split * fmax / p.splits;
-    const int je = (u.split + 1) * fmax / p.splits;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        u.qt[t] = 2 * pair + t;
-        u.j1[t] = min(je, t == 0 ? full0 : full1);
-        u.n[t] = max(u.j1[t] - u.j0, 0);
-    }
-    u.n_max = max(u.n[0], u.n[1]);
-    return u;
+    const int fmax = max(key_tiles(p, 2 * pair), key_tiles(p, 2 * pair + 1));
+    return make_unit(p, rest % p.BH, split, pair, split * fmax / p.splits,
+                     (split + 1) * fmax / p.splits);
+}
+
+// Stream-K (one Q-tile pair per head): the BH * F (head, key tile) steps,
+// head-major, are dealt in equal contiguous ranges, CTA c taking
+// [c W / G, (c+1) W / G).  A head split over several CTAs gets one partial
+// slot per CTA, numbered from the first CTA that covers it.
+__host__ __device__ __forceinline__ long long sk_lo(long long W, int G, long long c)
+{
+    return c * W / G;
+}
+// The CTA whose range holds step x: the largest c with lo(c) <= x.
+__host__ __device__ __forceinline__ int sk_cta(long long W, int G, long long x)
+{
+    return static_cast<int>(((x + 1) * G - 1) / W);
 }
 
 // Serpentine deal: round r gives CTA c the unit r*G + c (r even) or
@@ -163,6 +197,27 @@ __device__ __forceinline__ Unit unit_at(const Params &p, int k)
 __device__ __forceinline__ int unit_index(int round, int cta, int grid)
 {
     return round * grid + ((round & 1) ? grid - 1 - cta : cta);
+}
+
+// The r-th work unit of this CTA; false past its last.  Under stream-K the
+// r-th unit is the r-th head of the CTA's range: every head after the first
+// starts inside the range, so this CTA is its first (slot 0).
+__device__ __forceinline__ bool cta_unit(const Params &p, const Bars &b, int r, Unit &u)
+{
+    if (p.streamk) {
+        const int h = b.sk_h0 + r;
+        const long long base = static_cast<long long>(h) * p.F;
+        if (h >= p.BH || base >= b.sk_hi)
+            return false;
+        const int je = static_cast<int>(min(b.sk_hi - base, static_cast<long long>(p.F)));
+        u = make_unit(p, h, r == 0 ? b.sk_slot0 : 0, 0, r == 0 ? b.sk_j0 : 0, je);
+        return true;
+    }
+    const int k = unit_index(r, blockIdx.x, gridDim.x);
+    if (k >= p.units)
+        return false;
+    u = unit_at(p, k);
+    return true;
 }
 
 __device__ __forceinline__ void record_failure(Bars &b, uint32_t role)
@@ -214,10 +269,9 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
     bool ok = true;
     int last_q_parity[2] = {-1, -1};
     for (int r = 0; ok; ++r) {
-        const int k = unit_index(r, blockIdx.x, gridDim.x);
-        if (k >= p.units)
+        Unit u;
+        if (!cta_unit(p, b, r, u))
             break;
-        const Unit u = unit_at(p, k);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (!ok || u.n[t] == 0)
@@ -333,10 +387,9 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
     };
 
     for (int r = 0; ok; ++r) {
-        const int k = unit_index(r, blockIdx.x, gridDim.x);
-        if (k >= p.units)
+        Unit u;
+        if (!cta_unit(p, b, r, u))
             break;
-        const Unit u = unit_at(p, k);
         const uint32_t base = pos;  // K_(j0+i) at base + 2i, V_(j0+i) at base + 2i + 1
         if (u.n_max == 0)
             continue;
@@ -429,10 +482,9 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
     bool ok = true;
 
     for (int rr = 0; ok; ++rr) {
-        const int k = unit_index(rr, blockIdx.x, gridDim.x);
-        if (k >= p.units)
+        Unit u;
+        if (!cta_unit(p, b, rr, u))
             break;
-        const Unit u = unit_at(p, k);
         if (u.n[t] == 0)
             continue;
         const int qt = u.qt[t];
@@ -638,6 +690,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_addr(&b.drain), 1);
         b.abort = 0;
+        if (p.streamk) {
+            const long long lo = sk_lo(p.W, p.grid, blockIdx.x);
+            const long long h0 = lo / p.F;
+            b.sk_h0 = static_cast<int>(h0);
+            b.sk_j0 = static_cast<int>(lo - h0 * p.F);
+            b.sk_slot0 = static_cast<int>(blockIdx.x) - sk_cta(p.W, p.grid, h0 * p.F);
+            b.sk_hi = sk_lo(p.W, p.grid, blockIdx.x + 1);
+        }
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -678,8 +738,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 // partial outputs O_s = acc_s / l_round_s:
 //   lse = ln2 * log2(sum_s 2^le_s)
 //   O   = sum_s w_s O_s,  w_s = 2^lr_s / sum_s' 2^lr_s'
-// Splits with no key tile for the row's Q tile are skipped (the same ranges
-// as unit_at).  One warp per row; lane l owns D/32 consecutive columns.
+// Slots with no key tile for the row's Q tile are skipped (the same ranges
+// as unit_at / cta_unit).  One warp per row; lane l owns D/32 consecutive
+// columns.
+//
+// Key-tile range [j0, je) of partial slot sp of head bh's pair (false: no
+// such slot).
+__device__ __forceinline__ bool slot_range(const Params &p, int bh, int fmax, int sp, int &j0,
+                                           int &je)
+{
+    if (!p.streamk) {
+        j0 = sp * fmax / p.splits;
+        je = (sp + 1) * fmax / p.splits;
+        return sp < p.splits;
+    }
+    const long long x = static_cast<long long>(bh) * p.F;
+    const long long c = sk_cta(p.W, p.grid, x) + sp;
+    if (c >= p.grid)
+        return false;
+    const long long lo = sk_lo(p.W, p.grid, c);
+    if (lo >= x + p.F)
+        return false;
+    j0 = static_cast<int>(max(lo - x, 0LL));
+    je = static_cast<int>(min(sk_lo(p.W, p.grid, c + 1) - x, static_cast<long long>(p.F)));
+    return true;
+}
+
 template <int D, bool kF16>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_l, const Params p)
@@ -690,37 +774,52 @@ __global__ void __launch_bounds__(256)
     if (row >= rows)
         return;
     const int lane = threadIdx.x & 31;
+    const int bh = static_cast<int>(row / p.Nq);
     const int i = static_cast<int>(row % p.Nq);
     const int qt = i / kBM, pair = qt / 2;
     const int full0 = key_tiles(p, 2 * pair), full1 = key_tiles(p, 2 * pair + 1);
     const int fmax = max(full0, full1), fown = (qt & 1) ? full1 : full0;
-    float mx_e = -INFINITY, mx_r = -INFINITY;
-    for (int sp = 0; sp < p.splits; ++sp) {
-        const int j0 = sp * fmax / p.splits, je = (sp + 1) * fmax / p.splits;
-        if (min(je, fown) <= j0)
-            continue;
-        const float2 ll = ws_l[static_cast<size_t>(sp) * rows + row];
-        mx_e = fmaxf(mx_e, ll.x);
-        mx_r = fmaxf(mx_r, ll.y);
-    }
-    float se = 0.f, sr = 0.f;
+    // Online merge over the slots, kBatch at a time: all loads of a batch are
+    // issued before any of them is used.  A slot whose range held no key of
+    // this row (l = 0, partial lse -inf) contributes nothing.
+    constexpr int kBatch = 4;
+    float mx_e = -INFINITY, mx_r = -INFINITY, se = 0.f, sr = 0.f;
     float acc[kCols];
 #pragma unroll
     for (int c = 0; c < kCols; ++c)
         acc[c] = 0.f;
-    for (int sp = 0; sp < p.splits; ++sp) {
-        const int j0 = sp * fmax / p.splits, je = (sp + 1) * fmax / p.splits;
-        if (min(je, fown) <= j0)
-            continue;
-        const size_t srow = static_cast<size_t>(sp) * rows + row;
-        const float2 ll = ws_l[srow];
-        se += ex2(ll.x - mx_e);
-        const float w = ex2(ll.y - mx_r);
-        sr += w;
-        const float *src = ws_o + srow * D + lane * kCols;
+    bool more = true;
+    for (int sp0 = 0; more; sp0 += kBatch) {
+        float2 ll[kBatch];
+        float o[kBatch][kCols];
 #pragma unroll
-        for (int c = 0; c < kCols; ++c)
-            acc[c] = fmaf(w, src[c], acc[c]);
+        for (int u = 0; u < kBatch; ++u) {
+            int j0 = 0, je = 0;
+            more = more && slot_range(p, bh, fmax, sp0 + u, j0, je);
+            ll[u] = make_float2(-INFINITY, -INFINITY);
+            if (more && min(je, fown) > j0) {
+                const size_t srow = static_cast<size_t>(sp0 + u) * rows + row;
+                ll[u] = ws_l[srow];
+                const float *src = ws_o + srow * D + lane * kCols;
+#pragma unroll
+                for (int c = 0; c < kCols; ++c)
+                    o[u][c] = src[c];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (ll[u].x == -INFINITY)
+                continue;
+            const float ne = fmaxf(mx_e, ll[u].x), nr = fmaxf(mx_r, ll[u].y);
+            se = se * ex2(mx_e - ne) + ex2(ll[u].x - ne);
+            const float a = ex2(mx_r - nr), w = ex2(ll[u].y - nr);
+            sr = sr * a + w;
+#pragma unroll
+            for (int c = 0; c < kCols; ++c)
+                acc[c] = fmaf(w, o[u][c], acc[c] * a);
+            mx_e = ne;
+            mx_r = nr;
+        }
     }
     const float inv = 1.f / sr;
     uint16_t *dst = static_cast<uint16_t *>(p.o) + static_cast<size_t>(row) * D + lane * kCols;
@@ -750,13 +849,22 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     p.KT = (a.Nk + kBN - 1) / kBN;
     p.pairs = (p.QT + 1) / 2;
     p.splits = split.splits < 1 ? 1 : split.splits;
-    const long long units = static_cast<long long>(p.BH) * p.pairs * p.splits;
+    p.causal = a.causal;
+    p.streamk = split.streamk;
+    long long units = static_cast<long long>(p.BH) * p.pairs * p.splits;
+    if (p.streamk) {
+        if (p.pairs != 1 || p.splits < 2)
+            return cudaErrorInvalidValue;
+        p.F = max(key_tiles(p.QT, p.KT, p.extra, p.causal, 0),
+                  key_tiles(p.QT, p.KT, p.extra, p.causal, 1));
+        p.W = static_cast<long long>(p.BH) * p.F;
+        units = p.W;
+    }
     if (units == 0)
         return cudaSuccess;
-    if (units > 0x7fffffffLL)
+    if (!p.streamk && units > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    p.units = static_cast<int>(units);
-    p.causal = a.causal;
+    p.units = static_cast<int>(min(units, 0x7fffffffLL));
     p.sl2 = a.scale * kLog2e;
     const size_t smem = C::kTilesBytes + sizeof(Bars) + 1024;
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kF16>,
@@ -765,6 +873,7 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     if (e != cudaSuccess)
         return e;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+    p.grid = grid;
     fwd_kernel<D, kF16><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
         return e;
@@ -777,6 +886,33 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
 }
 
 }  // namespace
+
+FwdPlan plan_fwd_streamk(int B, int H, int N, int Nk, int causal, int num_sms)
+{
+    const FwdPlan none{0, 0};
+    // Only for one 128-row Q tile per head: with two, the pair's work per key
+    // tile is twice the tensor work and the partial outputs, their merge and
+    // the extra unit boundaries cost more than the idle SMs (measured: 256
+    // queries x 16K keys x 128 heads, 1173 TFLOP/s stream-K against 1304
+    // with whole heads).
+    const int QT = (N + kBM - 1) / kBM, KT = (Nk + kBN - 1) / kBN;
+    if (QT != 1 || num_sms < 1)
+        return none;
+    const int off = Nk - N;
+    const int extra = off > 0 ? (off + kBN - 1) / kBN : 0;
+    const long long F = max(key_tiles(QT, KT, extra, causal, 0), key_tiles(QT, KT, extra, causal, 1));
+    const long long BH = static_cast<long long>(B) * H;
+    const long long W = BH * F;
+    // Whole heads per CTA already fill the SMs to within 3 %, or there are
+    // fewer than two key tiles per SM: no stream-K.
+    const long long rounds = (BH + num_sms - 1) / num_sms;
+    if (BH * 100 >= rounds * num_sms * 97 || W < 2LL * num_sms)
+        return none;
+    // A head's F steps meet at most ceil(F / shortest range) + 1 ranges.
+    const long long shortest = W / num_sms;
+    const long long slots = (F + shortest - 1) / shortest + 1;
+    return FwdPlan{1, static_cast<int>(slots)};
+}
 
 cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
                              int num_sms, cudaStream_t stream)

@@ -32,10 +32,22 @@ struct FwdMaps {
 // ([splits][B*H*N][d]) and base-2 partial lse pairs ([splits][B*H*N] x 2
 // floats) to caller-provided scratch, then a combine kernel writes o / lse.
 struct FwdSplit {
-    int splits;
+    int splits;  // stream-K: partial slots per head
     float *ws_o;
     float *ws_l;
+    int streamk = 0;  // 1: stream-K schedule (one Q-tile pair per head)
 };
+
+// Stream-K plan for N queries against Nk keys per head: when every head has
+// one pair of 128-row Q tiles (N <= 256) and whole heads per CTA would leave
+// SMs idle, the (head, key tile) steps are dealt evenly over the SMs and the
+// partial results merged; slots bounds the partials of one head.  streamk 0:
+// no stream-K plan for this shape.
+struct FwdPlan {
+    int streamk;
+    int slots;
+};
+FwdPlan plan_fwd_streamk(int B, int H, int N, int Nk, int causal, int num_sms);
 
 // Device status word codes (see fattn_get_device_status in fattn.h).
 enum DeviceRole : uint32_t {

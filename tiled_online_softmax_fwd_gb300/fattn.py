@@ -78,7 +78,7 @@ def load():
         lib.attn_fwd_kv.restype = ctypes.c_int
         lib.attn_fwd_kv.argtypes = [vp] * 5 + [ip] * 5 + [fp, ip, ip, vp, ctypes.c_size_t, vp]
         lib.attn_fwd_kv_workspace_size.restype = ctypes.c_size_t
-        lib.attn_fwd_kv_workspace_size.argtypes = [ip] * 6
+        lib.attn_fwd_kv_workspace_size.argtypes = [ip] * 7
         lib.attn_bwd.restype = ctypes.c_int
         lib.attn_bwd.argtypes = [vp] * 9 + [ip, ip, ip, ip, fp, ip, vp, ctypes.c_size_t, vp]
         lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
@@ -221,10 +221,12 @@ def attn_fwd_split(q, k, v, causal: bool = False, scale: float | None = None,
     return out, lse
 
 
-def kv_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
-    """Scratch bytes attn_fwd_kv needs (num_splits 0: the library's choice on
-    the current device)."""
-    return int(load().attn_fwd_kv_workspace_size(B, H, Nq, Nk, d, num_splits))
+def kv_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool,
+                      num_splits: int = 0) -> int:
+    """Scratch bytes attn_fwd_kv needs (num_splits 0: the library's schedule
+    on the current device)."""
+    return int(load().attn_fwd_kv_workspace_size(B, H, Nq, Nk, d, 1 if causal else 0,
+                                                 num_splits))
 
 
 def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None,
@@ -251,7 +253,7 @@ def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None,
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        need = kv_workspace_size(B, H, Nq, Nk, d, num_splits)
+        need = kv_workspace_size(B, H, Nq, Nk, d, causal, num_splits)
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
         st = load().attn_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),

@@ -125,8 +125,11 @@ class KvWorkload:
 
 
 # Decode-shaped workloads: one new query row per head against a 32K-key
-# cache, and a 256-row chunk of new queries against a 16K-key cache.
+# cache (256 heads, and 64 heads for profiling), and a 256-row chunk of new
+# queries against a 16K-key cache.
 KV_WORKLOADS = {
+    "decode_B2_H32_Nq1_Nk32768_d128": KvWorkload("decode_B2_H32_Nq1_Nk32768_d128", 2, 32, 1,
+                                                 32768, 128, True, 13),
     "decode_B8_H32_Nq1_Nk32768_d128": KvWorkload("decode_B8_H32_Nq1_Nk32768_d128", 8, 32, 1,
                                                  32768, 128, True, 11),
     "chunk_B4_H32_Nq256_Nk16384_d128_causal": KvWorkload(
