@@ -68,17 +68,21 @@ def profiled_traffic(workload: str):
     """DRAM bytes per launch from a committed ncu summary of this kernel source
     and workload (null when none matches the current source)."""
     want = kernel_source_hash()
-    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
-        fields = {}
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        groups = []  # a "workload" key starts a new group of bench-key fields
         for line in open(path):
             if line.startswith("bench-key "):
                 k, _, v = line[len("bench-key "):].strip().partition("=")
-                fields[k.strip()] = v.strip()
-        if fields.get("workload") == workload and fields.get("kernel_source") == want:
-            try:
-                return int(float(fields["dram_bytes_per_launch"])), os.path.basename(path)
-            except (KeyError, ValueError):
-                pass
+                if k.strip() == "workload":
+                    groups.append({})
+                if groups:
+                    groups[-1][k.strip()] = v.strip()
+        for fields in groups:
+            if fields.get("workload") == workload and fields.get("kernel_source") == want:
+                try:
+                    return int(float(fields["dram_bytes_per_launch"])), os.path.basename(path)
+                except (KeyError, ValueError):
+                    pass
     return None, None
 
 
@@ -389,6 +393,7 @@ def run_kv(args, world, rank, local):
     hbm, hbm_src = peak_hbm()
     tc, tc_src = measured_peak()
     bound = "hbm" if gbs / hbm >= tflops / tc else "tensor"
+    traffic, traffic_src = profiled_traffic(w.name)
     if need > 0:
         rows = w.B * w.H * w.Nq
         per_split = (w.d * 4 + 8) * rows
@@ -447,7 +452,8 @@ def run_kv(args, world, rank, local):
                      "peak": hbm if bound == "hbm" else tc,
                      "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
                      "frac": gbs / hbm if bound == "hbm" else tflops / tc,
-                     "peak_source": hbm_src if bound == "hbm" else tc_src, "traffic": None,
+                     "peak_source": hbm_src if bound == "hbm" else tc_src, "traffic": traffic,
+                     "traffic_source": traffic_src,
                      "hbm_frac": gbs / hbm, "tensor_frac": tflops / tc,
                      "algorithmic_bytes_per_launch": w.io_bytes,
                      "algorithmic_flops_per_launch": w.flops},
