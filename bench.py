@@ -189,8 +189,13 @@ def cpu_baseline(w, q, k, v, rows_all, budget_s=15.0):
         total_rows += take.numel()
         total_flops += rows_flops(w, take)
         used += 1
+    # The same oracle on one core, over the first block of rows.
+    take = per_head[:, :8].reshape(-1)[:64]
+    t0 = time.perf_counter()
+    oracle.attn_fwd(qd, kd, vd, w.scale, w.causal, rows=take.numpy(), threads=1)
+    single = rows_flops(w, take) / (time.perf_counter() - t0) / 1e12
     return {"value": total_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle",
+            "kind": "oracle", "single_core_value": single,
             "sample": "%d query rows (%d seeded rows per head x %d heads, all their keys), %.1f s" %
                       (total_rows, total_rows // (w.B * w.H), w.B * w.H, t_total)}
 
@@ -510,6 +515,7 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
 
+    step_ms = None
     with ClockSampler(local) as clocks:
         t_wall0 = time.perf_counter()
         if big:
@@ -530,7 +536,8 @@ def run_gpu(args, world, rank, local):
                 step()
                 b.record(stream)
             torch.cuda.synchronize()
-            kernel_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+            step_ms = sorted(a.elapsed_time(b) for a, b in evs)
+            kernel_ms = sum(step_ms) / args.steps
         wall_ms = (time.perf_counter() - t_wall0) * 1e3 / args.steps
     barrier(world)
     torch.cuda.synchronize()
@@ -589,6 +596,12 @@ def run_gpu(args, world, rank, local):
         "clocks": clocks.summary(),
         "device_status": status,
     }
+    if step_ms is not None:
+        # Steps timed one by one (L2 flushed before each): quantiles of the
+        # step time and the achieved bandwidth of the algorithmic bytes.
+        q = lambda f: step_ms[min(len(step_ms) - 1, int(f * len(step_ms)))]
+        line["step_quantiles_ms"] = {"p20": q(0.2), "p50": q(0.5), "p80": q(0.8)}
+        line["algorithmic_gbs_p50"] = w.io_bytes / (q(0.5) * 1e-3) / 1e9
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:

@@ -202,6 +202,35 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
  */
 size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal,
                                   int num_splits);
+
+/*
+ * attn_fwd_strided -- attn_fwd_kv on tensors with arbitrary strides: the
+ * kernel takes the layout's strides explicitly instead of assuming a
+ * contiguous one ("Triton programming template", the Python wrapper section;
+ * "CS336 lecture 6: kernels and Triton", the matmul + ReLU example's note on
+ * strided pointers for non-contiguous layouts).  E.g. q, k, v as views of one
+ * packed [B][N][3][H][d] projection output, or o written into a [B][N][H][d]
+ * buffer.
+ *
+ *   x_strides[3] : element strides of (batch, head, row) for x in q, k, v, o;
+ *                  the last dimension (d) is contiguous (stride 1).
+ * Element (b, h, i, c) of x lives at x + b*s[0] + h*s[1] + i*s[2] + c.
+ * Every stride must be a positive multiple of 8 elements (16 bytes) and at
+ * most 2^38; the stride of a dimension of extent 1 is ignored.  q, k, v may
+ * overlap each other (all are only read); o's elements must be distinct
+ * (checked by nesting: its strides sorted by size, each at least the span
+ * of the smaller dimensions) and o must not overlap q, k, v or lse (checked
+ * over each tensor's address span).  lse stays contiguous fp32 [B][H][Nq].
+ * Everything else -- shapes, the causal alignment, num_splits, the workspace
+ * (attn_fwd_kv_workspace_size) and the errors -- is attn_fwd_kv's.  A
+ * stride array that is NULL gives FATTN_ERR_INVALID_ARG.
+ */
+fattn_status_t attn_fwd_strided(const void *q, const void *k, const void *v, void *o,
+                                float *lse, int B, int H, int Nq, int Nk, int d,
+                                const long long *q_strides, const long long *k_strides,
+                                const long long *v_strides, const long long *o_strides,
+                                float scale, int causal, int num_splits, void *workspace,
+                                size_t workspace_bytes, struct CUstream_st *stream);
 fattn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
                            int num_splits, void *workspace, size_t workspace_bytes,

@@ -183,6 +183,36 @@ def test_kv_arguments_are_checked(lib):
     assert call(1, 1, 0, 0, 64, causal=1) == OK
 
 
+def test_strided_arguments_are_checked(lib):
+    f = lib.attn_fwd_strided
+    L3 = ctypes.c_longlong * 3
+    ptrs = [A, A + (1 << 24), A + (2 << 24), A + (3 << 24), A + (4 << 24)]
+    B, H, N, d = 2, 3, 40, 64
+    dense = L3(H * N * d, N * d, d)
+
+    def call(qs=dense, ks=dense, vs=dense, os_=dense, p=ptrs, causal=0):
+        return f(*p, B, H, N, N, d, qs, ks, vs, os_, 0.125, causal, 1, None, 0, None)
+    assert call(qs=None) == INVALID
+    assert call(os_=L3(H * N * d, N * d, d + 4)) == INVALID       # not a multiple of 8
+    assert call(ks=L3(H * N * d, 0, d)) == INVALID                # zero stride, extent 3
+    assert call(os_=L3(H * N * d, N * d, 32)) == INVALID          # o rows overlap (32 < d)
+    assert call(os_=L3(N * d, N * d, d)) == INVALID               # o heads alias batches
+    # o's span reaching into k's span
+    assert call(p=ptrs[:3] + [ptrs[1] + 64] + ptrs[4:]) == INVALID
+    # The layouts below pass the layout checks; with no device the call then
+    # fails on the device query (with one, on the fake pointers).
+    import torch
+    if torch.cuda.is_available():
+        return
+    # q, k, v may overlap each other: one packed buffer [B][N][3][H][d]
+    packed = L3(N * 3 * H * d, d, 3 * H * d)
+    q0 = A
+    p_packed = [q0, q0 + H * d * 2, q0 + 2 * H * d * 2, A + (5 << 24), A + (6 << 24)]
+    assert call(qs=packed, ks=packed, vs=packed, p=p_packed) not in (INVALID, UNSUPPORTED)
+    # o interleaved as [B][N][H][d] is a valid nesting
+    assert call(os_=L3(N * H * d, d, H * d)) not in (INVALID, UNSUPPORTED)
+
+
 def test_rowop_arguments_are_checked(lib):
     for f in (lib.fattn_softmax_rows, lib.fattn_row_sum):
         assert f(A, A + (1 << 24), -1, 4, 0, None) == INVALID      # negative M

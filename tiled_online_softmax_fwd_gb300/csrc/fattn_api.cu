@@ -180,14 +180,113 @@ fattn_status_t make_map(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m
     return FATTN_OK;
 }
 
+// Element strides (batch, head, row) of q, k, v and o; the last dimension
+// (d) is contiguous.
+struct Layout {
+    long long q[3], k[3], v[3], o[3];
+};
+
+Layout dense_layout(int H, int N, int Nk, int d)
+{
+    const long long qn = d, qh = static_cast<long long>(N) * d, qb = qh * H;
+    const long long kh = static_cast<long long>(Nk) * d, kb = kh * H;
+    return Layout{{qb, qh, qn}, {kb, kh, qn}, {kb, kh, qn}, {qb, qh, qn}};
+}
+
+// Bytes from a tensor's base to one past its last element.
+size_t span_bytes(const long long st[3], int B, int H, int rows, int d)
+{
+    return static_cast<size_t>(st[0] * (B - 1) + st[1] * (H - 1) +
+                               st[2] * static_cast<long long>(rows - 1) + d) * 2;
+}
+
+// 4-D map (d, rows, H, B) of a 16-bit tensor with element strides st
+// (batch, head, row), box (64, 128, 1, 1), 128-byte swizzle, zero fill
+// outside the tensor.
+fattn_status_t make_map4(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m,
+                         const void *ptr, int rows, int d, int H, int B, const long long st[3],
+                         bool f16)
+{
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2,
+                                   static_cast<cuuint64_t>(st[1]) * 2,
+                                   static_cast<cuuint64_t>(st[0]) * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+    const CUresult r = encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              4, const_cast<void *>(ptr), dims, strides, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return FATTN_ERR_CUDA;
+    }
+    return FATTN_OK;
+}
+
+// Stride rules of a strided call: every stride a positive multiple of 8
+// elements (16 bytes, the tensor-map rule; o is written in 16-byte pieces),
+// each tensor's span below 2^39 bytes, o's elements all distinct (nested
+// strides: sorted by size, each stride at least the span of the smaller
+// dimensions), and no output overlapping an input or the other output.
+fattn_status_t check_layout(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, int B, int H, int N, int Nk, int d, const Layout &L)
+{
+    if (!q || !k || !v || !o || !lse)
+        return FATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FATTN_ERR_INVALID_ARG;
+    const long long *all[4] = {L.q, L.k, L.v, L.o};
+    const int rows[4] = {N, Nk, Nk, N};
+    size_t span[4];
+    for (int t = 0; t < 4; ++t) {
+        for (int i = 0; i < 3; ++i)
+            if (all[t][i] < 1 || all[t][i] % 8 != 0 || all[t][i] > (1LL << 38))
+                return FATTN_ERR_INVALID_ARG;
+        const long double far = static_cast<long double>(all[t][0]) * (B - 1) +
+                                static_cast<long double>(all[t][1]) * (H - 1) +
+                                static_cast<long double>(all[t][2]) * (rows[t] - 1) + d;
+        if (far * 2 >= static_cast<long double>(1LL << 39))
+            return FATTN_ERR_UNSUPPORTED;
+        span[t] = span_bytes(all[t], B, H, rows[t], d);
+    }
+    // o: nested strides over the dimensions of extent > 1.
+    long long st[3] = {L.o[2], L.o[1], L.o[0]};
+    long long ext[3] = {N, H, B};
+    for (int i = 0; i < 3; ++i)  // sort by stride (3 elements)
+        for (int j = i + 1; j < 3; ++j)
+            if (st[j] < st[i]) {
+                long long t = st[i]; st[i] = st[j]; st[j] = t;
+                t = ext[i]; ext[i] = ext[j]; ext[j] = t;
+            }
+    long long covered = d;
+    for (int i = 0; i < 3; ++i) {
+        if (ext[i] <= 1)
+            continue;
+        if (st[i] < covered)
+            return FATTN_ERR_INVALID_ARG;
+        covered += st[i] * (ext[i] - 1);
+    }
+    const size_t lb = static_cast<size_t>(B) * H * N * 4;
+    if (overlap(o, span[3], q, span[0]) || overlap(o, span[3], k, span[1]) ||
+        overlap(o, span[3], v, span[2]) || overlap(o, span[3], lse, lb) ||
+        overlap(lse, lb, q, span[0]) || overlap(lse, lb, k, span[1]) ||
+        overlap(lse, lb, v, span[2]))
+        return FATTN_ERR_INVALID_ARG;
+    return FATTN_OK;
+}
+
 enum class Kernel { kTcgen05, kTcgen05F16, kSimt };
 
 // Every check of a forward call with N queries and Nk keys per head.  On
 // FATTN_OK, *empty tells whether there is any work, and (when there is)
 // *dev / *info describe the current device.
+// L == nullptr: contiguous tensors.
 fattn_status_t validate(const void *q, const void *k, const void *v, const void *o,
                         const float *lse, int B, int H, int N, int Nk, int d, float scale,
-                        int causal, bool *empty, int *dev, DeviceInfo *info)
+                        int causal, bool *empty, int *dev, DeviceInfo *info,
+                        const Layout *L = nullptr)
 {
     fattn_status_t s = check_shape(B, H, N, d, scale, causal, empty);
     if (s != FATTN_OK)
@@ -196,7 +295,11 @@ fattn_status_t validate(const void *q, const void *k, const void *v, const void 
         return s;
     const size_t rows = static_cast<size_t>(B) * H * N;
     const size_t kv_bytes = static_cast<size_t>(B) * H * Nk * d * 2;
-    if ((s = check_pointers(q, k, v, o, lse, rows * d * 2, kv_bytes, rows * 4)) != FATTN_OK)
+    if (L != nullptr)
+        s = check_layout(q, k, v, o, lse, B, H, N, Nk, d, *L);
+    else
+        s = check_pointers(q, k, v, o, lse, rows * d * 2, kv_bytes, rows * 4);
+    if (s != FATTN_OK)
         return s;
     if ((s = current_device(dev, info)) != FATTN_OK)
         return s;
@@ -212,7 +315,8 @@ fattn_status_t validate(const void *q, const void *k, const void *v, const void 
 fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const void *k,
                       const void *v, void *o, float *lse, int B, int H, int N, int Nk, int d,
                       float scale, int causal, cudaStream_t stream,
-                      const fattn::FwdSplit &split = fattn::FwdSplit{1, nullptr, nullptr})
+                      const fattn::FwdSplit &split = fattn::FwdSplit{1, nullptr, nullptr},
+                      const Layout *L = nullptr)
 {
     fattn::FwdArgs a{q, k, v, o, lse, B, H, N, d, scale, causal};
     const bool f16 = which == Kernel::kTcgen05F16;
@@ -220,7 +324,7 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
     a.Nk = Nk;
     cudaError_t e;
     if (which == Kernel::kSimt) {
-        if (Nk != N)
+        if (Nk != N || L != nullptr)
             return FATTN_ERR_UNSUPPORTED;
         e = fattn::launch_fwd_simt(a, stream);
     } else {
@@ -228,11 +332,14 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
         fattn_status_t s;
         if ((s = get_encoder(&encode)) != FATTN_OK)
             return s;
+        const Layout lay = L != nullptr ? *L : dense_layout(H, N, Nk, d);
+        a.o_sb = lay.o[0];
+        a.o_sh = lay.o[1];
+        a.o_sn = lay.o[2];
         fattn::FwdMaps maps;
-        const long long BH = static_cast<long long>(B) * H;
-        if ((s = make_map(encode, &maps.q, q, N, d, BH, f16)) != FATTN_OK ||
-            (s = make_map(encode, &maps.k, k, Nk, d, BH, f16)) != FATTN_OK ||
-            (s = make_map(encode, &maps.v, v, Nk, d, BH, f16)) != FATTN_OK)
+        if ((s = make_map4(encode, &maps.q, q, N, d, H, B, lay.q, f16)) != FATTN_OK ||
+            (s = make_map4(encode, &maps.k, k, Nk, d, H, B, lay.k, f16)) != FATTN_OK ||
+            (s = make_map4(encode, &maps.v, v, Nk, d, H, B, lay.v, f16)) != FATTN_OK)
             return s;
         e = fattn::launch_fwd_sm103(a, maps, split, info.num_sms, stream);
     }
@@ -311,10 +418,11 @@ int auto_slots(int B, int H, int Nq, int Nk, int causal, int num_sms, int *strea
 }
 
 // num_splits == 0: the automatic schedule for the current device.
+// L == nullptr: contiguous tensors.
 fattn_status_t forward_split(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int H, int N, int Nk, int d, float scale, int causal,
                              int num_splits, void *workspace, size_t workspace_bytes,
-                             cudaStream_t stream)
+                             cudaStream_t stream, const Layout *L = nullptr)
 {
     if (num_splits < 0 || num_splits > kMaxSplits)
         return FATTN_ERR_INVALID_ARG;
@@ -322,7 +430,7 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
     int dev = 0;
     DeviceInfo info;
     fattn_status_t s =
-        validate(q, k, v, o, lse, B, H, N, Nk, d, scale, causal, &empty, &dev, &info);
+        validate(q, k, v, o, lse, B, H, N, Nk, d, scale, causal, &empty, &dev, &info, L);
     if (s != FATTN_OK || empty)
         return s;
     int streamk = 0;
@@ -330,15 +438,16 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
         num_splits = auto_slots(B, H, N, Nk, causal, info.num_sms, &streamk);
     if (num_splits == 1)
         return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal,
-                      stream);
+                      stream, fattn::FwdSplit{1, nullptr, nullptr}, L);
     const size_t need = split_ws_bytes(B, H, N, d, num_splits);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return FATTN_ERR_INVALID_ARG;
-    const size_t rows = static_cast<size_t>(B) * H * N;
-    const size_t tb = rows * d * 2, lb = rows * 4;
-    const size_t kvb = static_cast<size_t>(B) * H * Nk * d * 2;
-    if (overlap(workspace, need, q, tb) || overlap(workspace, need, k, kvb) ||
-        overlap(workspace, need, v, kvb) || overlap(workspace, need, o, tb) ||
+    const Layout lay = L != nullptr ? *L : dense_layout(H, N, Nk, d);
+    const size_t lb = static_cast<size_t>(B) * H * N * 4;
+    if (overlap(workspace, need, q, span_bytes(lay.q, B, H, N, d)) ||
+        overlap(workspace, need, k, span_bytes(lay.k, B, H, Nk, d)) ||
+        overlap(workspace, need, v, span_bytes(lay.v, B, H, Nk, d)) ||
+        overlap(workspace, need, o, span_bytes(lay.o, B, H, N, d)) ||
         overlap(workspace, need, lse, lb))
         return FATTN_ERR_INVALID_ARG;
     if ((s = check_device_buffer(workspace, dev)) != FATTN_OK)
@@ -349,7 +458,7 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
         reinterpret_cast<float *>(ws + align_up(split_ws_o_bytes(B, H, N, d, num_splits), kWsAlign)),
         streamk};
     return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream,
-                  split);
+                  split, L);
 }
 
 // ---------------------------------------------------------------- no-allocation split
@@ -426,6 +535,38 @@ fattn_status_t attn_fwd_split(const void *q, const void *k, const void *v, void 
         return FATTN_ERR_INVALID_ARG;
     return forward_split(q, k, v, o, lse, B, H, N, N, d, scale, causal, num_splits, workspace,
                          workspace_bytes, stream);
+}
+
+fattn_status_t attn_fwd_strided(const void *q, const void *k, const void *v, void *o,
+                                float *lse, int B, int H, int Nq, int Nk, int d,
+                                const long long *q_strides, const long long *k_strides,
+                                const long long *v_strides, const long long *o_strides,
+                                float scale, int causal, int num_splits, void *workspace,
+                                size_t workspace_bytes, struct CUstream_st *stream)
+{
+    if (!q_strides || !k_strides || !v_strides || !o_strides)
+        return FATTN_ERR_INVALID_ARG;
+    Layout L;
+    for (int i = 0; i < 3; ++i) {
+        L.q[i] = q_strides[i];
+        L.k[i] = k_strides[i];
+        L.v[i] = v_strides[i];
+        L.o[i] = o_strides[i];
+    }
+    // A dimension of extent 1 has no meaningful stride: give it the span of
+    // the smaller dimensions, as a contiguous tensor would have.
+    long long *all[4] = {L.q, L.k, L.v, L.o};
+    const int rows[4] = {Nq, Nk, Nk, Nq};
+    for (int t = 0; t < 4; ++t) {
+        if (rows[t] == 1)
+            all[t][2] = (static_cast<long long>(d) + 7) / 8 * 8;
+        if (H == 1)
+            all[t][1] = all[t][2] * (rows[t] > 0 ? rows[t] : 1);
+        if (B == 1)
+            all[t][0] = all[t][1] * (H > 0 ? H : 1);
+    }
+    return forward_split(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, workspace,
+                         workspace_bytes, stream, &L);
 }
 
 size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal,

@@ -98,7 +98,7 @@ struct Bars {
 };
 
 struct Params {
-    void *o;       // bf16 or fp16 [B*H*Nq][D]
+    void *o;       // bf16 or fp16, element (b, h, i, c) at b*o_sb + h*o_sh + i*o_sn + c
     float *lse;
     float *ws_o;   // split mode: fp32 partial O [splits][B*H*Nq][D]
     float2 *ws_l;  // split mode: base-2 partial lse (exact sum, rounded sum) [splits][B*H*Nq]
@@ -107,6 +107,8 @@ struct Params {
     int off;       // Nk - Nq: query i sits at key position i + off (causal mask)
     int extra;     // ceil(off / 128): key tiles past the diagonal (causal mask)
     int BH;        // batch * heads
+    int H;         // heads
+    long long o_sb, o_sh, o_sn;  // element strides of o (batch, head, row)
     int QT;        // query tiles per head = ceil(Nq / 128)
     int KT;        // key tiles per head = ceil(Nk / 128)
     int pairs;     // Q-tile pairs per head = ceil(QT / 2)
@@ -272,6 +274,7 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
         Unit u;
         if (!cta_unit(p, b, r, u))
             break;
+        const int hh = u.bh % p.H, bb = u.bh / p.H;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (!ok || u.n[t] == 0)
@@ -286,7 +289,7 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
                 const uint32_t dst = smem_base + t * C::kTileBytes;
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(dst + c * kChunkBytes, mq, full, 64 * c, u.qt[t] * kBM, u.bh);
+                    tma_load_4d(dst + c * kChunkBytes, mq, full, 64 * c, u.qt[t] * kBM, hh, bb);
             }
             last_q_parity[t] = q_phase[t];
             q_phase[t] ^= 1;
@@ -307,7 +310,7 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
                     const CUtensorMap *m = which == 0 ? mk : mv;
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(dst + c * kChunkBytes, m, full, 64 * c, j * kBN, u.bh);
+                        tma_load_4d(dst + c * kChunkBytes, m, full, 64 * c, j * kBN, hh, bb);
                 }
             }
         }
@@ -609,7 +612,8 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         const bool live = row < p.Nq;
         const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
         if (p.splits == 1) {
-            uint16_t *orow = static_cast<uint16_t *>(p.o) + grow * D;
+            uint16_t *orow = static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb +
+                             (u.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -822,7 +826,8 @@ __global__ void __launch_bounds__(256)
         }
     }
     const float inv = 1.f / sr;
-    uint16_t *dst = static_cast<uint16_t *>(p.o) + static_cast<size_t>(row) * D + lane * kCols;
+    uint16_t *dst = static_cast<uint16_t *>(p.o) + (bh / p.H) * p.o_sb + (bh % p.H) * p.o_sh +
+                    static_cast<long long>(i) * p.o_sn + lane * kCols;
 #pragma unroll
     for (int c = 0; c < kCols; c += 2)
         *reinterpret_cast<uint32_t *>(dst + c) = pack2<kF16>(acc[c] * inv, acc[c + 1] * inv);
@@ -845,6 +850,11 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     p.off = a.Nk - a.N;
     p.extra = p.off > 0 ? (p.off + kBN - 1) / kBN : 0;
     p.BH = a.B * a.H;
+    p.H = a.H;
+    const bool dense_o = a.o_sb == 0 && a.o_sh == 0 && a.o_sn == 0;
+    p.o_sn = dense_o ? D : a.o_sn;
+    p.o_sh = dense_o ? static_cast<long long>(a.N) * D : a.o_sh;
+    p.o_sb = dense_o ? static_cast<long long>(a.H) * a.N * D : a.o_sb;
     p.QT = (a.N + kBM - 1) / kBM;
     p.KT = (a.Nk + kBN - 1) / kBN;
     p.pairs = (p.QT + 1) / 2;

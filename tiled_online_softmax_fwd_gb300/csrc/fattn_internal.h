@@ -20,10 +20,14 @@ struct FwdArgs {
     int f16 = 0;  // 1: fp16 q, k, v, o (P in fp16); 0: bf16
     int Nk = 0;   // keys per head (N: queries per head); the queries are the
                   // last N key positions under the causal mask
+    // Element strides of o for (batch, head, row); all 0 = contiguous.
+    long long o_sb = 0, o_sh = 0, o_sn = 0;
 };
 
-// Tensor maps over Q, K, V viewed as 3-D bf16 arrays (d, N or Nk, B*H), box
-// (64, 128, 1), 128-byte swizzle, zero fill outside the sequence.
+// Tensor maps over Q, K, V.  The forward kernel takes 4-D maps (d, N or Nk,
+// H, B) with the tensors' own row, head and batch strides, box (64, 128, 1,
+// 1); the backward takes 3-D maps (d, N, B*H) of contiguous tensors, box
+// (64, 128, 1).  128-byte swizzle, zero fill outside the sequence.
 struct FwdMaps {
     CUtensorMap q, k, v;
 };

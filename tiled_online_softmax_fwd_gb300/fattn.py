@@ -22,7 +22,7 @@ FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
                 3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
 EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_fp16", "attn_fwd_host",
-            "attn_fwd_kv", "attn_fwd_kv_workspace_size", "attn_fwd_simt",
+            "attn_fwd_kv", "attn_fwd_kv_workspace_size", "attn_fwd_simt", "attn_fwd_strided",
             "attn_fwd_split",
             "attn_fwd_split_count", "attn_fwd_split_noalloc", "attn_fwd_split_workspace_size",
             "fattn_status_string",
@@ -77,6 +77,10 @@ def load():
         lib.attn_fwd_split_workspace_size.argtypes = [ip, ip, ip, ip, ip]
         lib.attn_fwd_kv.restype = ctypes.c_int
         lib.attn_fwd_kv.argtypes = [vp] * 5 + [ip] * 5 + [fp, ip, ip, vp, ctypes.c_size_t, vp]
+        i64p = ctypes.POINTER(ctypes.c_longlong)
+        lib.attn_fwd_strided.restype = ctypes.c_int
+        lib.attn_fwd_strided.argtypes = [vp] * 5 + [ip] * 5 + [i64p] * 4 + [
+            fp, ip, ip, vp, ctypes.c_size_t, vp]
         lib.attn_fwd_kv_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_kv_workspace_size.argtypes = [ip] * 7
         lib.attn_bwd.restype = ctypes.c_int
@@ -261,6 +265,47 @@ def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None,
                                 int(num_splits), workspace.data_ptr() if need > 0 else 0,
                                 workspace.numel(), _stream_handle(stream, q.device))
     _check(st, "attn_fwd_kv")
+    return out, lse
+
+
+def attn_fwd_strided(q, k, v, causal: bool = False, scale: float | None = None,
+                     num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
+    """attn_fwd_kv on 4-D bf16 views [B, H, Nq|Nk, d] with any strides whose last
+    dimension is contiguous (libfattn attn_fwd_strided): e.g. q, k, v sliced
+    from one packed projection output.  ``out`` may be a strided view too;
+    by default a contiguous one is allocated."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 \
+                or t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError("%s must be a 4-D bf16 CUDA tensor with a contiguous last "
+                             "dimension" % name)
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] do not match: %s %s %s"
+                         % (q.shape, k.shape, v.shape))
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = default_scale(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or out.stride(3) != 1:
+        raise ValueError("out must be a bf16 [B, H, Nq, d] view with a contiguous last dimension")
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+
+    def strides(t):
+        return (ctypes.c_longlong * 3)(*t.stride()[:3])
+    with torch.cuda.device(q.device):
+        need = kv_workspace_size(B, H, Nq, Nk, d, causal, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        st = load().attn_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     lse.data_ptr(), B, H, Nq, Nk, d, strides(q), strides(k),
+                                     strides(v), strides(out), float(scale),
+                                     1 if causal else 0, int(num_splits),
+                                     workspace.data_ptr() if need > 0 else 0, workspace.numel(),
+                                     _stream_handle(stream, q.device))
+    _check(st, "attn_fwd_strided")
     return out, lse
 
 
