@@ -35,8 +35,11 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from tiled_online_softmax_fwd_gb300.inputs import (KV_WORKLOADS, WORKLOADS, digest,  # noqa: E402
-                                                   make_qkv_kv, make_workload)
+from tiled_online_softmax_fwd_gb300.inputs import (KV_WORKLOADS, VARIANT_WORKLOADS,  # noqa: E402
+                                                   WORKLOADS, digest, make_qkv_kv,
+                                                   make_workload)
+
+ALL_WORKLOADS = {**WORKLOADS, **VARIANT_WORKLOADS}
 
 DEFAULT_WORKLOAD = "B1_H32_N16384_d128_causal_sigma3"
 METRIC = "attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
@@ -204,7 +207,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     import oracle
-    w = WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     g = torch.Generator("cpu").manual_seed(w.seed)
     from tiled_online_softmax_fwd_gb300.inputs import make_qkv, sample_rows
     q, k, v = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, generator=g)
@@ -478,7 +481,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     fattn.load()
-    w = WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     q, k, v, rows_all = make_workload(w, dtype=torch.float16 if args.fp16 else torch.bfloat16)
     in_digest = digest(q, k, v)
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
@@ -617,7 +620,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(ALL_WORKLOADS))
     ap.add_argument("--impl", default="libfattn", choices=["libfattn", "reference"])
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")

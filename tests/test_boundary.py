@@ -74,7 +74,7 @@ def test_empty_problems_are_noops(lib):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(B=-1), INVALID), (dict(H=-1), INVALID), (dict(N=-5), INVALID),
-    (dict(d=96), UNSUPPORTED), (dict(d=0), UNSUPPORTED), (dict(d=256), UNSUPPORTED),
+    (dict(d=80), UNSUPPORTED), (dict(d=0), UNSUPPORTED), (dict(d=256), UNSUPPORTED),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(causal=2), INVALID), (dict(causal=-1), INVALID),
@@ -136,7 +136,7 @@ def test_split_workspace_size(lib):
     o_bytes = 10 * rows * 64 * 4
     aligned = (o_bytes + 255) // 256 * 256
     assert f(1, 1, 4096, 64, 10) == aligned + 10 * rows * 8
-    assert f(1, 1, 4096, 96, 2) == 0 and f(1, 1, 4096, 64, 0) == 0 and f(1, 1, 4096, 64, 65) == 0
+    assert f(1, 1, 4096, 80, 2) == 0 and f(1, 1, 4096, 64, 0) == 0 and f(1, 1, 4096, 64, 65) == 0
 
 
 def test_split_arguments_are_checked(lib):
@@ -155,7 +155,7 @@ def test_kv_workspace_size(lib):
     o_bytes = 7 * rows * 128 * 4
     assert f(2, 3, 5, 9000, 128, 1, 7) == (o_bytes + 255) // 256 * 256 + 7 * rows * 8
     assert f(2, 3, 5, 9000, 128, 0, 1) == 0
-    assert f(2, 3, 5, 9000, 96, 0, 7) == 0 and f(2, 3, 5, 9000, 128, 0, 65) == 0
+    assert f(2, 3, 5, 9000, 80, 0, 7) == 0 and f(2, 3, 5, 9000, 128, 0, 65) == 0
     assert f(2, 3, 5, 9000, 128, 0, -1) == 0 and f(2, 3, 5, 0, 128, 0, 7) == 0   # no keys
     assert f(2, 3, 5, -1, 128, 0, 7) == 0 and f(1, 1, 9, 5, 64, 1, 2) == 0   # Nq > Nk, causal
 

@@ -95,7 +95,7 @@ fattn_status_t check_shape(int B, int H, int N, int d, float scale, int causal, 
         return FATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale))
         return FATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128)
+    if (d != 64 && d != 96 && d != 128)
         return FATTN_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(B) * H * N;
     *empty = rows == 0;
@@ -624,7 +624,7 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
 size_t attn_bwd_workspace_size(int B, int H, int N, int d)
 {
     bool empty = false;
-    if (check_shape(B, H, N, d, 1.0f, 0, &empty) != FATTN_OK || empty)
+    if (d == 96 || check_shape(B, H, N, d, 1.0f, 0, &empty) != FATTN_OK || empty)
         return 0;
     return static_cast<size_t>(B) * H * N * sizeof(float);
 }
@@ -638,6 +638,8 @@ fattn_status_t attn_bwd(const void *q, const void *k, const void *v, const void 
     fattn_status_t s = check_shape(B, H, N, d, scale, causal, &empty);
     if (s != FATTN_OK || empty)
         return s;
+    if (d == 96)  // the backward kernels take d = 64 or 128
+        return FATTN_ERR_UNSUPPORTED;
     const size_t rows = static_cast<size_t>(B) * H * N;
     const size_t tb = rows * d * 2, lb = rows * 4;
     const void *ins[6] = {q, k, v, o, lse, dout};

@@ -136,6 +136,9 @@ cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t stream)
     if (a.d == 64)
         fwd_simt_kernel<64><<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(
             q, k, v, o, a.lse, a.N, row_blocks, a.scale, a.causal);
+    else if (a.d == 96)
+        fwd_simt_kernel<96><<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(
+            q, k, v, o, a.lse, a.N, row_blocks, a.scale, a.causal);
     else
         fwd_simt_kernel<128><<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(
             q, k, v, o, a.lse, a.N, row_blocks, a.scale, a.causal);

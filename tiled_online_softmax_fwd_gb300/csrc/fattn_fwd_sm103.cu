@@ -74,9 +74,12 @@ constexpr uint32_t kChunkBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 
 
 template <int D>
 struct Cfg {
-    static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along d
+    // 128-byte swizzle atoms along d.  d = 96 takes two: the tensor map's
+    // 64-column box reads columns 96..127 as zeros, which no MMA uses (the
+    // S product stops at K = 96, the P V product has N = 96).
+    static constexpr int kChunks = (D + 63) / 64;
     static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
-    static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring depth
+    static constexpr int kStages = kChunks == 2 ? 4 : 8;  // K/V ring depth
     static constexpr uint32_t kTilesBytes = (2 + kStages) * kTileBytes;
     static constexpr uint32_t kColO0 = 256;
     static constexpr uint32_t kColO1 = 256 + D;
@@ -359,7 +362,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint3
                                          bool accumulate)
 {
     constexpr uint32_t idesc = idesc_f32acc(kBM, D, true, kF16);
-    constexpr uint32_t kVLbo = D == 128 ? kChunkBytes : 1024;
+    constexpr uint32_t kVLbo = D > 64 ? kChunkBytes : 1024;
     constexpr uint32_t hi = smem_desc_hi(1024);
     const uint32_t b_lo = smem_desc_lo(v_smem, kVLbo);
     const uint32_t acc0 = accumulate ? 1u : 0u;
@@ -828,9 +831,15 @@ __global__ void __launch_bounds__(256)
     const float inv = 1.f / sr;
     uint16_t *dst = static_cast<uint16_t *>(p.o) + (bh / p.H) * p.o_sb + (bh % p.H) * p.o_sh +
                     static_cast<long long>(i) * p.o_sn + lane * kCols;
+    if constexpr (kCols % 2 == 0) {
 #pragma unroll
-    for (int c = 0; c < kCols; c += 2)
-        *reinterpret_cast<uint32_t *>(dst + c) = pack2<kF16>(acc[c] * inv, acc[c + 1] * inv);
+        for (int c = 0; c < kCols; c += 2)
+            *reinterpret_cast<uint32_t *>(dst + c) = pack2<kF16>(acc[c] * inv, acc[c + 1] * inv);
+    } else {  // d = 96: three columns per lane, stored one by one
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+            dst[c] = static_cast<uint16_t>(pack2<kF16>(acc[c] * inv, 0.f) & 0xffffu);
+    }
     if (lane == 0)
         p.lse[row] = (mx_e + log2f(se)) * kLn2;
 }
@@ -927,11 +936,18 @@ FwdPlan plan_fwd_streamk(int B, int H, int N, int Nk, int causal, int num_sms)
 cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
                              int num_sms, cudaStream_t stream)
 {
-    if (a.f16)
-        return a.d == 64 ? launch<64, true>(a, maps, split, num_sms, stream)
-                         : launch<128, true>(a, maps, split, num_sms, stream);
-    return a.d == 64 ? launch<64, false>(a, maps, split, num_sms, stream)
+    switch (a.d) {
+    case 64:
+        return a.f16 ? launch<64, true>(a, maps, split, num_sms, stream)
+                     : launch<64, false>(a, maps, split, num_sms, stream);
+    case 96:
+        return a.f16 ? launch<96, true>(a, maps, split, num_sms, stream)
+                     : launch<96, false>(a, maps, split, num_sms, stream);
+    case 128:
+        return a.f16 ? launch<128, true>(a, maps, split, num_sms, stream)
                      : launch<128, false>(a, maps, split, num_sms, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 namespace {

@@ -140,8 +140,8 @@ def _validate(q, k, v, dtype=torch.bfloat16):
         raise ValueError("q, k, v shapes differ: %s %s %s" % (q.shape, k.shape, v.shape))
     if not (q.device == k.device == v.device):
         raise ValueError("q, k, v are on different devices")
-    if q.shape[-1] not in (64, 128):
-        raise ValueError("head dimension must be 64 or 128, got %d" % q.shape[-1])
+    if q.shape[-1] not in (64, 96, 128):
+        raise ValueError("head dimension must be 64, 96 or 128, got %d" % q.shape[-1])
 
 
 def _forward(entry: str, q, k, v, causal, scale, out, lse, stream):
@@ -317,6 +317,8 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     given (the library itself never allocates)."""
     _validate(q, k, v)
     B, H, N, d = q.shape
+    if d not in (64, 128):
+        raise ValueError("the backward takes head dimension 64 or 128, got %d" % d)
     for name, t in (("o", o), ("dout", dout)):
         if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() \
                 or t.device != q.device:

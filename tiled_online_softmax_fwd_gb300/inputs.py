@@ -71,6 +71,12 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# A head dimension outside the five: d = 96, causal, the shape of the third.
+VARIANT_WORKLOADS = {
+    "B4_H16_N4096_d96_causal": Workload("B4_H16_N4096_d96_causal", 4, 16, 4096, 96, True, 5,
+                                        rows_per_head=256),
+}
+
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int, sigma_qk: float = 1.0,
              generator: torch.Generator | None = None, dtype=torch.bfloat16):
