@@ -43,6 +43,10 @@
 // fp32 probabilities, for lse, and l_round of the bf16-rounded probabilities
 // that actually enter P V, which normalises O, so that the weights applied to
 // V sum to one exactly (the rounding of a dominant p cancels in O / l_round).
+// For bf16 with d = 64 the tensor cores form l_round: V is extended by a
+// constant column of ones (its own 16 KB swizzle atom after the K/V ring),
+// so column d of the O accumulator is the row sum of the rounded P, summed in
+// fp32 and rescaled together with O (see Cfg::kOnes).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <float.h>
@@ -72,7 +76,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kChunkBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 box
 
-template <int D>
+template <int D, bool kF16 = false>
 struct Cfg {
     // 128-byte swizzle atoms along d.  d = 96 takes two: the tensor map's
     // 64-column box reads columns 96..127 as zeros, which no MMA uses (the
@@ -80,9 +84,15 @@ struct Cfg {
     static constexpr int kChunks = (D + 63) / 64;
     static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
     static constexpr int kStages = kChunks == 2 ? 4 : 8;  // K/V ring depth
-    static constexpr uint32_t kTilesBytes = (2 + kStages) * kTileBytes;
+    // Ones column: P V runs with N = D + 16 against V extended by a constant
+    // atom whose first column is 1.0, so O column D accumulates l_round.
+    // Needs 2 * (128 + D + 16) <= 512 TMEM columns; used for bf16, d = 64.
+    static constexpr bool kOnes = !kF16 && D == 64;
+    static constexpr uint32_t kOnesOffset = (2 + kStages) * kTileBytes;
+    static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
+    static constexpr uint32_t kON = D + (kOnes ? 16 : 0);  // O accumulator columns
     static constexpr uint32_t kColO0 = 256;
-    static constexpr uint32_t kColO1 = 256 + D;
+    static constexpr uint32_t kColO1 = 256 + kON;
 };
 
 struct Bars {
@@ -357,14 +367,17 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32
 // halves of d = 128 is one 16 KB box (LBO; with d = 64 there is one half and
 // the value is irrelevant, so it is kept inside the tile).  P is read from
 // tensor memory, 8 columns (16 keys of bf16 pairs) per K = 16 step.
+// With the ones column (Cfg::kOnes, d = 64) N = 80: the MMA's second atom
+// along N is the constant ones atom, so LBO is its distance from this stage.
 template <int D, bool kF16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_smem,
-                                         bool accumulate)
+                                         uint32_t ones_smem, bool accumulate)
 {
-    constexpr uint32_t idesc = idesc_f32acc(kBM, D, true, kF16);
+    using C = Cfg<D, kF16>;
+    constexpr uint32_t idesc = idesc_f32acc(kBM, C::kON, true, kF16);
     constexpr uint32_t kVLbo = D > 64 ? kChunkBytes : 1024;
     constexpr uint32_t hi = smem_desc_hi(1024);
-    const uint32_t b_lo = smem_desc_lo(v_smem, kVLbo);
+    const uint32_t b_lo = smem_desc_lo(v_smem, C::kOnes ? ones_smem - v_smem : kVLbo);
     const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
@@ -375,7 +388,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint3
 template <int D, bool kF16>
 __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t tmem)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kF16>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
     uint32_t q_phase[2] = {0, 0}, p_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
@@ -446,7 +459,8 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
                 const uint32_t col_s = t == 0 ? 0u : 128u;
                 const uint32_t col_o = t == 0 ? C::kColO0 : C::kColO1;
                 if (leader)
-                    issue_pv<D, kF16>(tmem + col_o, tmem + col_s, kv_smem(at_v), j - 1 > 0);
+                    issue_pv<D, kF16>(tmem + col_o, tmem + col_s, kv_smem(at_v),
+                                      smem_base + C::kOnesOffset, j - 1 > 0);
                 if (j < u.n[t]) {
                     if (leader)
                         issue_s<D, kF16>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
@@ -476,7 +490,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
 template <int D, bool kF16>
 __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kF16>;
     const volatile int *abort = &b.abort;
     const int warp = (threadIdx.x / 32) & 3;
     const int lane = threadIdx.x & 31;
@@ -564,7 +578,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                     const float p0 = ex2(x0), p1 = ex2(x1);
                     pk[i] = pack2<kF16>(p0, p1);
                     sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
-                    if constexpr (!kF16)
+                    if constexpr (!kF16 && !C::kOnes)
                         sum_round[i & 1] =
                             f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
                                                              __uint_as_float(pk[i] & 0xffff0000u)));
@@ -577,7 +591,8 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             f2_unpack(sum_round[0], r0, r1);
             f2_unpack(sum_round[1], r2, r3);
             l = l * alpha + ((e0 + e1) + (e2 + e3));
-            l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
+            if constexpr (!C::kOnes)
+                l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
             if (!first && __any_sync(0xffffffffu, m_new != m)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -588,6 +603,15 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                     for (int i = 0; i < 32; ++i)
                         o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                     tmem_st32(t_o + c * 32, o);
+                }
+                if constexpr (C::kOnes) {  // the l_round column and its 15 zero neighbours
+                    uint32_t o[16];
+                    tmem_ld16(t_o + D, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st16(t_o + D, o);
                 }
             }
             m = m_new;
@@ -608,8 +632,12 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             break;
         tc_fence_after();
         // fp16 P is rounded 8x more finely than bf16 P: O is normalised by
-        // the exact sum there.
+        // the exact sum there.  With the ones column l_round is O column D.
         // l is 0 only for a split that saw no key of this row.
+        if constexpr (C::kOnes) {
+            l_round = __uint_as_float(tmem_ld1(t_o + D));
+            tmem_wait_ld();
+        }
         const float l_norm = kF16 ? l : l_round;
         const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
         const bool live = row < p.Nq;
@@ -674,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const Params p)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kF16>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t smem_base = (raw + 1023u) & ~1023u;
@@ -706,6 +734,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             b.sk_hi = sk_lo(p.W, p.grid, blockIdx.x + 1);
         }
         fence_barrier_init();
+    }
+    if constexpr (C::kOnes) {
+        // The ones atom: 128 key rows of 128 bytes in the 128-byte swizzle
+        // (16-byte chunk c of row k stored at chunk c ^ (k % 8)); column 0
+        // (chunk 0, first element) is 1.0, everything else 0.
+        uint32_t *ones = reinterpret_cast<uint32_t *>(smem_raw + (smem_base - raw) + C::kOnesOffset);
+        for (int w = threadIdx.x; w < static_cast<int>(kChunkBytes / 4); w += blockDim.x) {
+            const int k = w / 32, wr = w % 32;
+            ones[w] = wr == (k % 8) * 4 ? 0x3F80u : 0u;  // bf16 1.0 in the low half
+        }
+        fence_proxy_async_smem();
     }
     if (warp == kWarpMma) {
         tmem_alloc(smem_addr(&b.tmem_base), kTmemCols);
@@ -848,7 +887,7 @@ template <int D, bool kF16>
 cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split, int num_sms,
                    cudaStream_t stream)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, kF16>;
     Params p;
     p.o = a.o;
     p.lse = a.lse;
