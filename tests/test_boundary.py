@@ -74,7 +74,7 @@ def test_empty_problems_are_noops(lib):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(B=-1), INVALID), (dict(H=-1), INVALID), (dict(N=-5), INVALID),
-    (dict(d=80), UNSUPPORTED), (dict(d=0), UNSUPPORTED), (dict(d=256), UNSUPPORTED),
+    (dict(d=80), UNSUPPORTED), (dict(d=0), UNSUPPORTED), (dict(d=512), UNSUPPORTED),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(causal=2), INVALID), (dict(causal=-1), INVALID),

@@ -95,7 +95,7 @@ fattn_status_t check_shape(int B, int H, int N, int d, float scale, int causal, 
         return FATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale))
         return FATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 96 && d != 128)
+    if (d != 64 && d != 96 && d != 128 && d != 256)
         return FATTN_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(B) * H * N;
     *empty = rows == 0;
@@ -324,7 +324,7 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
     a.Nk = Nk;
     cudaError_t e;
     if (which == Kernel::kSimt) {
-        if (Nk != N || L != nullptr)
+        if (Nk != N || L != nullptr || d > 128)
             return FATTN_ERR_UNSUPPORTED;
         e = fattn::launch_fwd_simt(a, stream);
     } else {
@@ -387,9 +387,11 @@ size_t split_ws_bytes(int B, int H, int N, int d, int splits)
 // measured on one and four splits of 16 pairs x 32 key tiles, d = 64).  Ties
 // go to the smaller s.
 constexpr long long kUnitCost = 3, kMergeCost = 6;
-int choose_splits(int B, int H, int Nq, int Nk, int num_sms)
+int choose_splits(int B, int H, int Nq, int Nk, int d, int num_sms)
 {
-    const long long pairs = ((static_cast<long long>(Nq) + 127) / 128 + 1) / 2;
+    // A work unit is a pair of 128-row Q tiles, or one Q tile for d = 256.
+    const long long q_tiles = (static_cast<long long>(Nq) + 127) / 128;
+    const long long pairs = d == 256 ? q_tiles : (q_tiles + 1) / 2;
     const long long units = static_cast<long long>(B) * H * pairs;
     const long long key_tiles = (static_cast<long long>(Nk) + 127) / 128;
     if (units <= 0 || units >= num_sms)
@@ -410,11 +412,11 @@ int choose_splits(int B, int H, int Nq, int Nk, int num_sms)
 // The automatic schedule of attn_fwd_kv: stream-K for one Q-tile pair per
 // head when whole heads would leave SMs idle, else choose_splits.  Returns
 // the partial slots per head (1: no split).
-int auto_slots(int B, int H, int Nq, int Nk, int causal, int num_sms, int *streamk)
+int auto_slots(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int *streamk)
 {
     const fattn::FwdPlan plan = fattn::plan_fwd_streamk(B, H, Nq, Nk, causal, num_sms);
     *streamk = plan.streamk;
-    return plan.streamk ? plan.slots : choose_splits(B, H, Nq, Nk, num_sms);
+    return plan.streamk ? plan.slots : choose_splits(B, H, Nq, Nk, d, num_sms);
 }
 
 // num_splits == 0: the automatic schedule for the current device.
@@ -435,7 +437,7 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
         return s;
     int streamk = 0;
     if (num_splits == 0)
-        num_splits = auto_slots(B, H, N, Nk, causal, info.num_sms, &streamk);
+        num_splits = auto_slots(B, H, N, Nk, d, causal, info.num_sms, &streamk);
     if (num_splits == 1)
         return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal,
                       stream, fattn::FwdSplit{1, nullptr, nullptr}, L);
@@ -515,7 +517,7 @@ int attn_fwd_split_count(int B, int H, int N, int d, int causal)
     DeviceInfo info;
     if (current_device(&dev, &info) != FATTN_OK)
         return 0;
-    return choose_splits(B, H, N, N, info.num_sms);
+    return choose_splits(B, H, N, N, d, info.num_sms);
 }
 
 size_t attn_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits)
@@ -582,7 +584,7 @@ size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causa
         DeviceInfo info;
         if (current_device(&dev, &info) != FATTN_OK)
             return 0;
-        num_splits = auto_slots(B, H, Nq, Nk, causal, info.num_sms, &streamk);
+        num_splits = auto_slots(B, H, Nq, Nk, d, causal, info.num_sms, &streamk);
     }
     return split_ws_bytes(B, H, Nq, d, num_splits);
 }
@@ -624,7 +626,7 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
 size_t attn_bwd_workspace_size(int B, int H, int N, int d)
 {
     bool empty = false;
-    if (d == 96 || check_shape(B, H, N, d, 1.0f, 0, &empty) != FATTN_OK || empty)
+    if ((d != 64 && d != 128) || check_shape(B, H, N, d, 1.0f, 0, &empty) != FATTN_OK || empty)
         return 0;
     return static_cast<size_t>(B) * H * N * sizeof(float);
 }
@@ -638,7 +640,7 @@ fattn_status_t attn_bwd(const void *q, const void *k, const void *v, const void 
     fattn_status_t s = check_shape(B, H, N, d, scale, causal, &empty);
     if (s != FATTN_OK || empty)
         return s;
-    if (d == 96)  // the backward kernels take d = 64 or 128
+    if (d != 64 && d != 128)  // the backward kernels take d = 64 or 128
         return FATTN_ERR_UNSUPPORTED;
     const size_t rows = static_cast<size_t>(B) * H * N;
     const size_t tb = rows * d * 2, lb = rows * 4;

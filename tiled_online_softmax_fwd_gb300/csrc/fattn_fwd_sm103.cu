@@ -83,12 +83,15 @@ struct Cfg {
     // S product stops at K = 96, the P V product has N = 96).
     static constexpr int kChunks = (D + 63) / 64;
     static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
-    static constexpr int kStages = kChunks == 2 ? 4 : 8;  // K/V ring depth
+    // d = 256 runs one Q tile per CTA (fwd_single_kernel): a 64 KB Q tile and
+    // two 64 KB K/V stages.  Otherwise two Q tiles and a deeper ring.
+    static constexpr int kQTiles = D == 256 ? 1 : 2;
+    static constexpr int kStages = kChunks == 4 ? 2 : (kChunks == 2 ? 4 : 8);  // K/V ring
     // Ones column: P V runs with N = D + 16 against V extended by a constant
     // atom whose first column is 1.0, so O column D accumulates l_round.
     // Needs 2 * (128 + D + 16) <= 512 TMEM columns; used for bf16, d = 64.
     static constexpr bool kOnes = !kF16 && D == 64;
-    static constexpr uint32_t kOnesOffset = (2 + kStages) * kTileBytes;
+    static constexpr uint32_t kOnesOffset = (kQTiles + kStages) * kTileBytes;
     static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
     static constexpr uint32_t kON = D + (kOnes ? 16 : 0);  // O accumulator columns
     static constexpr uint32_t kColO0 = 256;
@@ -100,6 +103,7 @@ struct Bars {
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
     uint64_t drain;
+    uint64_t pv_done;  // single-tile kernel: completion of each P V
     uint32_t tmem_base;
     int abort;
     // Stream-K range of this CTA (see cta_unit): first head, its first key
@@ -129,6 +133,7 @@ struct Params {
                    // stream-K: partial slots per head
     int units;     // BH * pairs * splits
     int causal;
+    int single;    // 1: a work unit has one Q tile (d = 256), "pairs" counts Q tiles
     int streamk;   // 1: one Q-tile pair per head, key tiles dealt evenly over CTAs
     int grid;      // CTAs of the launch (stream-K ranges)
     int F;         // key tiles of the pair (stream-K)
@@ -163,6 +168,19 @@ __device__ __forceinline__ int key_tiles(const Params &p, int qt)
     return key_tiles(p.QT, p.KT, p.extra, p.causal, qt);
 }
 
+// Q tile t of a unit (pair index, or Q tile index in single-tile mode, where
+// the second tile is absent: index QT has no key tiles).
+__device__ __forceinline__ int unit_tile(const Params &p, int pair, int t)
+{
+    return p.single ? (t == 0 ? pair : p.QT) : 2 * pair + t;
+}
+
+// Key tiles of a unit: the max over its Q tiles.
+__device__ __forceinline__ int unit_tiles(const Params &p, int pair)
+{
+    return max(key_tiles(p, unit_tile(p, pair, 0)), key_tiles(p, unit_tile(p, pair, 1)));
+}
+
 // Tile t of the pair works on key tiles [j0, min(je, its own count)).
 __device__ __forceinline__ Unit make_unit(const Params &p, int bh, int split, int pair, int j0,
                                           int je)
@@ -173,7 +191,7 @@ __device__ __forceinline__ Unit make_unit(const Params &p, int bh, int split, in
     u.j0 = j0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        u.qt[t] = 2 * pair + t;
+        u.qt[t] = unit_tile(p, pair, t);
         u.j1[t] = min(je, key_tiles(p, u.qt[t]));
         u.n[t] = max(u.j1[t] - u.j0, 0);
     }
@@ -188,7 +206,7 @@ __device__ __forceinline__ Unit unit_at(const Params &p, int k)
     const int split = k % p.splits;
     const int rest = k / p.splits;
     const int pair = p.pairs - 1 - rest / p.BH;  // heaviest pairs first
-    const int fmax = max(key_tiles(p, 2 * pair), key_tiles(p, 2 * pair + 1));
+    const int fmax = unit_tiles(p, pair);
     return make_unit(p, rest % p.BH, split, pair, split * fmax / p.splits,
                      (split + 1) * fmax / p.splits);
 }
@@ -487,6 +505,177 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
 }
 
 // ------------------------------------------------------------------ softmax
+// One key tile of one row (thread r of the tile's warpgroup), on the S row at
+// TMEM address t_s: mask, row max, p = 2^(s*scale*log2e - m), P (16-bit)
+// written over the first 64 columns of S, and the row sums.  Returns the
+// rescale factor alpha of O and l for the new running max m_new.
+template <int D, bool kF16, bool kOnes>
+__device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int r, int j,
+                                              int first_vis, bool first, float m, float &m_new,
+                                              float &l, float &l_round)
+{
+    // The whole S row: four 32-column loads in flight, one wait.
+    uint32_t sraw[kBN / 32][32];
+#pragma unroll
+    for (int c = 0; c < kBN / 32; ++c)
+        tmem_ld32(t_s + c * 32, sraw[c]);
+    tmem_wait_ld();
+    float s[kBN];
+#pragma unroll
+    for (int i = 0; i < kBN; ++i)
+        s[i] = __uint_as_float(sraw[i / 32][i % 32]);
+    // Mask (only on tiles that cross the diagonal and on the ragged last
+    // tile; the branch is uniform across the warp): keys past row position +
+    // off and keys past Nk get -inf, i.e. weight exactly 0.  first_vis is
+    // the last visible column of row 0 in this key tile.
+    const bool diag = p.causal && first_vis < kBN - 1;
+    const bool tail = (j + 1) * kBN > p.Nk;
+    if (diag || tail) {
+        int limit = diag ? first_vis + r : kBN - 1;
+        if (tail)
+            limit = min(limit, p.Nk - 1 - j * kBN);
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+            s[i] = i > limit ? -INFINITY : s[i];
+    }
+    // Row max: four independent chains of 3-input max.
+    float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+    for (int i = 4; i < kBN; i += 8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
+    }
+    const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
+    m_new = (first || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
+    const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
+    // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row sums:
+    // of the fp32 p (for lse) and of the bf16-rounded p that P V actually
+    // uses (to normalise O; formed by the tensor cores instead with kOnes).
+    const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
+    const uint64_t negm = f2_pack(-m_new, -m_new);
+    // Two independent packed accumulators per sum (four partials).
+    uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+    uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+    for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm), x0,
+                      x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            pk[i] = pack2<kF16>(p0, p1);
+            sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
+            if constexpr (!kF16 && !kOnes)
+                sum_round[i & 1] =
+                    f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
+                                                     __uint_as_float(pk[i] & 0xffff0000u)));
+        }
+        tmem_st16(t_s + c * 16, pk);
+    }
+    float e0, e1, e2, e3, r0, r1, r2, r3;
+    f2_unpack(sum_exact[0], e0, e1);
+    f2_unpack(sum_exact[1], e2, e3);
+    f2_unpack(sum_round[0], r0, r1);
+    f2_unpack(sum_round[1], r2, r3);
+    l = l * alpha + ((e0 + e1) + (e2 + e3));
+    if constexpr (!kOnes)
+        l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
+    return alpha;
+}
+
+// O row (and with kOnes the l_round column) times alpha, in TMEM.
+template <int D, bool kOnes>
+__device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
+{
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(t_o + c * 32, o);
+    }
+    if constexpr (kOnes) {  // the l_round column and its 15 zero neighbours
+        uint32_t o[16];
+        tmem_ld16(t_o + D, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st16(t_o + D, o);
+    }
+}
+
+// Epilogue of one row after the unit's last P V: O / l_round in bf16 (fp16)
+// and lse = ln2 * (m + log2 l); in split mode the fp32 partial O and the two
+// base-2 partial lse go to the workspace instead, for the combine kernel.
+template <int D, bool kF16, bool kOnes>
+__device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uint32_t t_o, int row,
+                                             float m, float l, float l_round)
+{
+    // fp16 P is rounded 8x more finely than bf16 P: O is normalised by the
+    // exact sum there.  With the ones column l_round is O column D.  l is 0
+    // only for a split that saw no key of this row.
+    if constexpr (kOnes) {
+        l_round = __uint_as_float(tmem_ld1(t_o + D));
+        tmem_wait_ld();
+    }
+    const float l_norm = kF16 ? l : l_round;
+    const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
+    const bool live = row < p.Nq;
+    const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
+    if (p.splits == 1) {
+        uint16_t *orow = static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb +
+                         (u.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            __syncwarp();
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack2<kF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (live) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+        if (live)
+            p.lse[grow] = (m + log2f(l)) * kLn2;
+    } else {
+        const size_t srow = static_cast<size_t>(u.split) * p.BH * p.Nq + grow;
+        float *orow = p.ws_o + srow * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            __syncwarp();
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+            if (live) {
+                float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l,
+                                         __uint_as_float(o[4 * i + 1]) * inv_l,
+                                         __uint_as_float(o[4 * i + 2]) * inv_l,
+                                         __uint_as_float(o[4 * i + 3]) * inv_l);
+            }
+        }
+        if (live)
+            p.ws_l[srow] = make_float2(m + log2f(l), m + log2f(l_norm));
+    }
+}
+
 template <int D, bool kF16>
 __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 {
@@ -524,96 +713,11 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                 break;
             tc_fence_after();
             __syncwarp();
-            // The whole S row: four 32-column loads in flight, one wait.
-            uint32_t sraw[kBN / 32][32];
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c)
-                tmem_ld32(t_s + c * 32, sraw[c]);
-            tmem_wait_ld();
-            float s[kBN];
-#pragma unroll
-            for (int i = 0; i < kBN; ++i)
-                s[i] = __uint_as_float(sraw[i / 32][i % 32]);
-            // Mask (only on tiles that cross the diagonal and on the ragged
-            // last tile; the branch is uniform across the warp): keys past
-            // row position + off and keys past Nk get -inf, i.e. weight
-            // exactly 0.
-            const bool diag = p.causal && first_vis < kBN - 1;
-            const bool tail = (j + 1) * kBN > p.Nk;
-            if (diag || tail) {
-                int limit = diag ? first_vis + r : kBN - 1;
-                if (tail)
-                    limit = min(limit, p.Nk - 1 - j * kBN);
-#pragma unroll
-                for (int i = 0; i < kBN; ++i)
-                    s[i] = i > limit ? -INFINITY : s[i];
-            }
-            // Row max: four independent chains of 3-input max.
-            float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-            for (int i = 4; i < kBN; i += 8) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
-            }
-            const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
-            const float m_new = (first || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
-            const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
-            // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row
-            // sums: of the fp32 p (for lse) and of the bf16-rounded p that
-            // P V actually uses (to normalise O).
-            const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
-            const uint64_t negm = f2_pack(-m_new, -m_new);
-            // Two independent packed accumulators per sum (four partials).
-            uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-            uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm),
-                              x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    pk[i] = pack2<kF16>(p0, p1);
-                    sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
-                    if constexpr (!kF16 && !C::kOnes)
-                        sum_round[i & 1] =
-                            f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                             __uint_as_float(pk[i] & 0xffff0000u)));
-                }
-                tmem_st16(t_s + c * 16, pk);
-            }
-            float e0, e1, e2, e3, r0, r1, r2, r3;
-            f2_unpack(sum_exact[0], e0, e1);
-            f2_unpack(sum_exact[1], e2, e3);
-            f2_unpack(sum_round[0], r0, r1);
-            f2_unpack(sum_round[1], r2, r3);
-            l = l * alpha + ((e0 + e1) + (e2 + e3));
-            if constexpr (!C::kOnes)
-                l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
-            if (!first && __any_sync(0xffffffffu, m_new != m)) {
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(t_o + c * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(t_o + c * 32, o);
-                }
-                if constexpr (C::kOnes) {  // the l_round column and its 15 zero neighbours
-                    uint32_t o[16];
-                    tmem_ld16(t_o + D, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st16(t_o + D, o);
-                }
-            }
+            float m_new;
+            const float alpha =
+                softmax_tile<D, kF16, C::kOnes>(p, t_s, r, j, first_vis, first, m, m_new, l, l_round);
+            if (!first && __any_sync(0xffffffffu, m_new != m))
+                rescale_o<D, C::kOnes>(t_o, alpha);
             m = m_new;
             tmem_wait_st();
             tc_fence_before();
@@ -623,70 +727,12 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         }
         if (!ok)
             break;
-        // Epilogue: O / l_round in bf16 and lse = ln2 * (m + log2 l); in
-        // split mode the fp32 partial O and the two base-2 partial lse go to
-        // the workspace instead, for the combine kernel.
         ok = mbar_wait(smem_addr(&b.o_full[t]), of_phase, kWaitLimitNs, abort);
         of_phase ^= 1;
         if (!ok)
             break;
         tc_fence_after();
-        // fp16 P is rounded 8x more finely than bf16 P: O is normalised by
-        // the exact sum there.  With the ones column l_round is O column D.
-        // l is 0 only for a split that saw no key of this row.
-        if constexpr (C::kOnes) {
-            l_round = __uint_as_float(tmem_ld1(t_o + D));
-            tmem_wait_ld();
-        }
-        const float l_norm = kF16 ? l : l_round;
-        const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
-        const bool live = row < p.Nq;
-        const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
-        if (p.splits == 1) {
-            uint16_t *orow = static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb +
-                             (u.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                __syncwarp();
-                tmem_ld32(t_o + c * 32, o);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<kF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                        __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (live) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-            }
-            if (live)
-                p.lse[grow] = (m + log2f(l)) * kLn2;
-        } else {
-            const size_t srow = static_cast<size_t>(u.split) * p.BH * p.Nq + grow;
-            float *orow = p.ws_o + srow * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                __syncwarp();
-                tmem_ld32(t_o + c * 32, o);
-                tmem_wait_ld();
-                if (live) {
-                    float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l,
-                                             __uint_as_float(o[4 * i + 1]) * inv_l,
-                                             __uint_as_float(o[4 * i + 2]) * inv_l,
-                                             __uint_as_float(o[4 * i + 3]) * inv_l);
-                }
-            }
-            if (live)
-                p.ws_l[srow] = make_float2(m + log2f(l), m + log2f(l_round));
-        }
+        epilogue_row<D, kF16, C::kOnes>(p, u, t_o, row, m, l, l_round);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -697,6 +743,20 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 }
 
 // ------------------------------------------------------------------ kernel
+// The ones atom (Cfg::kOnes): 128 key rows of 128 bytes in the 128-byte
+// swizzle (16-byte chunk c of row k stored at chunk c ^ (k % 8)); column 0
+// (chunk 0, first element) is bf16 1.0, everything else 0.  Written by all
+// threads before the CTA-wide barrier that precedes the first MMA.
+__device__ __forceinline__ void init_ones_atom(uint8_t *atom)
+{
+    uint32_t *ones = reinterpret_cast<uint32_t *>(atom);
+    for (int w = threadIdx.x; w < static_cast<int>(kChunkBytes / 4); w += blockDim.x) {
+        const int k = w / 32, wr = w % 32;
+        ones[w] = wr == (k % 8) * 4 ? 0x3F80u : 0u;  // bf16 1.0 in the low half
+    }
+    fence_proxy_async_smem();
+}
+
 template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -735,17 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_barrier_init();
     }
-    if constexpr (C::kOnes) {
-        // The ones atom: 128 key rows of 128 bytes in the 128-byte swizzle
-        // (16-byte chunk c of row k stored at chunk c ^ (k % 8)); column 0
-        // (chunk 0, first element) is 1.0, everything else 0.
-        uint32_t *ones = reinterpret_cast<uint32_t *>(smem_raw + (smem_base - raw) + C::kOnesOffset);
-        for (int w = threadIdx.x; w < static_cast<int>(kChunkBytes / 4); w += blockDim.x) {
-            const int k = w / 32, wr = w % 32;
-            ones[w] = wr == (k % 8) * 4 ? 0x3F80u : 0u;  // bf16 1.0 in the low half
-        }
-        fence_proxy_async_smem();
-    }
+    if constexpr (C::kOnes)
+        init_ones_atom(smem_raw + (smem_base - raw) + C::kOnesOffset);
     if (warp == kWarpMma) {
         tmem_alloc(smem_addr(&b.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -772,6 +823,317 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ single tile
+// d = 256: a 128-row Q tile and its 256-column O accumulator leave TMEM room
+// for one Q tile per CTA, so the overlap comes from two S buffers instead of
+// two Q tiles: S(j+1) is computed into the other buffer while the softmax
+// works on S(j), and the tensor cores run P V(j) and S(j+2) once P(j) is
+// written.  TMEM: S buffers at columns 0 and 128, O at 256..511.  Roles: warps
+// 0-3 softmax (thread r owns row r), warp 4 TMA, warp 5 MMA.  K/V ring of two
+// 64 KB stages, filled in the order the MMAs consume it: K0, K1, then V(i)
+// and K(i+2) alternately.
+constexpr int kSingleThreads = 192;
+constexpr int kSingleWarpLoad = 4;
+constexpr int kSingleWarpMma = 5;
+
+template <int D>
+__device__ void run_load_single(const Params &p, Bars &b, uint32_t smem_base,
+                                const CUtensorMap *mq, const CUtensorMap *mk,
+                                const CUtensorMap *mv)
+{
+    using C = Cfg<D>;
+    const volatile int *abort = &b.abort;
+    const bool leader = elect_one();
+    uint32_t q_phase = 0, pos = 0;
+    int last_q_parity = -1;
+    bool ok = true;
+    auto load_tile = [&](const CUtensorMap *m, int row, int hh, int bb) {
+        const uint32_t stage = pos % C::kStages;
+        ok = warp_wait(smem_addr(&b.kv_empty[stage]), ((pos / C::kStages) & 1) ^ 1, abort);
+        if (ok && leader) {
+            const uint32_t full = smem_addr(&b.kv_full[stage]);
+            mbar_arrive_expect_tx(full, C::kTileBytes);
+            const uint32_t dst = smem_base + (C::kQTiles + stage) * C::kTileBytes;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(dst + c * kChunkBytes, m, full, 64 * c, row, hh, bb);
+        }
+        pos += ok ? 1 : 0;
+    };
+    for (int r = 0; ok; ++r) {
+        Unit u;
+        if (!cta_unit(p, b, r, u))
+            break;
+        const int n = u.n[0];
+        if (n == 0)
+            continue;
+        const int hh = u.bh % p.H, bb = u.bh / p.H;
+        if (!warp_wait(smem_addr(&b.q_empty[0]), q_phase ^ 1, abort)) {
+            ok = false;
+            break;
+        }
+        if (leader) {
+            const uint32_t full = smem_addr(&b.q_full[0]);
+            mbar_arrive_expect_tx(full, C::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(smem_base + c * kChunkBytes, mq, full, 64 * c, u.qt[0] * kBM, hh, bb);
+        }
+        last_q_parity = q_phase;
+        q_phase ^= 1;
+        load_tile(mk, u.j0 * kBN, hh, bb);
+        if (ok && n > 1)
+            load_tile(mk, (u.j0 + 1) * kBN, hh, bb);
+        for (int i = 0; ok && i < n; ++i) {
+            load_tile(mv, (u.j0 + i) * kBN, hh, bb);
+            if (ok && i + 2 < n)
+                load_tile(mk, (u.j0 + i + 2) * kBN, hh, bb);
+        }
+    }
+    if (!ok) {
+        if (leader)
+            record_failure(b, kRoleLoad);
+        // Let the copies already issued land before the CTA exits.
+        const uint32_t first = pos > (uint32_t)C::kStages ? pos - C::kStages : 0;
+        for (uint32_t q = first; q < pos; ++q)
+            mbar_wait(smem_addr(&b.kv_full[q % C::kStages]), (q / C::kStages) & 1,
+                      kWaitLimitNs / 8, nullptr);
+        if (last_q_parity >= 0)
+            mbar_wait(smem_addr(&b.q_full[0]), last_q_parity, kWaitLimitNs / 8, nullptr);
+    }
+}
+
+template <int D, bool kF16>
+__device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uint32_t tmem)
+{
+    using C = Cfg<D, kF16>;
+    const volatile int *abort = &b.abort;
+    const bool leader = elect_one();
+    uint32_t q_phase = 0, oe_phase = 0, p_phase[2] = {0, 0}, pos = 0;
+    bool ok = true;
+    auto commit = [&](uint64_t &bar) {
+        if (leader)
+            mma_commit(smem_addr(&bar));
+    };
+    // Waits for the next ring position; returns its shared-memory address.
+    auto next_tile = [&](uint32_t &addr) {
+        const uint32_t stage = pos % C::kStages;
+        ok = warp_wait(smem_addr(&b.kv_full[stage]), (pos / C::kStages) & 1, abort);
+        addr = smem_base + (C::kQTiles + stage) * C::kTileBytes;
+        return stage;
+    };
+    for (int r = 0; ok; ++r) {
+        Unit u;
+        if (!cta_unit(p, b, r, u))
+            break;
+        const int n = u.n[0];
+        if (n == 0)
+            continue;
+        ok = warp_wait(smem_addr(&b.q_full[0]), q_phase, abort);
+        q_phase ^= 1;
+        if (!ok)
+            break;
+        // S(0) and S(1) into the two buffers.
+        for (int i = 0; i < 2 && i < n && ok; ++i) {
+            uint32_t k_addr;
+            const uint32_t stage = next_tile(k_addr);
+            if (!ok)
+                break;
+            tc_fence_after();
+            if (leader)
+                issue_s<D, kF16>(tmem + i * 128u, smem_base, k_addr);
+            commit(b.s_full[i]);
+            commit(b.kv_empty[stage]);
+            ++pos;
+            if (i == n - 1)
+                commit(b.q_empty[0]);
+        }
+        for (int i = 0; i < n && ok; ++i) {
+            const int buf = i & 1;
+            ok = warp_wait(smem_addr(&b.p_full[buf]), p_phase[buf], abort);
+            p_phase[buf] ^= 1;
+            if (ok && i == 0) {  // the first P V of the unit overwrites O
+                ok = warp_wait(smem_addr(&b.o_empty[0]), oe_phase ^ 1, abort);
+                oe_phase ^= 1;
+            }
+            uint32_t v_addr = 0, stage = 0;
+            if (ok)
+                stage = next_tile(v_addr);
+            if (!ok)
+                break;
+            tc_fence_after();
+            if (leader)
+                issue_pv<D, kF16>(tmem + C::kColO0, tmem + buf * 128u, v_addr,
+                                  smem_base + C::kOnesOffset, i > 0);
+            commit(b.pv_done);
+            commit(b.kv_empty[stage]);
+            ++pos;
+            if (i + 2 < n) {  // S(i+2) into the buffer P V(i) has just read
+                uint32_t k_addr;
+                const uint32_t ks = next_tile(k_addr);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                if (leader)
+                    issue_s<D, kF16>(tmem + buf * 128u, smem_base, k_addr);
+                commit(b.s_full[buf]);
+                commit(b.kv_empty[ks]);
+                ++pos;
+                if (i + 2 == n - 1)
+                    commit(b.q_empty[0]);
+            }
+        }
+        if (ok)
+            commit(b.o_full[0]);
+    }
+    if (!ok && leader)
+        record_failure(b, kRoleMma);
+    // Wait until every MMA this warp issued has completed.
+    commit(b.drain);
+    mbar_wait(smem_addr(&b.drain), 0, kWaitLimitNs, nullptr);
+}
+
+template <int D, bool kF16>
+__device__ void run_softmax_single(const Params &p, Bars &b, uint32_t tmem)
+{
+    using C = Cfg<D, kF16>;
+    const volatile int *abort = &b.abort;
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int r = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_o = tmem + lane_off + C::kColO0;
+    uint32_t s_phase[2] = {0, 0}, of_phase = 0, pv_count = 0;
+    bool ok = true;
+
+    for (int rr = 0; ok; ++rr) {
+        Unit u;
+        if (!cta_unit(p, b, rr, u))
+            break;
+        if (u.n[0] == 0)
+            continue;
+        const int qt = u.qt[0];
+        const int row = qt * kBM + r;
+        float m = -FLT_MAX, l = 0.f, l_round = 0.f;  // -FLT_MAX: see run_softmax
+        int first_vis = qt * kBM + p.off - u.j0 * kBN;
+        for (int j = u.j0; j < u.j1[0]; ++j, first_vis -= kBN) {
+            const bool first = j == u.j0;
+            const int buf = (j - u.j0) & 1;
+            ok = mbar_wait(smem_addr(&b.s_full[buf]), s_phase[buf], kWaitLimitNs, abort);
+            s_phase[buf] ^= 1;
+            if (!ok)
+                break;
+            tc_fence_after();
+            __syncwarp();
+            float m_new;
+            const float alpha = softmax_tile<D, kF16, C::kOnes>(p, tmem + lane_off + buf * 128u, r,
+                                                                j, first_vis, first, m, m_new, l,
+                                                                l_round);
+            if (!first && __any_sync(0xffffffffu, m_new != m)) {
+                // O may still be receiving P V of the previous key tile: wait
+                // for that product (the pv_count-th P V of this CTA) first.
+                ok = mbar_wait(smem_addr(&b.pv_done), (pv_count - 1) & 1, kWaitLimitNs, abort);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                rescale_o<D, C::kOnes>(t_o, alpha);
+            }
+            m = m_new;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&b.p_full[buf]));
+            ++pv_count;
+        }
+        if (!ok)
+            break;
+        ok = mbar_wait(smem_addr(&b.o_full[0]), of_phase, kWaitLimitNs, abort);
+        of_phase ^= 1;
+        if (!ok)
+            break;
+        tc_fence_after();
+        epilogue_row<D, kF16, C::kOnes>(p, u, t_o, row, m, l, l_round);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&b.o_empty[0]));
+    }
+    if (!ok)
+        record_failure(b, kRoleSoftmax);
+}
+
+template <int D, bool kF16>
+__global__ void __launch_bounds__(kSingleThreads, 1)
+    fwd_single_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                      const __grid_constant__ CUtensorMap mv, const Params p)
+{
+    using C = Cfg<D, kF16>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t smem_base = (raw + 1023u) & ~1023u;
+    Bars &b = *reinterpret_cast<Bars *>(smem_raw + (smem_base - raw) + C::kTilesBytes);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_addr(&b.q_full[t]), 1);
+            mbar_init(smem_addr(&b.q_empty[t]), 1);
+            mbar_init(smem_addr(&b.s_full[t]), 1);
+            mbar_init(smem_addr(&b.p_full[t]), 4);
+            mbar_init(smem_addr(&b.o_full[t]), 1);
+            mbar_init(smem_addr(&b.o_empty[t]), 4);
+        }
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_addr(&b.kv_full[s]), 1);
+            mbar_init(smem_addr(&b.kv_empty[s]), 1);
+        }
+        mbar_init(smem_addr(&b.drain), 1);
+        mbar_init(smem_addr(&b.pv_done), 1);
+        b.abort = 0;
+        if (p.streamk) {
+            const long long lo = sk_lo(p.W, p.grid, blockIdx.x);
+            const long long h0 = lo / p.F;
+            b.sk_h0 = static_cast<int>(h0);
+            b.sk_j0 = static_cast<int>(lo - h0 * p.F);
+            b.sk_slot0 = static_cast<int>(blockIdx.x) - sk_cta(p.W, p.grid, h0 * p.F);
+            b.sk_hi = sk_lo(p.W, p.grid, blockIdx.x + 1);
+        }
+        fence_barrier_init();
+    }
+    if constexpr (C::kOnes)
+        init_ones_atom(smem_raw + (smem_base - raw) + C::kOnesOffset);
+    if (warp == kSingleWarpMma) {
+        tmem_alloc(smem_addr(&b.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kSingleWarpLoad && lane == 0) {
+        prefetch_tensormap(&mq);
+        prefetch_tensormap(&mk);
+        prefetch_tensormap(&mv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = b.tmem_base;
+
+    if (warp < 4)
+        run_softmax_single<D, kF16>(p, b, tmem);
+    else if (warp == kSingleWarpLoad)
+        run_load_single<D>(p, b, smem_base, &mq, &mk, &mv);
+    else if (warp == kSingleWarpMma)
+        run_mma_single<D, kF16>(p, b, smem_base, tmem);
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kSingleWarpMma) {
         __syncwarp();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -822,9 +1184,8 @@ __global__ void __launch_bounds__(256)
     const int lane = threadIdx.x & 31;
     const int bh = static_cast<int>(row / p.Nq);
     const int i = static_cast<int>(row % p.Nq);
-    const int qt = i / kBM, pair = qt / 2;
-    const int full0 = key_tiles(p, 2 * pair), full1 = key_tiles(p, 2 * pair + 1);
-    const int fmax = max(full0, full1), fown = (qt & 1) ? full1 : full0;
+    const int qt = i / kBM, pair = p.single ? qt : qt / 2;
+    const int fmax = unit_tiles(p, pair), fown = key_tiles(p, qt);
     // Online merge over the slots, kBatch at a time: all loads of a batch are
     // issued before any of them is used.  A slot whose range held no key of
     // this row (l = 0, partial lse -inf) contributes nothing.
@@ -905,7 +1266,8 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     p.o_sb = dense_o ? static_cast<long long>(a.H) * a.N * D : a.o_sb;
     p.QT = (a.N + kBM - 1) / kBM;
     p.KT = (a.Nk + kBN - 1) / kBN;
-    p.pairs = (p.QT + 1) / 2;
+    p.single = D == 256 ? 1 : 0;
+    p.pairs = p.single ? p.QT : (p.QT + 1) / 2;
     p.splits = split.splits < 1 ? 1 : split.splits;
     p.causal = a.causal;
     p.streamk = split.streamk;
@@ -925,14 +1287,23 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     p.units = static_cast<int>(min(units, 0x7fffffffLL));
     p.sl2 = a.scale * kLog2e;
     const size_t smem = C::kTilesBytes + sizeof(Bars) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e;
+    if constexpr (D == 256)
+        e = cudaFuncSetAttribute(fwd_single_kernel<D, kF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+    else
+        e = cudaFuncSetAttribute(fwd_kernel<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
     p.grid = grid;
-    fwd_kernel<D, kF16><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
+    if constexpr (D == 256)
+        fwd_single_kernel<D, kF16><<<grid, kSingleThreads, smem, stream>>>(maps.q, maps.k,
+                                                                          maps.v, p);
+    else
+        fwd_kernel<D, kF16><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
         return e;
     const long long rows = static_cast<long long>(p.BH) * p.Nq;
@@ -985,6 +1356,9 @@ cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, const FwdSpl
     case 128:
         return a.f16 ? launch<128, true>(a, maps, split, num_sms, stream)
                      : launch<128, false>(a, maps, split, num_sms, stream);
+    case 256:
+        return a.f16 ? launch<256, true>(a, maps, split, num_sms, stream)
+                     : launch<256, false>(a, maps, split, num_sms, stream);
     }
     return cudaErrorInvalidValue;
 }

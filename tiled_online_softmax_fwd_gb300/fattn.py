@@ -140,8 +140,8 @@ def _validate(q, k, v, dtype=torch.bfloat16):
         raise ValueError("q, k, v shapes differ: %s %s %s" % (q.shape, k.shape, v.shape))
     if not (q.device == k.device == v.device):
         raise ValueError("q, k, v are on different devices")
-    if q.shape[-1] not in (64, 96, 128):
-        raise ValueError("head dimension must be 64, 96 or 128, got %d" % q.shape[-1])
+    if q.shape[-1] not in (64, 96, 128, 256):
+        raise ValueError("head dimension must be 64, 96, 128 or 256, got %d" % q.shape[-1])
 
 
 def _forward(entry: str, q, k, v, causal, scale, out, lse, stream):

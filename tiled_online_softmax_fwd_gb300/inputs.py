@@ -71,10 +71,13 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
-# A head dimension outside the five: d = 96, causal, the shape of the third.
+# Head dimensions outside the five: d = 96 in the shape of the third, and
+# d = 256 (one Q tile per CTA) at 8K tokens.
 VARIANT_WORKLOADS = {
     "B4_H16_N4096_d96_causal": Workload("B4_H16_N4096_d96_causal", 4, 16, 4096, 96, True, 5,
                                         rows_per_head=256),
+    "B2_H16_N8192_d256_causal": Workload("B2_H16_N8192_d256_causal", 2, 16, 8192, 256, True, 6,
+                                         rows_per_head=128),
 }
 
 
