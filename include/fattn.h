@@ -221,6 +221,8 @@ size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causa
  * (checked by nesting: its strides sorted by size, each at least the span
  * of the smaller dimensions) and o must not overlap q, k, v or lse (checked
  * over each tensor's address span).  lse stays contiguous fp32 [B][H][Nq].
+ * dtype: 0 = bf16 q, k, v, o; 1 = fp16 (as attn_fwd_fp16: P rounded to fp16,
+ * O normalised by the fp32 sum); anything else gives FATTN_ERR_INVALID_ARG.
  * Everything else -- shapes, the causal alignment, num_splits, the workspace
  * (attn_fwd_kv_workspace_size) and the errors -- is attn_fwd_kv's.  A
  * stride array that is NULL gives FATTN_ERR_INVALID_ARG.
@@ -230,7 +232,7 @@ fattn_status_t attn_fwd_strided(const void *q, const void *k, const void *v, voi
                                 const long long *q_strides, const long long *k_strides,
                                 const long long *v_strides, const long long *o_strides,
                                 float scale, int causal, int num_splits, void *workspace,
-                                size_t workspace_bytes, struct CUstream_st *stream);
+                                size_t workspace_bytes, int dtype, struct CUstream_st *stream);
 fattn_status_t attn_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
                            int B, int H, int Nq, int Nk, int d, float scale, int causal,
                            int num_splits, void *workspace, size_t workspace_bytes,

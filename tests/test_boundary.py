@@ -190,9 +190,10 @@ def test_strided_arguments_are_checked(lib):
     B, H, N, d = 2, 3, 40, 64
     dense = L3(H * N * d, N * d, d)
 
-    def call(qs=dense, ks=dense, vs=dense, os_=dense, p=ptrs, causal=0):
-        return f(*p, B, H, N, N, d, qs, ks, vs, os_, 0.125, causal, 1, None, 0, None)
+    def call(qs=dense, ks=dense, vs=dense, os_=dense, p=ptrs, causal=0, dtype=0):
+        return f(*p, B, H, N, N, d, qs, ks, vs, os_, 0.125, causal, 1, None, 0, dtype, None)
     assert call(qs=None) == INVALID
+    assert call(dtype=2) == INVALID
     assert call(os_=L3(H * N * d, N * d, d + 4)) == INVALID       # not a multiple of 8
     assert call(ks=L3(H * N * d, 0, d)) == INVALID                # zero stride, extent 3
     assert call(os_=L3(H * N * d, N * d, 32)) == INVALID          # o rows overlap (32 < d)

@@ -102,3 +102,21 @@ def test_head_major_batch_minor_layout():
     r = compare(o.contiguous().cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref,
                 mean_rule="floor")
     assert_parity(r, "head-major")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_fp16_strided_kv_and_splits(d):
+    """fp16 through the general entry: packed q/k/v views, decode-shaped
+    queries against a longer key sequence, the automatic schedule."""
+    B, H, Nq, Nk = 1, 3, 100, 3000
+    q, k, v = make_qkv_kv(B, H, Nq, Nk, d, seed=d, dtype=torch.float16)
+    kv = torch.empty((B, Nk, 2, H, d), dtype=torch.float16, device="cuda")
+    kv[:, :, 0] = k.permute(0, 2, 1, 3).cuda()
+    kv[:, :, 1] = v.permute(0, 2, 1, 3).cuda()
+    dk, dv = kv[:, :, 0].permute(0, 2, 1, 3), kv[:, :, 1].permute(0, 2, 1, 3)
+    o, lse = fattn.attn_fwd_strided(q.cuda(), dk, dv, causal=True)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd_kv(q, k, v, fattn.default_scale(d), True)
+    r = compare(o.float().cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref,
+                mean_rule="floor")
+    assert_parity(r, "fp16 strided d%d" % d)

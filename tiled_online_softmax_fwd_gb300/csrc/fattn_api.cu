@@ -424,7 +424,8 @@ int auto_slots(int B, int H, int Nq, int Nk, int d, int causal, int num_sms, int
 fattn_status_t forward_split(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int H, int N, int Nk, int d, float scale, int causal,
                              int num_splits, void *workspace, size_t workspace_bytes,
-                             cudaStream_t stream, const Layout *L = nullptr)
+                             cudaStream_t stream, const Layout *L = nullptr,
+                             Kernel which = Kernel::kTcgen05)
 {
     if (num_splits < 0 || num_splits > kMaxSplits)
         return FATTN_ERR_INVALID_ARG;
@@ -439,8 +440,8 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
     if (num_splits == 0)
         num_splits = auto_slots(B, H, N, Nk, d, causal, info.num_sms, &streamk);
     if (num_splits == 1)
-        return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal,
-                      stream, fattn::FwdSplit{1, nullptr, nullptr}, L);
+        return launch(which, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream,
+                      fattn::FwdSplit{1, nullptr, nullptr}, L);
     const size_t need = split_ws_bytes(B, H, N, d, num_splits);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return FATTN_ERR_INVALID_ARG;
@@ -459,8 +460,7 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
         num_splits, reinterpret_cast<float *>(ws),
         reinterpret_cast<float *>(ws + align_up(split_ws_o_bytes(B, H, N, d, num_splits), kWsAlign)),
         streamk};
-    return launch(Kernel::kTcgen05, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream,
-                  split, L);
+    return launch(which, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream, split, L);
 }
 
 // ---------------------------------------------------------------- no-allocation split
@@ -544,9 +544,9 @@ fattn_status_t attn_fwd_strided(const void *q, const void *k, const void *v, voi
                                 const long long *q_strides, const long long *k_strides,
                                 const long long *v_strides, const long long *o_strides,
                                 float scale, int causal, int num_splits, void *workspace,
-                                size_t workspace_bytes, struct CUstream_st *stream)
+                                size_t workspace_bytes, int dtype, struct CUstream_st *stream)
 {
-    if (!q_strides || !k_strides || !v_strides || !o_strides)
+    if (!q_strides || !k_strides || !v_strides || !o_strides || (dtype != 0 && dtype != 1))
         return FATTN_ERR_INVALID_ARG;
     Layout L;
     for (int i = 0; i < 3; ++i) {
@@ -568,7 +568,8 @@ fattn_status_t attn_fwd_strided(const void *q, const void *k, const void *v, voi
             all[t][0] = all[t][1] * (H > 0 ? H : 1);
     }
     return forward_split(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, workspace,
-                         workspace_bytes, stream, &L);
+                         workspace_bytes, stream, &L,
+                         dtype == 1 ? Kernel::kTcgen05F16 : Kernel::kTcgen05);
 }
 
 size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal,

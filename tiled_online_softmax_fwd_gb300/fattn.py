@@ -80,7 +80,7 @@ def load():
         i64p = ctypes.POINTER(ctypes.c_longlong)
         lib.attn_fwd_strided.restype = ctypes.c_int
         lib.attn_fwd_strided.argtypes = [vp] * 5 + [ip] * 5 + [i64p] * 4 + [
-            fp, ip, ip, vp, ctypes.c_size_t, vp]
+            fp, ip, ip, vp, ctypes.c_size_t, ip, vp]
         lib.attn_fwd_kv_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_kv_workspace_size.argtypes = [ip] * 7
         lib.attn_bwd.restype = ctypes.c_int
@@ -270,15 +270,16 @@ def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None,
 
 def attn_fwd_strided(q, k, v, causal: bool = False, scale: float | None = None,
                      num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
-    """attn_fwd_kv on 4-D bf16 views [B, H, Nq|Nk, d] with any strides whose last
-    dimension is contiguous (libfattn attn_fwd_strided): e.g. q, k, v sliced
-    from one packed projection output.  ``out`` may be a strided view too;
-    by default a contiguous one is allocated."""
+    """attn_fwd_kv on 4-D bf16 or fp16 views [B, H, Nq|Nk, d] with any
+    strides whose last dimension is contiguous (libfattn attn_fwd_strided):
+    e.g. q, k, v sliced from one packed projection output.  ``out`` may be a
+    strided view too; by default a contiguous one is allocated."""
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 \
-                or t.dim() != 4 or t.stride(3) != 1:
-            raise ValueError("%s must be a 4-D bf16 CUDA tensor with a contiguous last "
-                             "dimension" % name)
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 \
+                or t.dtype not in (torch.bfloat16, torch.float16) or t.stride(3) != 1 \
+                or t.dtype != q.dtype:
+            raise ValueError("%s must be a 4-D bf16 or fp16 CUDA tensor (all of one type) with "
+                             "a contiguous last dimension" % name)
     if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
         raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] do not match: %s %s %s"
                          % (q.shape, k.shape, v.shape))
@@ -289,7 +290,8 @@ def attn_fwd_strided(q, k, v, causal: bool = False, scale: float | None = None,
     if out is None:
         out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
     if out.shape != q.shape or out.dtype != q.dtype or out.stride(3) != 1:
-        raise ValueError("out must be a bf16 [B, H, Nq, d] view with a contiguous last dimension")
+        raise ValueError("out must be a [B, H, Nq, d] view of q's type with a contiguous last "
+                         "dimension")
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
 
@@ -304,6 +306,7 @@ def attn_fwd_strided(q, k, v, causal: bool = False, scale: float | None = None,
                                      strides(v), strides(out), float(scale),
                                      1 if causal else 0, int(num_splits),
                                      workspace.data_ptr() if need > 0 else 0, workspace.numel(),
+                                     1 if q.dtype == torch.float16 else 0,
                                      _stream_handle(stream, q.device))
     _check(st, "attn_fwd_strided")
     return out, lse
