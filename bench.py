@@ -602,9 +602,11 @@ def run_gpu(args, world, rank, local):
     if step_ms is not None:
         # Steps timed one by one (L2 flushed before each): quantiles of the
         # step time and the achieved bandwidth of the algorithmic bytes.
-        q = lambda f: step_ms[min(len(step_ms) - 1, int(f * len(step_ms)))]
-        line["step_quantiles_ms"] = {"p20": q(0.2), "p50": q(0.5), "p80": q(0.8)}
-        line["algorithmic_gbs_p50"] = w.io_bytes / (q(0.5) * 1e-3) / 1e9
+        def quantile(f):
+            return step_ms[min(len(step_ms) - 1, int(f * len(step_ms)))]
+        line["step_quantiles_ms"] = {"p20": quantile(0.2), "p50": quantile(0.5),
+                                     "p80": quantile(0.8)}
+        line["algorithmic_gbs_p50"] = w.io_bytes / (quantile(0.5) * 1e-3) / 1e9
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
