@@ -592,8 +592,9 @@ def run_gpu(args, world, rank, local):
                      "algorithmic_flops_per_launch": w.flops,
                      "algorithmic_bytes_per_launch": w.io_bytes},
         "gpu_launches": args.steps * (2 if splits > 1 else 1),
-        "kernel": "fattn fwd_kernel<%d> (tcgen05/TMA, persistent)%s" % (
-            w.d, " + combine_kernel, %d key-range splits; roofline.achieved uses the whole step" % splits
+        "kernel": "fattn %s<%d> (tcgen05/TMA, persistent)%s" % (
+            "fwd_single_kernel" if w.d == 256 else "fwd_kernel", w.d,
+            " + combine_kernel, %d key-range splits; roofline.achieved uses the whole step" % splits
             if splits > 1 else ""),
         "wall_ms_per_step": wall_ms,
         "clocks": clocks.summary(),
