@@ -818,6 +818,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
         run_mma<D, kF16>(p, b, smem_base, tmem);
     }
+    // The merge kernel of a split call (launched with programmatic stream
+    // serialisation) may be scheduled now; it still waits for this grid to
+    // finish before it reads the partials.
+    grid_launch_dependents();
 
     tc_fence_before();
     __syncthreads();
@@ -1129,6 +1133,7 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
         run_load_single<D>(p, b, smem_base, &mq, &mk, &mv);
     else if (warp == kSingleWarpMma)
         run_mma_single<D, kF16>(p, b, smem_base, tmem);
+    grid_launch_dependents();  // see fwd_kernel
 
     tc_fence_before();
     __syncthreads();
@@ -1186,10 +1191,13 @@ __global__ void __launch_bounds__(256)
     const int i = static_cast<int>(row % p.Nq);
     const int qt = i / kBM, pair = p.single ? qt : qt / 2;
     const int fmax = unit_tiles(p, pair), fown = key_tiles(p, qt);
+    // Launched as a programmatic dependent of the forward grid: wait for it
+    // to finish (and its partials to be visible) before reading them.
+    grid_dependency_wait();
     // Online merge over the slots, kBatch at a time: all loads of a batch are
     // issued before any of them is used.  A slot whose range held no key of
     // this row (l = 0, partial lse -inf) contributes nothing.
-    constexpr int kBatch = 4;
+    constexpr int kBatch = 8;
     float mx_e = -INFINITY, mx_r = -INFINITY, se = 0.f, sr = 0.f;
     float acc[kCols];
 #pragma unroll
@@ -1310,8 +1318,20 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
-    combine_kernel<D, kF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p.ws_o, p.ws_l, p);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the merge grid is set up while the
+    // forward grid drains and waits for it in griddepcontrol.wait.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, kF16>, static_cast<const float *>(p.ws_o),
+                              static_cast<const float2 *>(p.ws_l), p);
 }
 
 }  // namespace

@@ -345,6 +345,20 @@ __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr)
     return r;
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start while the previous grid in the stream runs; it
+// waits here until that grid has completed and its memory is visible.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the dependent grid launch once every CTA of this grid has signalled
+// (or exited).
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem()
