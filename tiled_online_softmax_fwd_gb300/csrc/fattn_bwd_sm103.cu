@@ -25,6 +25,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "fattn_internal.h"
 #include "ptx_sm103.cuh"
 
@@ -50,7 +52,18 @@ struct BCfg {
     // smem: two resident tiles + 2 stages of two streamed tiles.
     static constexpr uint32_t kTilesBytes = 6 * kTileBytes;
     static constexpr uint32_t kColAcc1 = kColAcc0 + D;
+    // dq kernel: a second S buffer in the columns after the dQ accumulator,
+    // so that S of the next key tile is computed while the elementwise pass
+    // works on this one.
+    static constexpr uint32_t kColS1 = kColAcc0 + D;
 };
+
+// dq kernel: the S buffer of the i-th key tile of a unit.
+template <int D>
+__device__ __forceinline__ uint32_t dq_s_col(int i)
+{
+    return (i & 1) ? BCfg<D>::kColS1 : kColS;
+}
 
 struct BBars {
     uint64_t res_full, res_empty;  // the CTA's resident pair (K_j,V_j or Q_i,dO_i)
@@ -59,7 +72,7 @@ struct BBars {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    float lse2[2][kTile];  // dkdv: per query tile, lse * log2(e) and D
+    float lse2[2][kTile];  // dkdv: per query tile, -lse * log2(e) and -D
     float dd[2][kTile];
 };
 
@@ -236,6 +249,7 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
             mma_commit(smem_addr(&bar));
     };
     const uint32_t a0 = smem, a1 = smem + C::kTileBytes;  // resident pair
+    auto stage_smem = [&](uint32_t at) { return smem + (2 + 2 * (at & 1)) * C::kTileBytes; };
     for (int r = 0; ok; ++r) {
         const int k = deal(r, blockIdx.x, gridDim.x);
         if (k >= p.units)
@@ -250,36 +264,92 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
         oe_phase ^= 1;
         if (!ok)
             break;
-        for (int t = lo; ok && t < hi; ++t, ++pos) {
-            const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
-            ok = warp_wait(smem_addr(&b.st_full[stage]), phase, abort);
+        if constexpr (!kDkDv) {
+            // dq: S(t+1) goes into the other S buffer before P(t) is ready,
+            // and dP(t+1) follows as soon as the elementwise pass of t has
+            // read dP(t); dQ += dS(t) K_t comes after it.  With the ring of
+            // two stages, K/V of tiles t and t+1 are resident together.
+            // Position pos is tile lo; the stage of tile t is (pos+t-lo) & 1.
+            if (hi <= lo)
+                continue;
+            auto wait_stage = [&](int t) {
+                const uint32_t at = pos + (t - lo);
+                return warp_wait(smem_addr(&b.st_full[at & 1]), (at >> 1) & 1, abort);
+            };
+            ok = wait_stage(lo);
             if (!ok)
                 break;
             tc_fence_after();
-            const uint32_t b0 = smem + (2 + 2 * stage) * C::kTileBytes, b1 = b0 + C::kTileBytes;
             if (leader) {
-                mma_nt<D>(tmem + kColS, a0, b0);   // S^T = K Q^T  |  S = Q K^T
-                mma_nt<D>(tmem + kColDP, a1, b1);  // dP^T = V dO^T | dP = dO V^T
+                mma_nt<D>(tmem + dq_s_col<D>(0), a0, stage_smem(pos));            // S = Q K^T
+                mma_nt<D>(tmem + kColDP, a1, stage_smem(pos) + C::kTileBytes);  // dP = dO V^T
             }
             commit(b.s_full);
-            if (t == hi - 1)
-                commit(b.res_empty);  // resident pair no longer read
-            ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
-            s_phase ^= 1;
-            if (!ok)
-                break;
-            tc_fence_after();
-            if (leader) {
-                if (kDkDv) {
-                    mma_tn<D>(tmem + kColAcc0, tmem + kColS, b1, t > lo);          // dV += P^T dO
-                    mma_tn<D>(tmem + C::kColAcc1, tmem + kColDP, b0, t > lo);      // dK += dS^T Q
-                } else {
-                    mma_tn<D>(tmem + kColAcc0, tmem + kColS, b0, t > lo);          // dQ += dS K
+            if (lo == hi - 1)
+                commit(b.res_empty);
+            for (int t = lo; ok && t < hi; ++t) {
+                const uint32_t at = pos + (t - lo);
+                const bool next = t + 1 < hi;
+                if (next) {
+                    ok = wait_stage(t + 1);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    if (leader)
+                        mma_nt<D>(tmem + dq_s_col<D>(t + 1 - lo), a0, stage_smem(at + 1));
                 }
+                ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
+                s_phase ^= 1;
+                if (!ok)
+                    break;
+                tc_fence_after();
+                if (next) {
+                    if (leader)
+                        mma_nt<D>(tmem + kColDP, a1, stage_smem(at + 1) + C::kTileBytes);
+                    commit(b.s_full);
+                    if (t + 1 == hi - 1)
+                        commit(b.res_empty);  // resident pair no longer read
+                }
+                if (leader)
+                    mma_tn<D>(tmem + kColAcc0, tmem + dq_s_col<D>(t - lo), stage_smem(at),
+                              t > lo);  // dQ += dS K
+                commit(b.st_empty[at & 1]);
+                if (t == hi - 1)
+                    commit(b.o_full);
             }
-            commit(b.st_empty[stage]);
-            if (t == hi - 1)
-                commit(b.o_full);
+            pos += hi - lo;
+        } else {
+            for (int t = lo; ok && t < hi; ++t, ++pos) {
+                const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
+                ok = warp_wait(smem_addr(&b.st_full[stage]), phase, abort);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t b0 = smem + (2 + 2 * stage) * C::kTileBytes, b1 = b0 + C::kTileBytes;
+                if (leader) {
+                    mma_nt<D>(tmem + kColS, a0, b0);   // S^T = K Q^T  |  S = Q K^T
+                    mma_nt<D>(tmem + kColDP, a1, b1);  // dP^T = V dO^T | dP = dO V^T
+                }
+                commit(b.s_full);
+                if (t == hi - 1)
+                    commit(b.res_empty);  // resident pair no longer read
+                ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
+                s_phase ^= 1;
+                if (!ok)
+                    break;
+                tc_fence_after();
+                if (leader) {
+                    if (kDkDv) {
+                        mma_tn<D>(tmem + kColAcc0, tmem + kColS, b1, t > lo);          // dV += P^T dO
+                        mma_tn<D>(tmem + C::kColAcc1, tmem + kColDP, b0, t > lo);      // dK += dS^T Q
+                    } else {
+                        mma_tn<D>(tmem + kColAcc0, tmem + kColS, b0, t > lo);          // dQ += dS K
+                    }
+                }
+                commit(b.st_empty[stage]);
+                if (t == hi - 1)
+                    commit(b.o_full);
+            }
         }
     }
     if (!ok && leader)
@@ -320,8 +390,8 @@ __device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
                 // lse and D of the 128 queries of tile t, shared through smem
                 // (double-buffered; a 128-thread barrier publishes them).
                 const int qrow = t * kTile + r;
-                b.lse2[xbuf][r] = qrow < p.N ? p.lse[head + qrow] * kLog2e : 0.f;
-                b.dd[xbuf][r] = qrow < p.N ? p.dvec[head + qrow] : 0.f;
+                b.lse2[xbuf][r] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
+                b.dd[xbuf][r] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
             }
             ok = mbar_wait(smem_addr(&b.s_full), s_phase, kWaitLimitNs, abort);
@@ -342,37 +412,61 @@ __device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
                     c_hi = r;  // key t*128+c <= query own*128+r
             }
             c_hi = min(c_hi, p.N - 1 - col0);
-#pragma unroll 1
-            for (int ch = 0; ch < kTile / 32; ++ch) {
+            const uint32_t col_s = kDkDv ? kColS : dq_s_col<D>(t - lo);
+            // Element mask only on the diagonal tile and the ragged last one
+            // (the branch is uniform across the warp).
+            const bool masked = (p.causal && t == own) || col0 + kTile > p.N;
+            const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
+            const uint64_t row_nl2 = f2_pack(-my_lse2, -my_lse2), row_nd = f2_pack(-my_d, -my_d);
+            // One 32-column chunk: p = 2^(s*scale*log2e - lse*log2e) and
+            // dS = p (dP - D), two columns per packed instruction.
+            auto chunk = [&](int ch, auto masked_tag) {
+                constexpr bool kMasked = decltype(masked_tag)::value;
                 uint32_t sr[32], dr[32];
                 __syncwarp();
-                tmem_ld32(tmem + lane_off + kColS + ch * 32, sr);
+                tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
                 tmem_ld32(tmem + lane_off + kColDP + ch * 32, dr);
                 tmem_wait_ld();
                 uint32_t pk[16], dk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = ch * 32 + 2 * i + h;
-                        const float l2 = kDkDv ? b.lse2[xbuf][c] : my_lse2;
-                        const float dd = kDkDv ? b.dd[xbuf][c] : my_d;
-                        const bool valid = c >= c_lo && c <= c_hi;
-                        const float pe = valid ? ex2(fmaf(__uint_as_float(sr[2 * i + h]), p.sl2, -l2))
-                                               : 0.f;
-                        pv[h] = pe;
-                        dsv[h] = pe * (__uint_as_float(dr[2 * i + h]) - dd);
+                    const int c = ch * 32 + 2 * i;
+                    uint64_t nl2 = row_nl2, nd = row_nd;
+                    if (kDkDv) {
+                        nl2 = *reinterpret_cast<const uint64_t *>(&b.lse2[xbuf][c]);
+                        nd = *reinterpret_cast<const uint64_t *>(&b.dd[xbuf][c]);
                     }
-                    pk[i] = pack2(pv[0], pv[1]);
-                    dk[i] = pack2(dsv[0], dsv[1]);
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                     sl2x2, nl2),
+                              x0, x1);
+                    float p0 = ex2(x0), p1 = ex2(x1);
+                    if constexpr (kMasked) {
+                        p0 = (c >= c_lo && c <= c_hi) ? p0 : 0.f;
+                        p1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? p1 : 0.f;
+                    }
+                    const uint64_t pp = f2_pack(p0, p1);
+                    float d0, d1;
+                    f2_unpack(f2_mul(pp, f2_add(f2_pack(__uint_as_float(dr[2 * i]),
+                                                        __uint_as_float(dr[2 * i + 1])),
+                                                nd)),
+                              d0, d1);
+                    pk[i] = pack2(p0, p1);
+                    dk[i] = pack2(d0, d1);
                 }
                 if (kDkDv) {  // P^T over S, dS^T over dP
                     tmem_st16(tmem + lane_off + kColS + ch * 16, pk);
                     tmem_st16(tmem + lane_off + kColDP + ch * 16, dk);
                 } else {      // dS over S
-                    tmem_st16(tmem + lane_off + kColS + ch * 16, dk);
+                    tmem_st16(tmem + lane_off + col_s + ch * 16, dk);
                 }
+            };
+#pragma unroll 1
+            for (int ch = 0; ch < kTile / 32; ++ch) {
+                if (masked)
+                    chunk(ch, std::true_type{});
+                else
+                    chunk(ch, std::false_type{});
             }
             tmem_wait_st();
             tc_fence_before();
