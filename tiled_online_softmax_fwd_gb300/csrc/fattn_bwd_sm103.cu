@@ -69,6 +69,7 @@ struct BBars {
     uint64_t res_full, res_empty;  // the CTA's resident pair (K_j,V_j or Q_i,dO_i)
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full, p_full, o_full, o_empty;
+    uint64_t dp_free;  // dkdv: the elementwise pass has dP^T in registers
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -162,6 +163,25 @@ __device__ __forceinline__ void mma_tn(uint32_t tmem_d, uint32_t tmem_a, uint32_
                  kk > 0 ? 1u : acc0);
 }
 
+// Same product with A in the dK/dV kernel's interleaved TMEM layout: each
+// 32-column chunk of the S^T region holds 16 columns of P^T (part 0) then 16
+// of dS^T (part 16), i.e. K = 16 step kk of A sits at column
+// 32*(kk/2) + part + 8*(kk%2).
+template <int D>
+__device__ __forceinline__ void mma_tn_il(uint32_t tmem_d, uint32_t tmem_a, uint32_t part,
+                                          uint32_t b_smem, bool accumulate)
+{
+    constexpr uint32_t idesc = idesc_bf16_f32(kTile, D, true);
+    constexpr uint32_t lbo = D == 128 ? kChunkBytes : 1024;
+    constexpr uint32_t hi = smem_desc_hi(1024);
+    const uint32_t b_lo = smem_desc_lo(b_smem, lbo);
+    const uint32_t acc0 = accumulate ? 1u : 0u;
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ts_w(tmem_d, tmem_a + 32 * (kk >> 1) + part + 8 * (kk & 1),
+                 b_lo + ((kk * 16 * 128) >> 4), hi, idesc, kk > 0 ? 1u : acc0);
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -242,7 +262,7 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
     using C = BCfg<D>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
-    uint32_t res_phase = 0, s_phase = 0, oe_phase = 0, pos = 0;
+    uint32_t res_phase = 0, s_phase = 0, oe_phase = 0, dp_phase = 0, pos = 0;
     bool ok = true;
     auto commit = [&](uint64_t &bar) {
         if (leader)
@@ -319,37 +339,63 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
             }
             pos += hi - lo;
         } else {
-            for (int t = lo; ok && t < hi; ++t, ++pos) {
-                const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
-                ok = warp_wait(smem_addr(&b.st_full[stage]), phase, abort);
-                if (!ok)
-                    break;
-                tc_fence_after();
-                const uint32_t b0 = smem + (2 + 2 * stage) * C::kTileBytes, b1 = b0 + C::kTileBytes;
-                if (leader) {
-                    mma_nt<D>(tmem + kColS, a0, b0);   // S^T = K Q^T  |  S = Q K^T
-                    mma_nt<D>(tmem + kColDP, a1, b1);  // dP^T = V dO^T | dP = dO V^T
+            // dkdv: dP^T(t+1) is issued as soon as the elementwise pass holds
+            // dP^T(t) in registers; after P^T(t) and dS^T(t) (interleaved in
+            // the S^T columns) come dV += P^T dO and dK += dS^T Q, then
+            // S^T(t+1) over them.
+            if (hi <= lo)
+                continue;
+            auto wait_stage = [&](int t) {
+                const uint32_t at = pos + (t - lo);
+                return warp_wait(smem_addr(&b.st_full[at & 1]), (at >> 1) & 1, abort);
+            };
+            ok = wait_stage(lo);
+            if (!ok)
+                break;
+            tc_fence_after();
+            if (leader) {
+                mma_nt<D>(tmem + kColS, a0, stage_smem(pos));                   // S^T = K Q^T
+                mma_nt<D>(tmem + kColDP, a1, stage_smem(pos) + C::kTileBytes);  // dP^T = V dO^T
+            }
+            commit(b.s_full);
+            if (lo == hi - 1)
+                commit(b.res_empty);
+            for (int t = lo; ok && t < hi; ++t) {
+                const uint32_t at = pos + (t - lo);
+                const bool next = t + 1 < hi;
+                if (next) {
+                    ok = warp_wait(smem_addr(&b.dp_free), dp_phase, abort);
+                    dp_phase ^= 1;
+                    if (ok)
+                        ok = wait_stage(t + 1);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    if (leader)
+                        mma_nt<D>(tmem + kColDP, a1, stage_smem(at + 1) + C::kTileBytes);
                 }
-                commit(b.s_full);
-                if (t == hi - 1)
-                    commit(b.res_empty);  // resident pair no longer read
                 ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
                 s_phase ^= 1;
                 if (!ok)
                     break;
                 tc_fence_after();
                 if (leader) {
-                    if (kDkDv) {
-                        mma_tn<D>(tmem + kColAcc0, tmem + kColS, b1, t > lo);          // dV += P^T dO
-                        mma_tn<D>(tmem + C::kColAcc1, tmem + kColDP, b0, t > lo);      // dK += dS^T Q
-                    } else {
-                        mma_tn<D>(tmem + kColAcc0, tmem + kColS, b0, t > lo);          // dQ += dS K
-                    }
+                    const uint32_t q_t = stage_smem(at), do_t = q_t + C::kTileBytes;
+                    mma_tn_il<D>(tmem + kColAcc0, tmem + kColS, 0u, do_t, t > lo);      // dV += P^T dO
+                    mma_tn_il<D>(tmem + C::kColAcc1, tmem + kColS, 16u, q_t, t > lo);   // dK += dS^T Q
                 }
-                commit(b.st_empty[stage]);
+                commit(b.st_empty[at & 1]);
+                if (next) {
+                    if (leader)
+                        mma_nt<D>(tmem + kColS, a0, stage_smem(at + 1));  // S^T(t+1)
+                    commit(b.s_full);
+                    if (t + 1 == hi - 1)
+                        commit(b.res_empty);  // resident pair no longer read
+                }
                 if (t == hi - 1)
                     commit(b.o_full);
             }
+            pos += hi - lo;
         }
     }
     if (!ok && leader)
@@ -418,16 +464,12 @@ __device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
             const bool masked = (p.causal && t == own) || col0 + kTile > p.N;
             const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
             const uint64_t row_nl2 = f2_pack(-my_lse2, -my_lse2), row_nd = f2_pack(-my_d, -my_d);
-            // One 32-column chunk: p = 2^(s*scale*log2e - lse*log2e) and
-            // dS = p (dP - D), two columns per packed instruction.
-            auto chunk = [&](int ch, auto masked_tag) {
+            // 16 column pairs of one 32-column chunk: p = 2^(s*scale*log2e -
+            // lse*log2e) and dS = p (dP - D), two columns per packed
+            // instruction; returns P and dS packed to bf16 pairs.
+            auto pairs = [&](int ch, const uint32_t *sr, const uint32_t *dr, uint32_t *pk,
+                             uint32_t *dk, auto masked_tag) {
                 constexpr bool kMasked = decltype(masked_tag)::value;
-                uint32_t sr[32], dr[32];
-                __syncwarp();
-                tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
-                tmem_ld32(tmem + lane_off + kColDP + ch * 32, dr);
-                tmem_wait_ld();
-                uint32_t pk[16], dk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int c = ch * 32 + 2 * i;
@@ -454,19 +496,51 @@ __device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
                     pk[i] = pack2(p0, p1);
                     dk[i] = pack2(d0, d1);
                 }
-                if (kDkDv) {  // P^T over S, dS^T over dP
-                    tmem_st16(tmem + lane_off + kColS + ch * 16, pk);
-                    tmem_st16(tmem + lane_off + kColDP + ch * 16, dk);
-                } else {      // dS over S
-                    tmem_st16(tmem + lane_off + col_s + ch * 16, dk);
-                }
             };
+            if constexpr (kDkDv) {
+                // The whole dP^T row into registers first, so that the MMA
+                // warp can compute dP^T of the next query tile meanwhile.
+                uint32_t dr[kTile];
+#pragma unroll
+                for (int c = 0; c < kTile / 32; ++c)
+                    tmem_ld32(tmem + lane_off + kColDP + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&dr[c * 32]));
+                tmem_wait_ld();
+                if (t + 1 < hi) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_addr(&b.dp_free));
+                }
+                // P^T and dS^T of chunk ch go into that chunk's own S^T
+                // columns: 16 of P^T pairs, then 16 of dS^T pairs.
+#pragma unroll
+                for (int ch = 0; ch < kTile / 32; ++ch) {
+                    uint32_t sr[32], pk[16], dk[16];
+                    __syncwarp();
+                    tmem_ld32(tmem + lane_off + kColS + ch * 32, sr);
+                    tmem_wait_ld();
+                    if (masked)
+                        pairs(ch, sr, &dr[ch * 32], pk, dk, std::true_type{});
+                    else
+                        pairs(ch, sr, &dr[ch * 32], pk, dk, std::false_type{});
+                    tmem_st16(tmem + lane_off + kColS + ch * 32, pk);
+                    tmem_st16(tmem + lane_off + kColS + ch * 32 + 16, dk);
+                }
+            } else {
 #pragma unroll 1
-            for (int ch = 0; ch < kTile / 32; ++ch) {
-                if (masked)
-                    chunk(ch, std::true_type{});
-                else
-                    chunk(ch, std::false_type{});
+                for (int ch = 0; ch < kTile / 32; ++ch) {
+                    uint32_t sr[32], dr[32], pk[16], dk[16];
+                    __syncwarp();
+                    tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
+                    tmem_ld32(tmem + lane_off + kColDP + ch * 32, dr);
+                    tmem_wait_ld();
+                    if (masked)
+                        pairs(ch, sr, dr, pk, dk, std::true_type{});
+                    else
+                        pairs(ch, sr, dr, pk, dk, std::false_type{});
+                    tmem_st16(tmem + lane_off + col_s + ch * 16, dk);  // dS over S
+                }
             }
             tmem_wait_st();
             tc_fence_before();
@@ -540,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&b.p_full), 4);
         mbar_init(smem_addr(&b.o_full), 1);
         mbar_init(smem_addr(&b.o_empty), 4);
+        mbar_init(smem_addr(&b.dp_free), 4);
         mbar_init(smem_addr(&b.drain), 1);
         b.abort = 0;
         fence_barrier_init();
