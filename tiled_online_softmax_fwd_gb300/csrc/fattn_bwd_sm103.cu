@@ -45,12 +45,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kChunkBytes = kTile * 64 * 2;
 constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256;
 
-template <int D>
+template <int D, bool kDkDv = true>
 struct BCfg {
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;  // one [128][D] bf16 tile
-    // smem: two resident tiles + 2 stages of two streamed tiles.
-    static constexpr uint32_t kTilesBytes = 6 * kTileBytes;
+    // smem: two resident tiles, then
+    //   dK/dV: a ring of two stages, each a (Q, dO) pair;
+    //   dQ:    a ring of three K tiles and a separate ring of two V tiles
+    //          (V is released as soon as dP has read it, K only after dQ).
+    static constexpr int kKStages = 3, kVStages = 2;
+    static constexpr uint32_t kKRing = 2 * kTileBytes;
+    static constexpr uint32_t kVRing = kKRing + kKStages * kTileBytes;
+    static constexpr uint32_t kTilesBytes =
+        kDkDv ? 6 * kTileBytes : kVRing + kVStages * kTileBytes;
+    static constexpr uint32_t kBarsBytes = 256;  // BBars, rounded up
     static constexpr uint32_t kColAcc1 = kColAcc0 + D;
     // dq kernel: a second S buffer in the columns after the dQ accumulator,
     // so that S of the next key tile is computed while the elementwise pass
@@ -67,13 +75,21 @@ __device__ __forceinline__ uint32_t dq_s_col(int i)
 
 struct BBars {
     uint64_t res_full, res_empty;  // the CTA's resident pair (K_j,V_j or Q_i,dO_i)
-    uint64_t st_full[2], st_empty[2];
+    uint64_t st_full[3], st_empty[3];  // dK/dV: (Q, dO) stages; dQ: K stages
+    uint64_t v_full[2], v_empty[2];    // dQ: V stages
     uint64_t s_full, p_full, o_full, o_empty;
     uint64_t dp_free;  // dkdv: the elementwise pass has dP^T in registers
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    float lse2[2][kTile];  // dkdv: per query tile, -lse * log2(e) and -D
+};
+
+static_assert(sizeof(BBars) <= 256, "BBars outgrew its shared-memory slot");
+
+// dK/dV kernel only (after BBars): -lse * log2(e) and -D of the current query
+// tile's 128 rows, double-buffered.
+struct BXch {
+    float lse2[2][kTile];
     float dd[2][kTile];
 };
 
@@ -195,10 +211,10 @@ template <int D, bool kDkDv>
 __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtensorMap *ra0,
                          const CUtensorMap *ra1, const CUtensorMap *sb0, const CUtensorMap *sb1)
 {
-    using C = BCfg<D>;
+    using C = BCfg<D, kDkDv>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
-    uint32_t res_phase = 0, pos = 0;
+    uint32_t res_phase = 0, pos = 0, kpos = 0, vpos = 0;
     bool ok = true;
     int res_issued = 0;
     for (int r = 0; ok; ++r) {
@@ -224,21 +240,55 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
             }
         }
         ++res_issued;
-        for (int t = lo; ok && t < hi; ++t, ++pos) {
-            const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
-            if (!warp_wait(smem_addr(&b.st_empty[stage]), phase ^ 1, abort)) {
-                ok = false;
-                break;
-            }
-            if (leader) {
-                const uint32_t full = smem_addr(&b.st_full[stage]);
-                const uint32_t dst = smem + (2 + 2 * stage) * C::kTileBytes;
-                mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+        if constexpr (!kDkDv) {
+            // K(t) into the three-stage K ring, V(t) into the two-stage V ring.
+            for (int t = lo; ok && t < hi; ++t) {
+                const uint32_t ks = kpos % C::kKStages, kph = (kpos / C::kKStages) & 1;
+                const uint32_t vs = vpos % C::kVStages, vph = (vpos / C::kVStages) & 1;
+                if (!warp_wait(smem_addr(&b.st_empty[ks]), kph ^ 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    const uint32_t full = smem_addr(&b.st_full[ks]);
+                    const uint32_t dst = smem + C::kKRing + ks * C::kTileBytes;
+                    mbar_arrive_expect_tx(full, C::kTileBytes);
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(dst + c * kChunkBytes, sb0, full, 64 * c, t * kTile, bh);
-                    tma_load_3d(dst + C::kTileBytes + c * kChunkBytes, sb1, full, 64 * c, t * kTile,
-                                bh);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(dst + c * kChunkBytes, sb0, full, 64 * c, t * kTile, bh);
+                }
+                ++kpos;
+                if (!warp_wait(smem_addr(&b.v_empty[vs]), vph ^ 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    const uint32_t full = smem_addr(&b.v_full[vs]);
+                    const uint32_t dst = smem + C::kVRing + vs * C::kTileBytes;
+                    mbar_arrive_expect_tx(full, C::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(dst + c * kChunkBytes, sb1, full, 64 * c, t * kTile, bh);
+                }
+                ++vpos;
+            }
+        } else {
+            for (int t = lo; ok && t < hi; ++t, ++pos) {
+                const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
+                if (!warp_wait(smem_addr(&b.st_empty[stage]), phase ^ 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    const uint32_t full = smem_addr(&b.st_full[stage]);
+                    const uint32_t dst = smem + (2 + 2 * stage) * C::kTileBytes;
+                    mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(dst + c * kChunkBytes, sb0, full, 64 * c, t * kTile, bh);
+                        tma_load_3d(dst + C::kTileBytes + c * kChunkBytes, sb1, full, 64 * c,
+                                    t * kTile, bh);
+                    }
                 }
             }
         }
@@ -246,8 +296,16 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
     if (!ok) {
         if (leader)
             fail(p, b, kRoleLoad);
-        for (uint32_t q = pos > 2 ? pos - 2 : 0; q < pos; ++q)
-            mbar_wait(smem_addr(&b.st_full[q & 1]), (q >> 1) & 1, kWaitLimitNs / 8, nullptr);
+        // Let the copies already issued land before the CTA exits.
+        if constexpr (kDkDv) {
+            for (uint32_t q = pos > 2 ? pos - 2 : 0; q < pos; ++q)
+                mbar_wait(smem_addr(&b.st_full[q & 1]), (q >> 1) & 1, kWaitLimitNs / 8, nullptr);
+        } else {
+            for (uint32_t q = kpos > 3 ? kpos - 3 : 0; q < kpos; ++q)
+                mbar_wait(smem_addr(&b.st_full[q % 3]), (q / 3) & 1, kWaitLimitNs / 8, nullptr);
+            for (uint32_t q = vpos > 2 ? vpos - 2 : 0; q < vpos; ++q)
+                mbar_wait(smem_addr(&b.v_full[q & 1]), (q >> 1) & 1, kWaitLimitNs / 8, nullptr);
+        }
         if (res_issued > 0)
             mbar_wait(smem_addr(&b.res_full), res_phase ^ 1, kWaitLimitNs / 8, nullptr);
     }
@@ -259,7 +317,7 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
 template <int D, bool kDkDv>
 __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem)
 {
-    using C = BCfg<D>;
+    using C = BCfg<D, kDkDv>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
     uint32_t res_phase = 0, s_phase = 0, oe_phase = 0, dp_phase = 0, pos = 0;
@@ -287,53 +345,71 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
         if constexpr (!kDkDv) {
             // dq: S(t+1) goes into the other S buffer before P(t) is ready,
             // and dP(t+1) follows as soon as the elementwise pass of t has
-            // read dP(t); dQ += dS(t) K_t comes after it.  With the ring of
-            // two stages, K/V of tiles t and t+1 are resident together.
-            // Position pos is tile lo; the stage of tile t is (pos+t-lo) & 1.
+            // read dP(t); dQ += dS(t) K_t comes after it.  K(t) sits in the
+            // three-stage K ring until dQ(t), V(t) in the two-stage V ring
+            // until dP(t).  Position pos is tile lo in both rings.
             if (hi <= lo)
                 continue;
-            auto wait_stage = [&](int t) {
+            auto k_tile = [&](int t) {
                 const uint32_t at = pos + (t - lo);
-                return warp_wait(smem_addr(&b.st_full[at & 1]), (at >> 1) & 1, abort);
+                return smem + C::kKRing + (at % C::kKStages) * C::kTileBytes;
             };
-            ok = wait_stage(lo);
+            auto v_tile = [&](int t) {
+                const uint32_t at = pos + (t - lo);
+                return smem + C::kVRing + (at % C::kVStages) * C::kTileBytes;
+            };
+            auto wait_k = [&](int t) {
+                const uint32_t at = pos + (t - lo);
+                return warp_wait(smem_addr(&b.st_full[at % C::kKStages]), (at / C::kKStages) & 1,
+                                 abort);
+            };
+            auto wait_v = [&](int t) {
+                const uint32_t at = pos + (t - lo);
+                return warp_wait(smem_addr(&b.v_full[at % C::kVStages]), (at / C::kVStages) & 1,
+                                 abort);
+            };
+            auto release_v = [&](int t) { commit(b.v_empty[(pos + (t - lo)) % C::kVStages]); };
+            ok = wait_k(lo) && wait_v(lo);
             if (!ok)
                 break;
             tc_fence_after();
             if (leader) {
-                mma_nt<D>(tmem + dq_s_col<D>(0), a0, stage_smem(pos));            // S = Q K^T
-                mma_nt<D>(tmem + kColDP, a1, stage_smem(pos) + C::kTileBytes);  // dP = dO V^T
+                mma_nt<D>(tmem + dq_s_col<D>(0), a0, k_tile(lo));  // S = Q K^T
+                mma_nt<D>(tmem + kColDP, a1, v_tile(lo));          // dP = dO V^T
             }
             commit(b.s_full);
+            release_v(lo);
             if (lo == hi - 1)
                 commit(b.res_empty);
             for (int t = lo; ok && t < hi; ++t) {
-                const uint32_t at = pos + (t - lo);
                 const bool next = t + 1 < hi;
                 if (next) {
-                    ok = wait_stage(t + 1);
+                    ok = wait_k(t + 1);
                     if (!ok)
                         break;
                     tc_fence_after();
                     if (leader)
-                        mma_nt<D>(tmem + dq_s_col<D>(t + 1 - lo), a0, stage_smem(at + 1));
+                        mma_nt<D>(tmem + dq_s_col<D>(t + 1 - lo), a0, k_tile(t + 1));
                 }
                 ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
                 s_phase ^= 1;
+                if (ok && next)
+                    ok = wait_v(t + 1);
                 if (!ok)
                     break;
                 tc_fence_after();
                 if (next) {
                     if (leader)
-                        mma_nt<D>(tmem + kColDP, a1, stage_smem(at + 1) + C::kTileBytes);
+                        mma_nt<D>(tmem + kColDP, a1, v_tile(t + 1));
                     commit(b.s_full);
+                    release_v(t + 1);
                     if (t + 1 == hi - 1)
                         commit(b.res_empty);  // resident pair no longer read
                 }
                 if (leader)
-                    mma_tn<D>(tmem + kColAcc0, tmem + dq_s_col<D>(t - lo), stage_smem(at),
+                    mma_tn<D>(tmem + kColAcc0, tmem + dq_s_col<D>(t - lo), k_tile(t),
                               t > lo);  // dQ += dS K
-                commit(b.st_empty[at & 1]);
+                commit(b.st_empty[(pos + (t - lo)) % C::kKStages]);
                 if (t == hi - 1)
                     commit(b.o_full);
             }
@@ -407,7 +483,7 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
 // Elementwise warpgroup: thread r owns TMEM lane r = row `own*128 + r` of the
 // resident tile (a key in dkdv, a query in dq).
 template <int D, bool kDkDv>
-__device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
+__device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
 {
     using C = BCfg<D>;
     const volatile int *abort = &b.abort;
@@ -436,8 +512,8 @@ __device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
                 // lse and D of the 128 queries of tile t, shared through smem
                 // (double-buffered; a 128-thread barrier publishes them).
                 const int qrow = t * kTile + r;
-                b.lse2[xbuf][r] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
-                b.dd[xbuf][r] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
+                x.lse2[xbuf][r] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
+                x.dd[xbuf][r] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
             }
             ok = mbar_wait(smem_addr(&b.s_full), s_phase, kWaitLimitNs, abort);
@@ -475,8 +551,8 @@ __device__ void bwd_elem(const BParams &p, BBars &b, uint32_t tmem)
                     const int c = ch * 32 + 2 * i;
                     uint64_t nl2 = row_nl2, nd = row_nd;
                     if (kDkDv) {
-                        nl2 = *reinterpret_cast<const uint64_t *>(&b.lse2[xbuf][c]);
-                        nd = *reinterpret_cast<const uint64_t *>(&b.dd[xbuf][c]);
+                        nl2 = *reinterpret_cast<const uint64_t *>(&x.lse2[xbuf][c]);
+                        nd = *reinterpret_cast<const uint64_t *>(&x.dd[xbuf][c]);
                     }
                     float x0, x1;
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
@@ -597,18 +673,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap sb0, const __grid_constant__ CUtensorMap sb1,
                const BParams p)
 {
-    using C = BCfg<D>;
+    using C = BCfg<D, kDkDv>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t smem = (raw + 1023u) & ~1023u;
     BBars &b = *reinterpret_cast<BBars *>(smem_raw + (smem - raw) + C::kTilesBytes);
+    BXch &xch = *reinterpret_cast<BXch *>(smem_raw + (smem - raw) + C::kTilesBytes +
+                                          C::kBarsBytes);
     const int warp = threadIdx.x / 32;
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&b.res_full), 1);
         mbar_init(smem_addr(&b.res_empty), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < 3; ++s) {
             mbar_init(smem_addr(&b.st_full[s]), 1);
             mbar_init(smem_addr(&b.st_empty[s]), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_addr(&b.v_full[s]), 1);
+            mbar_init(smem_addr(&b.v_empty[s]), 1);
         }
         mbar_init(smem_addr(&b.s_full), 1);
         mbar_init(smem_addr(&b.p_full), 4);
@@ -628,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = b.tmem_base;
     if (warp < 4)
-        bwd_elem<D, kDkDv>(p, b, tmem);
+        bwd_elem<D, kDkDv>(p, b, xch, tmem);
     else if (warp == kWarpLoad)
         bwd_load<D, kDkDv>(p, b, smem, &ra0, &ra1, &sb0, &sb1);
     else
@@ -670,8 +752,8 @@ template <int D, bool kDkDv>
 cudaError_t launch_one(const CUtensorMap &ra0, const CUtensorMap &ra1, const CUtensorMap &sb0,
                        const CUtensorMap &sb1, const BParams &p, int num_sms, cudaStream_t stream)
 {
-    using C = BCfg<D>;
-    const size_t smem = C::kTilesBytes + sizeof(BBars) + 1024;
+    using C = BCfg<D, kDkDv>;
+    const size_t smem = C::kTilesBytes + C::kBarsBytes + (kDkDv ? sizeof(BXch) : 0) + 1024;
     cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kDkDv>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
