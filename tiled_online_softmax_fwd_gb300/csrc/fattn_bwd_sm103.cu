@@ -64,7 +64,19 @@ struct BCfg {
     // so that S of the next key tile is computed while the elementwise pass
     // works on this one.
     static constexpr uint32_t kColS1 = kColAcc0 + D;
+    // dK/dV kernel at d = 64: the two accumulators leave 128 columns, a
+    // second S^T buffer, so S^T of the next query tile is computed while the
+    // elementwise pass works on this one.
+    static constexpr bool kSDouble = kDkDv && D == 64;
+    static constexpr uint32_t kColS1DkDv = kColAcc0 + 2 * D;
 };
+
+// dK/dV kernel: the S^T buffer of the i-th query tile of a unit.
+template <int D>
+__device__ __forceinline__ uint32_t dkdv_s_col(int i)
+{
+    return (BCfg<D, true>::kSDouble && (i & 1)) ? BCfg<D, true>::kColS1DkDv : kColS;
+}
 
 // dq kernel: the S buffer of the i-th key tile of a unit.
 template <int D>
@@ -430,7 +442,7 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
                 break;
             tc_fence_after();
             if (leader) {
-                mma_nt<D>(tmem + kColS, a0, stage_smem(pos));                   // S^T = K Q^T
+                mma_nt<D>(tmem + dkdv_s_col<D>(0), a0, stage_smem(pos));        // S^T = K Q^T
                 mma_nt<D>(tmem + kColDP, a1, stage_smem(pos) + C::kTileBytes);  // dP^T = V dO^T
             }
             commit(b.s_full);
@@ -449,6 +461,13 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
                     tc_fence_after();
                     if (leader)
                         mma_nt<D>(tmem + kColDP, a1, stage_smem(at + 1) + C::kTileBytes);
+                    if constexpr (C::kSDouble) {  // S^T(t+1) into the other buffer
+                        if (leader)
+                            mma_nt<D>(tmem + dkdv_s_col<D>(t + 1 - lo), a0, stage_smem(at + 1));
+                        commit(b.s_full);
+                        if (t + 1 == hi - 1)
+                            commit(b.res_empty);
+                    }
                 }
                 ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
                 s_phase ^= 1;
@@ -457,11 +476,12 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
                 tc_fence_after();
                 if (leader) {
                     const uint32_t q_t = stage_smem(at), do_t = q_t + C::kTileBytes;
-                    mma_tn_il<D>(tmem + kColAcc0, tmem + kColS, 0u, do_t, t > lo);      // dV += P^T dO
-                    mma_tn_il<D>(tmem + C::kColAcc1, tmem + kColS, 16u, q_t, t > lo);   // dK += dS^T Q
+                    const uint32_t col = dkdv_s_col<D>(t - lo);
+                    mma_tn_il<D>(tmem + kColAcc0, tmem + col, 0u, do_t, t > lo);      // dV += P^T dO
+                    mma_tn_il<D>(tmem + C::kColAcc1, tmem + col, 16u, q_t, t > lo);   // dK += dS^T Q
                 }
                 commit(b.st_empty[at & 1]);
-                if (next) {
+                if (!C::kSDouble && next) {
                     if (leader)
                         mma_nt<D>(tmem + kColS, a0, stage_smem(at + 1));  // S^T(t+1)
                     commit(b.s_full);
@@ -534,7 +554,7 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                     c_hi = r;  // key t*128+c <= query own*128+r
             }
             c_hi = min(c_hi, p.N - 1 - col0);
-            const uint32_t col_s = kDkDv ? kColS : dq_s_col<D>(t - lo);
+            const uint32_t col_s = kDkDv ? dkdv_s_col<D>(t - lo) : dq_s_col<D>(t - lo);
             // Element mask only on the diagonal tile and the ragged last one
             // (the branch is uniform across the warp).
             const bool masked = (p.causal && t == own) || col0 + kTile > p.N;
@@ -594,14 +614,14 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                 for (int ch = 0; ch < kTile / 32; ++ch) {
                     uint32_t sr[32], pk[16], dk[16];
                     __syncwarp();
-                    tmem_ld32(tmem + lane_off + kColS + ch * 32, sr);
+                    tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
                     tmem_wait_ld();
                     if (masked)
                         pairs(ch, sr, &dr[ch * 32], pk, dk, std::true_type{});
                     else
                         pairs(ch, sr, &dr[ch * 32], pk, dk, std::false_type{});
-                    tmem_st16(tmem + lane_off + kColS + ch * 32, pk);
-                    tmem_st16(tmem + lane_off + kColS + ch * 32 + 16, dk);
+                    tmem_st16(tmem + lane_off + col_s + ch * 32, pk);
+                    tmem_st16(tmem + lane_off + col_s + ch * 32 + 16, dk);
                 }
             } else {
 #pragma unroll 1
