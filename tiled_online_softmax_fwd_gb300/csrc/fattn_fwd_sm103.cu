@@ -94,6 +94,10 @@ struct Cfg {
     static constexpr uint32_t kOnesOffset = (kQTiles + kStages) * kTileBytes;
     static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
     static constexpr uint32_t kON = D + (kOnes ? 16 : 0);  // O accumulator columns
+    // P V in two halves (keys 0-63 as soon as their P is written): faster at
+    // d = 64, where the softmax dominates (1101 -> 1148 TFLOP/s on B2 H8
+    // N65536), slower at d = 128 (1441 -> 1389 on the headline workload).
+    static constexpr bool kHalfP = D == 64;
     static constexpr uint32_t kColO0 = 256;
     static constexpr uint32_t kColO1 = 256 + kON;
 };
@@ -102,6 +106,7 @@ struct Bars {
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    uint64_t p_half[2];  // two-tile kernel: P of the first 64 keys written
     uint64_t drain;
     uint64_t pv_done;  // single-tile kernel: completion of each P V
     uint32_t tmem_base;
@@ -110,8 +115,6 @@ struct Bars {
     // tile and partial slot, and the end of the range.
     int sk_h0, sk_j0, sk_slot0;
     long long sk_hi;
-    float xmax[2][2 * kBM];  // row-half exchange (double-buffered): partial max / l_round
-    float xsum[2][2 * kBM];  // row-half exchange: partial l
 };
 
 struct Params {
@@ -387,7 +390,7 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32
 // tensor memory, 8 columns (16 keys of bf16 pairs) per K = 16 step.
 // With the ones column (Cfg::kOnes, d = 64) N = 80: the MMA's second atom
 // along N is the constant ones atom, so LBO is its distance from this stage.
-template <int D, bool kF16>
+template <int D, bool kF16, int kK0 = 0, int kK1 = kBN / 16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_smem,
                                          uint32_t ones_smem, bool accumulate)
 {
@@ -398,7 +401,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint3
     const uint32_t b_lo = smem_desc_lo(v_smem, C::kOnes ? ones_smem - v_smem : kVLbo);
     const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk)
+    for (int kk = kK0; kk < kK1; ++kk)
         mma_ts_w(tmem_d, tmem_p + kk * 8, b_lo + ((kk * 16 * 128) >> 4), hi, idesc,
                  kk > 0 ? 1u : acc0);
 }
@@ -409,7 +412,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
     using C = Cfg<D, kF16>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
-    uint32_t q_phase[2] = {0, 0}, p_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
+    uint32_t q_phase[2] = {0, 0}, p_phase[2] = {0, 0}, ph_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
     uint32_t pos = 0;
     bool ok = true;
 
@@ -465,8 +468,15 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
             for (int t = 0; t < 2 && ok; ++t) {
                 if (j - 1 >= u.n[t])
                     continue;  // tile t finished earlier (or is absent)
-                ok = warp_wait(smem_addr(&b.p_full[t]), p_phase[t], abort);
-                p_phase[t] ^= 1;
+                // With kHalfP, P V in two halves: keys 0-63 as soon as the
+                // softmax has written their P, keys 64-127 once all of P is.
+                if (C::kHalfP) {
+                    ok = warp_wait(smem_addr(&b.p_half[t]), ph_phase[t], abort);
+                    ph_phase[t] ^= 1;
+                } else {
+                    ok = warp_wait(smem_addr(&b.p_full[t]), p_phase[t], abort);
+                    p_phase[t] ^= 1;
+                }
                 if (ok && j - 1 == 0) {  // first P V of the unit overwrites O
                     ok = warp_wait(smem_addr(&b.o_empty[t]), oe_phase[t] ^ 1, abort);
                     oe_phase[t] ^= 1;
@@ -476,9 +486,23 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
                 tc_fence_after();
                 const uint32_t col_s = t == 0 ? 0u : 128u;
                 const uint32_t col_o = t == 0 ? C::kColO0 : C::kColO1;
-                if (leader)
+                if (C::kHalfP) {
+                    if (leader)
+                        issue_pv<D, kF16, 0, kBN / 32>(tmem + col_o, tmem + col_s, kv_smem(at_v),
+                                                       smem_base + C::kOnesOffset, j - 1 > 0);
+                    ok = warp_wait(smem_addr(&b.p_full[t]), p_phase[t], abort);
+                    p_phase[t] ^= 1;
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    if (leader)
+                        issue_pv<D, kF16, kBN / 32, kBN / 16>(tmem + col_o, tmem + col_s,
+                                                              kv_smem(at_v),
+                                                              smem_base + C::kOnesOffset, true);
+                } else if (leader) {
                     issue_pv<D, kF16>(tmem + col_o, tmem + col_s, kv_smem(at_v),
                                       smem_base + C::kOnesOffset, j - 1 > 0);
+                }
                 if (j < u.n[t]) {
                     if (leader)
                         issue_s<D, kF16>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
@@ -508,11 +532,19 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
 // One key tile of one row (thread r of the tile's warpgroup), on the S row at
 // TMEM address t_s: mask, row max, p = 2^(s*scale*log2e - m), P (16-bit)
 // written over the first 64 columns of S, and the row sums.  Returns the
-// rescale factor alpha of O and l for the new running max m_new.
-template <int D, bool kF16, bool kOnes>
+// rescale factor alpha of O and l for the new running max m_new.  pre(alpha)
+// runs once alpha is known, before any P is written; mid() runs when P of the
+// first 64 keys has been stored.
+struct NoHook {
+    __device__ __forceinline__ void operator()() const {}
+    __device__ __forceinline__ void operator()(float) const {}
+};
+
+template <int D, bool kF16, bool kOnes, class Pre = NoHook, class Mid = NoHook>
 __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int r, int j,
                                               int first_vis, bool first, float m, float &m_new,
-                                              float &l, float &l_round)
+                                              float &l, float &l_round, Pre pre = Pre(),
+                                              Mid mid = Mid())
 {
     // The whole S row: four 32-column loads in flight, one wait.
     uint32_t sraw[kBN / 32][32];
@@ -549,6 +581,7 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
     const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
     m_new = (first || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
     const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
+    pre(alpha);
     // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row sums:
     // of the fp32 p (for lse) and of the bf16-rounded p that P V actually
     // uses (to normalise O; formed by the tensor cores instead with kOnes).
@@ -574,6 +607,8 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
                                                      __uint_as_float(pk[i] & 0xffff0000u)));
         }
         tmem_st16(t_s + c * 16, pk);
+        if (c == kBN / 64 - 1)
+            mid();
     }
     float e0, e1, e2, e3, r0, r1, r2, r3;
     f2_unpack(sum_exact[0], e0, e1);
@@ -714,16 +749,46 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
             tc_fence_after();
             __syncwarp();
             float m_new;
-            const float alpha =
-                softmax_tile<D, kF16, C::kOnes>(p, t_s, r, j, first_vis, first, m, m_new, l, l_round);
-            if (!first && __any_sync(0xffffffffu, m_new != m))
-                rescale_o<D, C::kOnes>(t_o, alpha);
-            m = m_new;
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_addr(&b.p_full[t]));
+            if constexpr (C::kHalfP) {
+                // P of the first 64 keys goes to the tensor cores as soon as
+                // it is written, unless O has to be rescaled first (rare; the
+                // warp decides together): then both halves follow the rescale.
+                bool rescale = false;
+                auto pre = [&](float) { rescale = !first && __any_sync(0xffffffffu, m_new != m); };
+                auto mid = [&]() {
+                    if (!rescale) {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(smem_addr(&b.p_half[t]));
+                    }
+                };
+                const float alpha = softmax_tile<D, kF16, C::kOnes>(
+                    p, t_s, r, j, first_vis, first, m, m_new, l, l_round, pre, mid);
+                if (rescale)
+                    rescale_o<D, C::kOnes>(t_o, alpha);
+                m = m_new;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (rescale)
+                        mbar_arrive(smem_addr(&b.p_half[t]));
+                    mbar_arrive(smem_addr(&b.p_full[t]));
+                }
+            } else {
+                const float alpha = softmax_tile<D, kF16, C::kOnes>(p, t_s, r, j, first_vis, first,
+                                                                    m, m_new, l, l_round);
+                if (!first && __any_sync(0xffffffffu, m_new != m))
+                    rescale_o<D, C::kOnes>(t_o, alpha);
+                m = m_new;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&b.p_full[t]));
+            }
         }
         if (!ok)
             break;
@@ -776,6 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&b.q_empty[t]), 1);
             mbar_init(smem_addr(&b.s_full[t]), 1);
             mbar_init(smem_addr(&b.p_full[t]), 4);
+            mbar_init(smem_addr(&b.p_half[t]), 4);
             mbar_init(smem_addr(&b.o_full[t]), 1);
             mbar_init(smem_addr(&b.o_empty[t]), 4);
         }
