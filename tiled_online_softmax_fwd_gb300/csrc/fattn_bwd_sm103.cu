@@ -744,27 +744,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// D_i = dO_i . O_i (fp32), one warp per row.
+// D_i = dO_i . O_i (fp32).  Eight bf16 per lane per 16-byte load: a row of
+// D elements takes D/8 lanes, so one warp covers 256/D rows.
 template <int D>
 __global__ void __launch_bounds__(256)
     prep_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                 float *__restrict__ dvec, long long rows)
 {
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
-    if (row >= rows)
-        return;
+    constexpr int kLanes = D / 8;            // lanes per row
+    constexpr int kRowsPerWarp = 32 / kLanes;
     const int lane = threadIdx.x & 31;
-    constexpr int kPer = D / 32;  // 2 or 4 elements per lane
-    const __nv_bfloat16 *orow = o + row * D + lane * kPer;
-    const __nv_bfloat16 *drow = dout + row * D + lane * kPer;
+    const long long row = (static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32) * kRowsPerWarp +
+                          lane / kLanes;
+    const int part = lane % kLanes;
     float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
+        const uint4 c = *reinterpret_cast<const uint4 *>(dout + row * D + part * 8);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, cv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int i = 0; i < kPer; ++i)
-        acc = fmaf(__bfloat162float(orow[i]), __bfloat162float(drow[i]), acc);
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&av[i]));
+            const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&cv[i]));
+            acc = fmaf(x.x, y.x, acc);
+            acc = fmaf(x.y, y.y, acc);
+        }
+    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
+    for (int off = kLanes / 2; off > 0; off >>= 1)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0)
+    if (row < rows && part == 0)
         dvec[row] = acc;
 }
 
@@ -807,8 +816,9 @@ cudaError_t launch_bwd(const BwdArgs &a, const FwdMaps &m, const BwdMaps &mb, in
     p.scale = a.scale;
     p.sl2 = a.scale * kLog2e;
     const long long rows = static_cast<long long>(p.BH) * p.N;
-    prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p.o, p.dout, p.dvec,
-                                                                              rows);
+    const long long rows_per_block = 8LL * (256 / D);  // 8 warps of 256/D rows
+    prep_kernel<D><<<static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block), 256, 0,
+                     stream>>>(p.o, p.dout, p.dvec, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
