@@ -97,11 +97,17 @@ fattn_status_t attn_fwd_fp16(const void *q, const void *k, const void *v, void *
  *
  * Copies q_host, k_host, v_host to the caller's device buffers dq, dk, dv,
  * runs attn_fwd into do_ / dlse, and copies the results back to o_host and
- * lse_host, all enqueued on `stream`; it then synchronises the stream and
- * returns.  Host buffers should be page-locked (cudaHostAlloc / pinned) for
- * asynchronous full-bandwidth copies; pageable memory works but is slower.
- * Device buffers follow attn_fwd's rules.  The library allocates nothing.
- * The return value includes any error raised while the stream drained.
+ * lse_host; it returns once everything has completed.  The work is
+ * pipelined over up to eight chunks of consecutive (b, h) heads: the copies
+ * in run on a library-owned helper stream, the kernels on `stream`, the
+ * copies out on a second helper stream, ordered by events, so copies and
+ * compute overlap.  The helper streams first wait for the work already
+ * enqueued on `stream`.  Calls are serialised inside the library.  Host
+ * buffers should be page-locked (cudaHostAlloc / pinned) for asynchronous
+ * full-bandwidth copies; pageable memory works but is slower.  Device
+ * buffers follow attn_fwd's rules.  The library allocates no memory (the
+ * helper streams and events are created once per device).  The return value
+ * includes any error raised while the streams drained.
  */
 fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
                              void *o_host, float *lse_host,

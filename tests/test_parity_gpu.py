@@ -214,9 +214,13 @@ def test_side_stream_and_preallocated_outputs():
     assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
 
 
-def test_host_entry_point_matches_device_path():
-    B, H, N, d = 1, 4, 1000, 128
-    q, k, v = make_qkv(B, H, N, d, seed=31)
+@pytest.mark.parametrize("B,H,N,d", [(1, 4, 1000, 128), (2, 5, 700, 64), (3, 1, 300, 128),
+                                     (1, 1, 129, 64), (2, 16, 256, 128)])
+def test_host_entry_point_matches_device_path(B, H, N, d):
+    """The pipelined host entry (copies and compute overlapped over chunks of
+    heads, uneven when B*H is not a multiple of the chunk count) gives the
+    device path's bits."""
+    q, k, v = make_qkv(B, H, N, d, seed=31 + B * H)
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
     ho = torch.empty_like(hq).pin_memory()
     hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()

@@ -489,6 +489,41 @@ fattn_status_t noalloc_scratch(int dev, void **out)
     return FATTN_OK;
 }
 
+// attn_fwd_host's copy/compute pipeline: per-device helper streams and
+// events, created on first use and kept for the process.  Calls are
+// serialised by g_pipe_mutex (each call synchronises before it returns).
+constexpr int kHostChunks = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t ev_in[kHostChunks] = {}, ev_done[kHostChunks] = {};
+};
+std::mutex g_pipe_mutex;
+HostPipe g_pipe[kMaxDevices];
+
+fattn_status_t host_pipe(int dev, HostPipe **out)
+{
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+        for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+            e = cudaEventCreateWithFlags(&hp.ev_in[c], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&hp.ev_done[c], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        hp.ready = true;
+    }
+    *out = &hp;
+    return FATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -773,21 +808,64 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
         return s;
     if (!q_host || !k_host || !v_host || !o_host || !lse_host)
         return FATTN_ERR_INVALID_ARG;
-    const size_t rows = static_cast<size_t>(B) * H * N;
-    const size_t tensor_bytes = rows * d * 2, lse_bytes = rows * 4;
-    cudaError_t e;
-    if ((e = cudaMemcpyAsync(dq, q_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dk, k_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dv, v_host, tensor_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-        return cuda_fail(e);
-    if ((s = launch(Kernel::kTcgen05, info, dq, dk, dv, do_, dlse, B, H, N, N, d, scale, causal,
-                    stream)) != FATTN_OK)
+    // Heads are independent, so the copies and the compute are pipelined
+    // over chunks of consecutive (b, h) heads: copies in on one helper
+    // stream, the kernel on `stream`, copies out on another, ordered by
+    // events.  The helper streams first wait for the work already on
+    // `stream`; the call returns after everything has completed.
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe *hp = nullptr;
+    if ((s = host_pipe(dev, &hp)) != FATTN_OK)
         return s;
-    if ((e = cudaMemcpyAsync(o_host, do_, tensor_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(lse_host, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-        return cuda_fail(e);
-    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess)
-        return cuda_fail(e);
+    const long long BH = static_cast<long long>(B) * H;
+    const int chunks = static_cast<int>(BH < kHostChunks ? BH : kHostChunks);
+    const size_t head_bytes = static_cast<size_t>(N) * d * 2, head_lse = static_cast<size_t>(N) * 4;
+    auto at = [](const void *base, size_t off) {
+        return static_cast<const uint8_t *>(base) + off;
+    };
+    auto atw = [](void *base, size_t off) { return static_cast<uint8_t *>(base) + off; };
+    cudaError_t e = cudaEventRecord(hp->start, stream);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(hp->in, hp->start, 0);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(hp->out, hp->start, 0);
+    for (int c = 0; c < chunks && e == cudaSuccess && s == FATTN_OK; ++c) {
+        const long long h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const size_t off = static_cast<size_t>(h0) * head_bytes;
+        const size_t bytes = static_cast<size_t>(h1 - h0) * head_bytes;
+        if ((e = cudaMemcpyAsync(atw(dq, off), at(q_host, off), bytes, cudaMemcpyHostToDevice,
+                                 hp->in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(dk, off), at(k_host, off), bytes, cudaMemcpyHostToDevice,
+                                 hp->in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(dv, off), at(v_host, off), bytes, cudaMemcpyHostToDevice,
+                                 hp->in)) != cudaSuccess ||
+            (e = cudaEventRecord(hp->ev_in[c], hp->in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(stream, hp->ev_in[c], 0)) != cudaSuccess)
+            break;
+        float *lse_c = reinterpret_cast<float *>(atw(dlse, static_cast<size_t>(h0) * head_lse));
+        if ((s = launch(Kernel::kTcgen05, info, at(dq, off), at(dk, off), at(dv, off),
+                        atw(do_, off), lse_c, 1, static_cast<int>(h1 - h0), N, N, d, scale, causal,
+                        stream)) != FATTN_OK)
+            break;
+        if ((e = cudaEventRecord(hp->ev_done[c], stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hp->out, hp->ev_done[c], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(o_host, off), at(do_, off), bytes, cudaMemcpyDeviceToHost,
+                                 hp->out)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(lse_host, static_cast<size_t>(h0) * head_lse), lse_c,
+                                 static_cast<size_t>(h1 - h0) * head_lse, cudaMemcpyDeviceToHost,
+                                 hp->out)) != cudaSuccess)
+            break;
+    }
+    // Drain all three streams whatever happened, so that no copy still
+    // touches the caller's buffers after the return.
+    const cudaError_t e_in = cudaStreamSynchronize(hp->in);
+    const cudaError_t e_st = cudaStreamSynchronize(stream);
+    const cudaError_t e_out = cudaStreamSynchronize(hp->out);
+    if (s != FATTN_OK)
+        return s;
+    for (cudaError_t x : {e, e_in, e_st, e_out})
+        if (x != cudaSuccess)
+            return cuda_fail(x);
     return FATTN_OK;
 }
 
