@@ -570,10 +570,11 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
         for (int i = 0; i < kBN; ++i)
             s[i] = i > limit ? -INFINITY : s[i];
     }
-    // Row max: four independent chains of 3-input max.
-    float mx[4] = {s[0], s[1], s[2], s[3]};
+    // Row max: four independent chains of 3-input max over s[0..kBN).
+    float mx[4] = {fmaxf(s[0], s[1]), fmaxf(s[2], s[3]), fmaxf(s[4], s[5]), fmaxf(s[6], s[7])};
+    static_assert(kBN % 8 == 0, "the row max takes eight columns per step");
 #pragma unroll
-    for (int i = 4; i < kBN; i += 8) {
+    for (int i = 8; i < kBN; i += 8) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
