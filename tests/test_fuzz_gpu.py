@@ -80,3 +80,45 @@ def test_fuzz_matches_oracle(case):
     r = compare(o.float().cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref,
                 mean_rule="floor")
     assert_parity(r, case_id(case))
+
+
+# ---------------------------------------------------------------- backward
+def draw_bwd(seed):
+    rng = random.Random(seed)
+    d = rng.choice([64, 128])
+    B, H = rng.randint(1, 3), rng.randint(1, 3)
+    N = rng.choice([1, rng.randint(2, 130), rng.randint(131, 600)])
+    while B * H * N * N * d > 6e7:
+        N = max(1, N // 2)
+    return dict(B=B, H=H, N=N, d=d, causal=rng.random() < 0.6, sigma=rng.choice([0.5, 1.0, 2.0]))
+
+
+BWD_CASES = [draw_bwd(5000 + i) for i in range(20)]
+
+
+@pytest.mark.parametrize("case", BWD_CASES,
+                         ids=["B%dH%dN%dd%d%s_sig%g" % (c["B"], c["H"], c["N"], c["d"],
+                                                        "c" if c["causal"] else "", c["sigma"])
+                              for c in BWD_CASES])
+def test_fuzz_backward_matches_oracle(case):
+    """Random shapes through attn_bwd against the oracle's gradients, with the
+    backward tests' tolerances (max |delta| <= 2e-2 max |ref| + 1e-5, mean
+    |delta| <= 1e-2 mean |ref| + 1e-6 per tensor)."""
+    import numpy as np
+    B, H, N, d = case["B"], case["H"], case["N"], case["d"]
+    q, k, v = make_qkv_kv(B, H, N, N, d, seed=zlib.crc32(repr(case).encode()) % 100000,
+                          sigma_qk=case["sigma"])
+    g = torch.Generator("cpu").manual_seed(N + d)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    scale = fattn.default_scale(d)
+    dq_, dk_, dv_ = q.cuda(), k.cuda(), v.cuda()
+    o, lse = fattn.attn_fwd(dq_, dk_, dv_, causal=case["causal"], scale=scale)
+    grads = fattn.attn_bwd(dq_, dk_, dv_, o, lse, dout.cuda(), causal=case["causal"], scale=scale)
+    torch.cuda.synchronize()
+    refs = oracle.attn_bwd(q, k, v, dout, scale, case["causal"])
+    for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
+        got = got.cpu().double().numpy().reshape(ref.shape)
+        assert np.all(np.isfinite(got)), name
+        err = np.abs(got - ref)
+        assert err.max() <= 2e-2 * np.abs(ref).max() + 1e-5, (name, err.max(), np.abs(ref).max())
+        assert err.mean() <= 1e-2 * np.abs(ref).mean() + 1e-6, (name, err.mean(), np.abs(ref).mean())
