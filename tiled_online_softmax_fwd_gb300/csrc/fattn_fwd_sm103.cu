@@ -40,13 +40,17 @@
 // rarely); until then p may exceed 1 by at most 2^kRescaleLog2.  This is
 // exact algebra: O and l always refer to the same m, so O / l and
 // lse = ln2 * (m + log2 l) are unchanged.  Two row sums are kept: l of the
-// fp32 probabilities, for lse, and l_round of the bf16-rounded probabilities
-// that actually enter P V, which normalises O, so that the weights applied to
-// V sum to one exactly (the rounding of a dominant p cancels in O / l_round).
-// For bf16 with d = 64 the tensor cores form l_round: V is extended by a
-// constant column of ones (its own 16 KB swizzle atom after the K/V ring),
-// so column d of the O accumulator is the row sum of the rounded P, summed in
-// fp32 and rescaled together with O (see Cfg::kOnes).
+// fp32 probabilities, for lse, and l_round, which normalises O and stands for
+// the sum of the bf16-rounded probabilities that actually enter P V, so that
+// the rounding of a dominant p cancels in O / l_round.  For bf16 with d = 64
+// it is that sum exactly, formed by the tensor cores: V is extended by a
+// constant column of ones (its own 16 KB swizzle atom after the K/V ring), so
+// column d of the O accumulator is the row sum of the rounded P, summed in
+// fp32 and rescaled together with O (see Cfg::kOnes).  Otherwise l_round is l
+// minus the rounding error of the largest p of each key tile (the only terms
+// whose rounding can move O by more than the bf16 output rounding; the rest
+// are at most 2^-9 of the remaining weight and of random sign), which costs
+// one exponential per tile instead of a second sum over all 128 keys.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <float.h>
@@ -579,18 +583,16 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
         for (int c = 0; c < 4; ++c)
             mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
     }
-    const float cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
+    const float smax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    const float cand = smax * p.sl2;
     m_new = (first || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
     const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
     pre(alpha);
-    // p = 2^(s*scale*log2e - m), two lanes per instruction.  Two row sums:
-    // of the fp32 p (for lse) and of the bf16-rounded p that P V actually
-    // uses (to normalise O; formed by the tensor cores instead with kOnes).
+    // p = 2^(s*scale*log2e - m), two lanes per instruction, and its row sum
+    // (two independent packed accumulators, four partials).
     const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
     const uint64_t negm = f2_pack(-m_new, -m_new);
-    // Two independent packed accumulators per sum (four partials).
     uint64_t sum_exact[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-    uint64_t sum_round[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
     for (int c = 0; c < kBN / 32; ++c) {
         uint32_t pk[16];
@@ -602,23 +604,23 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
             const float p0 = ex2(x0), p1 = ex2(x1);
             pk[i] = pack2<kF16>(p0, p1);
             sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
-            if constexpr (!kF16 && !kOnes)
-                sum_round[i & 1] =
-                    f2_add(sum_round[i & 1], f2_pack(__uint_as_float(pk[i] << 16),
-                                                     __uint_as_float(pk[i] & 0xffff0000u)));
         }
         tmem_st16(t_s + c * 16, pk);
         if (c == kBN / 64 - 1)
             mid();
     }
-    float e0, e1, e2, e3, r0, r1, r2, r3;
+    float e0, e1, e2, e3;
     f2_unpack(sum_exact[0], e0, e1);
     f2_unpack(sum_exact[1], e2, e3);
-    f2_unpack(sum_round[0], r0, r1);
-    f2_unpack(sum_round[1], r2, r3);
-    l = l * alpha + ((e0 + e1) + (e2 + e3));
-    if constexpr (!kOnes)
-        l_round = l_round * alpha + ((r0 + r1) + (r2 + r3));
+    const float esum = (e0 + e1) + (e2 + e3);
+    l = l * alpha + esum;
+    if constexpr (!kF16 && !kOnes) {
+        // The tile's largest p, from the same fused multiply-add and
+        // exponential as its P element, and its bf16 rounding error.
+        const float pt = ex2(fmaf(smax, p.sl2, -m_new));
+        const float pt_round = __uint_as_float(pack2<false>(pt, pt) & 0xffff0000u);
+        l_round = l_round * alpha + (esum - (pt - pt_round));
+    }
     return alpha;
 }
 
