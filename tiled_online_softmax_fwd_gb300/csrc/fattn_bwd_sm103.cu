@@ -20,8 +20,9 @@
 // S and dP are computed twice (once per kernel) so that neither kernel needs
 // atomics or an fp32 dQ accumulator in memory.  The roles are those of the
 // forward kernel: a TMA producer warp, a warp-converged MMA warp with one
-// elected issuing lane, and one warpgroup for the elementwise work, with every
-// wait bounded.
+// elected issuing lane, and two warpgroups for the elementwise work (thread r
+// of warpgroup h owns TMEM lane r and columns 64h..64h+63: the pass has no
+// row reduction, so the halves are independent), with every wait bounded.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -36,9 +37,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kTile = 128;
-constexpr int kThreads = 192;  // warps 0-3 elementwise, 4 producer, 5 MMA
-constexpr int kWarpLoad = 4;
-constexpr int kWarpMma = 5;
+constexpr int kThreads = 320;  // warps 0-7 elementwise, 8 producer, 9 MMA
+constexpr int kElemWarps = 8;   // two warpgroups, one per half of the 128 columns
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -175,25 +177,10 @@ __device__ __forceinline__ void mma_nt(uint32_t tmem_d, uint32_t a_smem, uint32_
 }
 
 // TMEM [128 x 128] (bf16 pairs) x smem tile [128 x D] (D contiguous, i.e.
-// MN-major B) into D fp32 TMEM columns.
-template <int D>
-__device__ __forceinline__ void mma_tn(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_smem,
-                                       bool accumulate)
-{
-    constexpr uint32_t idesc = idesc_bf16_f32(kTile, D, true);
-    constexpr uint32_t lbo = D == 128 ? kChunkBytes : 1024;
-    constexpr uint32_t hi = smem_desc_hi(1024);
-    const uint32_t b_lo = smem_desc_lo(b_smem, lbo);
-    const uint32_t acc0 = accumulate ? 1u : 0u;
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_ts_w(tmem_d, tmem_a + kk * 8, b_lo + ((kk * 16 * 128) >> 4), hi, idesc,
-                 kk > 0 ? 1u : acc0);
-}
-
-// Same product with A in the dK/dV kernel's interleaved TMEM layout: each
-// 32-column chunk of the S^T region holds 16 columns of P^T (part 0) then 16
-// of dS^T (part 16), i.e. K = 16 step kk of A sits at column
+// MN-major B) into D fp32 TMEM columns, with A in the interleaved TMEM layout
+// of the elementwise pass: each 32-column chunk of the S (S^T) region holds
+// 16 columns of one operand (part 0: P^T, or dS in the dQ kernel) then 16 of
+// another (part 16: dS^T), i.e. K = 16 step kk of A sits at column
 // 32*(kk/2) + part + 8*(kk%2).
 template <int D>
 __device__ __forceinline__ void mma_tn_il(uint32_t tmem_d, uint32_t tmem_a, uint32_t part,
@@ -418,9 +405,9 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
                     if (t + 1 == hi - 1)
                         commit(b.res_empty);  // resident pair no longer read
                 }
-                if (leader)
-                    mma_tn<D>(tmem + kColAcc0, tmem + dq_s_col<D>(t - lo), k_tile(t),
-                              t > lo);  // dQ += dS K
+                if (leader)  // dQ += dS K (dS in the first 16 columns of each chunk)
+                    mma_tn_il<D>(tmem + kColAcc0, tmem + dq_s_col<D>(t - lo), 0u, k_tile(t),
+                                 t > lo);
                 commit(b.st_empty[(pos + (t - lo)) % C::kKStages]);
                 if (t == hi - 1)
                     commit(b.o_full);
@@ -500,16 +487,20 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
     mbar_wait(smem_addr(&b.drain), 0, kWaitLimitNs, nullptr);
 }
 
-// Elementwise warpgroup: thread r owns TMEM lane r = row `own*128 + r` of the
-// resident tile (a key in dkdv, a query in dq).
+// Elementwise warpgroups: thread r of either owns TMEM lane r = row
+// `own*128 + r` of the resident tile (a key in dkdv, a query in dq); warpgroup
+// h handles columns 64h..64h+63 of that row (two 32-column chunks), and each
+// chunk's results go back into that chunk's own columns.
 template <int D, bool kDkDv>
 __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
 {
     using C = BCfg<D>;
     const volatile int *abort = &b.abort;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int warp = (threadIdx.x / 32) & 3, lane = threadIdx.x & 31;
+    const int half = threadIdx.x / 128;  // this warpgroup's 64 columns
     const int r = warp * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    constexpr int kHalfChunks = kTile / 64;  // 32-column chunks per half
     uint32_t s_phase = 0, of_phase = 0;
     int xbuf = 0;
     bool ok = true;
@@ -530,11 +521,14 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
         for (int t = lo; ok && t < hi; ++t) {
             if (kDkDv) {
                 // lse and D of the 128 queries of tile t, shared through smem
-                // (double-buffered; a 128-thread barrier publishes them).
+                // (double-buffered; a barrier of both warpgroups publishes
+                // them): warpgroup 0 fetches lse, warpgroup 1 fetches D.
                 const int qrow = t * kTile + r;
-                x.lse2[xbuf][r] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
-                x.dd[xbuf][r] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (half == 0)
+                    x.lse2[xbuf][r] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
+                else
+                    x.dd[xbuf][r] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
+                asm volatile("bar.sync 1, 256;" ::: "memory");
             }
             ok = mbar_wait(smem_addr(&b.s_full), s_phase, kWaitLimitNs, abort);
             s_phase ^= 1;
@@ -594,12 +588,12 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                 }
             };
             if constexpr (kDkDv) {
-                // The whole dP^T row into registers first, so that the MMA
-                // warp can compute dP^T of the next query tile meanwhile.
-                uint32_t dr[kTile];
+                // This half of the dP^T row into registers first, so that the
+                // MMA warp can compute dP^T of the next query tile meanwhile.
+                uint32_t dr[kTile / 2];
 #pragma unroll
-                for (int c = 0; c < kTile / 32; ++c)
-                    tmem_ld32(tmem + lane_off + kColDP + c * 32,
+                for (int c = 0; c < kHalfChunks; ++c)
+                    tmem_ld32(tmem + lane_off + kColDP + (half * kHalfChunks + c) * 32,
                               *reinterpret_cast<uint32_t(*)[32]>(&dr[c * 32]));
                 tmem_wait_ld();
                 if (t + 1 < hi) {
@@ -611,21 +605,22 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                 // P^T and dS^T of chunk ch go into that chunk's own S^T
                 // columns: 16 of P^T pairs, then 16 of dS^T pairs.
 #pragma unroll
-                for (int ch = 0; ch < kTile / 32; ++ch) {
+                for (int hc = 0; hc < kHalfChunks; ++hc) {
+                    const int ch = half * kHalfChunks + hc;
                     uint32_t sr[32], pk[16], dk[16];
                     __syncwarp();
                     tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
                     tmem_wait_ld();
                     if (masked)
-                        pairs(ch, sr, &dr[ch * 32], pk, dk, std::true_type{});
+                        pairs(ch, sr, &dr[hc * 32], pk, dk, std::true_type{});
                     else
-                        pairs(ch, sr, &dr[ch * 32], pk, dk, std::false_type{});
+                        pairs(ch, sr, &dr[hc * 32], pk, dk, std::false_type{});
                     tmem_st16(tmem + lane_off + col_s + ch * 32, pk);
                     tmem_st16(tmem + lane_off + col_s + ch * 32 + 16, dk);
                 }
             } else {
 #pragma unroll 1
-                for (int ch = 0; ch < kTile / 32; ++ch) {
+                for (int ch = half * kHalfChunks; ch < (half + 1) * kHalfChunks; ++ch) {
                     uint32_t sr[32], dr[32], pk[16], dk[16];
                     __syncwarp();
                     tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
@@ -635,7 +630,9 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                         pairs(ch, sr, dr, pk, dk, std::true_type{});
                     else
                         pairs(ch, sr, dr, pk, dk, std::false_type{});
-                    tmem_st16(tmem + lane_off + col_s + ch * 16, dk);  // dS over S
+                    // dS over the first half of its own chunk of S (the
+                    // other warpgroup may still be reading its chunks).
+                    tmem_st16(tmem + lane_off + col_s + ch * 32, dk);
                 }
             }
             tmem_wait_st();
@@ -654,14 +651,17 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
             break;
         tc_fence_after();
         const bool live = row < p.N;
-#pragma unroll 1
-        for (int which = 0; which < (kDkDv ? 2 : 1); ++which) {
-            // dkdv: which 0 = dV (acc0, unscaled) -> g1, which 1 = dK (acc1) -> g0
-            const uint32_t col = which == 0 ? kColAcc0 : C::kColAcc1;
+        {
+            // dkdv: warpgroup 0 writes dV (acc0, unscaled) -> g1, warpgroup 1
+            // dK (acc1) -> g0; dq: each warpgroup half of the columns of dQ.
+            const int which = kDkDv ? half : 1;
+            const uint32_t col = which == 0 ? kColAcc0 : (kDkDv ? C::kColAcc1 : kColAcc0);
             const float f = (kDkDv && which == 0) ? 1.f : p.scale;
             __nv_bfloat16 *dst = ((kDkDv && which == 0) ? p.g1 : p.g0) + (head + row) * D;
+            const int c_begin = kDkDv ? 0 : half * (D / 64);
+            const int c_end = kDkDv ? D / 32 : (half + 1) * (D / 64);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = c_begin; c < c_end; ++c) {
                 uint32_t o[32];
                 __syncwarp();
                 tmem_ld32(tmem + lane_off + col + c * 32, o);
@@ -713,10 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&b.v_empty[s]), 1);
         }
         mbar_init(smem_addr(&b.s_full), 1);
-        mbar_init(smem_addr(&b.p_full), 4);
+        mbar_init(smem_addr(&b.p_full), kElemWarps);
         mbar_init(smem_addr(&b.o_full), 1);
-        mbar_init(smem_addr(&b.o_empty), 4);
-        mbar_init(smem_addr(&b.dp_free), 4);
+        mbar_init(smem_addr(&b.o_empty), kElemWarps);
+        mbar_init(smem_addr(&b.dp_free), kElemWarps);
         mbar_init(smem_addr(&b.drain), 1);
         b.abort = 0;
         fence_barrier_init();
@@ -729,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = b.tmem_base;
-    if (warp < 4)
+    if (warp < kElemWarps)
         bwd_elem<D, kDkDv>(p, b, xch, tmem);
     else if (warp == kWarpLoad)
         bwd_load<D, kDkDv>(p, b, smem, &ra0, &ra1, &sb0, &sb1);
