@@ -125,7 +125,7 @@ struct Params {
     void *o;       // bf16 or fp16, element (b, h, i, c) at b*o_sb + h*o_sh + i*o_sn + c
     float *lse;
     float *ws_o;   // split mode: fp32 partial O [splits][B*H*Nq][D]
-    float2 *ws_l;  // split mode: base-2 partial lse (exact sum, rounded sum) [splits][B*H*Nq]
+    float2 *ws_l;  // split mode: base-2 partial lse (of l, of l_round) [splits][B*H*Nq]
     int Nq;        // query rows per head
     int Nk;        // keys per head
     int off;       // Nk - Nq: query i sits at key position i + off (causal mask)
@@ -1216,8 +1216,8 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
 // ------------------------------------------------------------------ combine
 // Merge of the key-range splits of each row (the blocked softmax statistics
 // merge: per-block maxima and sums combined into the global ones).  With
-// base-2 partial log-sum-exps le_s (exact sums) and lr_s (rounded sums) and
-// partial outputs O_s = acc_s / l_round_s:
+// base-2 partial log-sum-exps le_s (of the exact sums l) and lr_s (of the
+// normalisers l_round) and partial outputs O_s = acc_s / l_round_s:
 //   lse = ln2 * log2(sum_s 2^le_s)
 //   O   = sum_s w_s O_s,  w_s = 2^lr_s / sum_s' 2^lr_s'
 // Slots with no key tile for the row's Q tile are skipped (the same ranges
