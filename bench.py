@@ -350,6 +350,55 @@ def run_bwd(args, world, rank, local):
     return 0
 
 
+SDPA_OPS = ["sdpa_" + n for n in sorted(WORKLOADS)]
+
+
+def run_sdpa(args, world, rank, local):
+    """Library context, not part of the product: torch's
+    scaled_dot_product_attention (bf16, whatever backend torch picks on this
+    GPU) timed on the same inputs as the forward workload, so that the
+    forward's figure can be read beside a library number."""
+    torch.cuda.set_device(local)
+    w = WORKLOADS[args.op[len("sdpa_"):]]
+    q, k, v, _ = make_workload(w)
+    dq_, dk_, dv_ = q.cuda(), k.cuda(), v.cuda()
+    sdpa = torch.nn.functional.scaled_dot_product_attention
+    label = "library: torch.nn.functional.scaled_dot_product_attention (torch %s)" % torch.__version__
+
+    def step():
+        return sdpa(dq_, dk_, dv_, is_causal=bool(w.causal), scale=w.scale)
+    try:
+        step()
+        torch.cuda.synchronize()
+    except Exception as e:  # no kernel for this GPU or shape
+        if rank == 0:
+            print(json.dumps({"impl": label, "unavailable": str(e).splitlines()[0][:200]}),
+                  flush=True)
+        return 0
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    value = w.flops / (ms * 1e-3) / 1e12
+    peak, peak_src = measured_peak()
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "impl": label, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, **w.describe()},
+            "frac_of_peak": value / peak, "peak_source": peak_src,
+            "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ decode shapes
 def peak_hbm():
     try:
@@ -629,8 +678,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--op", default=None,
-                    choices=sorted(ROWOP_WORKLOADS) + BWD_WORKLOADS + sorted(KV_WORKLOADS),
-                    help="time a row softmax / row sum, backward or decode-shape workload instead")
+                    choices=sorted(ROWOP_WORKLOADS) + BWD_WORKLOADS + sorted(KV_WORKLOADS) +
+                    SDPA_OPS,
+                    help="time a row softmax / row sum, backward or decode-shape workload "
+                         "instead, or (sdpa_*) torch's attention on a forward workload as context")
     ap.add_argument("--fp16", action="store_true", help="fp16 inputs through attn_fwd_fp16")
     ap.add_argument("--split", default="auto", choices=["auto", "off"],
                     help="key-range split when the library recommends one (auto) or never")
@@ -642,6 +693,8 @@ def main():
         return run_bwd(args, world, rank, local)
     if args.op in KV_WORKLOADS:
         return run_kv(args, world, rank, local)
+    if args.op in SDPA_OPS:
+        return run_sdpa(args, world, rank, local)
     if args.op:
         return run_rowop(args, world, rank, local)
     return run_gpu(args, world, rank, local)
