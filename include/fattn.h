@@ -26,7 +26,8 @@
  *     every buffer; q, k, v are only read; o and lse are fully overwritten
  *     (every row 0..N-1 of every head).  o and lse must not overlap q, k, v
  *     or each other.
- *   - Supported: d in {64, 128}; B, H, N >= 0 with B*H < 2^31 and each
+ *   - Supported: d in {64, 96, 128, 256} for the forward calls (attn_bwd:
+ *     64 or 128; attn_fwd_simt: up to 128); B, H, N >= 0 with B*H < 2^31 and each
  *     tensor under 2^39 bytes; scale finite and > 0; causal in {0, 1}.
  *     Any N works: a ragged last tile is masked (keys past N get weight 0,
  *     rows past N are not written).
@@ -53,7 +54,7 @@ struct CUstream_st; /* cudaStream_t / CUstream */
 typedef enum fattn_status {
     FATTN_OK = 0,
     FATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, misalignment, overlap */
-    FATTN_ERR_UNSUPPORTED = 2, /* d not in {64,128}, tensor too large, device is not sm_103 */
+    FATTN_ERR_UNSUPPORTED = 2, /* d not supported by the call, tensor too large, device is not sm_103 */
     FATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; see fattn_last_cuda_error() */
     FATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a pipeline wait (see fattn_get_device_status) */
 } fattn_status_t;
@@ -66,7 +67,7 @@ typedef enum fattn_status {
  *   lse     : device, fp32 [B][H][N], written: natural-log log-sum-exp of
  *             the scaled (and masked) scores of each row
  *   B, H, N : batch, heads, sequence length (queries and keys alike)
- *   d       : head dimension, 64 or 128
+ *   d       : head dimension, 64, 96, 128 or 256
  *   scale   : multiplies Q.K before masking and softmax (usually 1/sqrt(d))
  *   causal  : 1 keeps keys j <= i for query i, 0 keeps all keys
  *   stream  : CUDA stream the kernel is enqueued on
@@ -183,7 +184,7 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
  *
  *   q     : bf16 [B][H][Nq][d]      k, v : bf16 [B][H][Nk][d]
  *   o     : bf16 [B][H][Nq][d]      lse  : fp32 [B][H][Nq]
- * All contiguous, device memory, 16-byte aligned; d in {64, 128}.
+ * All contiguous, device memory, 16-byte aligned; d in {64, 96, 128, 256}.
  * Without the mask every query sees all Nk keys.  With causal = 1 the Nq
  * queries are the LAST Nq positions of the key sequence: query i sees keys
  * j <= i + (Nk - Nq), so Nq <= Nk is required; Nq == Nk is attn_fwd's causal
