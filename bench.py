@@ -181,6 +181,12 @@ def cpu_baseline(w, q, k, v, rows_all, budget_s=15.0):
     threads = oracle.default_threads()
     qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
     per_head = rows_all.view(w.B * w.H, -1)
+    # Past the checked rows, more seeded rows per head, so that the sample
+    # fills the time budget (about 10-30 s of CPU work) on a fast host.
+    g = torch.Generator("cpu").manual_seed(20250)
+    extra = torch.randint(0, w.N, (w.B * w.H, 8 * per_head.shape[1]), generator=g)
+    extra += (torch.arange(w.B * w.H, dtype=torch.int64) * w.N)[:, None]
+    per_head = torch.cat([per_head.to(torch.int64), extra], 1)
     total_rows, total_flops, t_total, used = 0, 0.0, 0.0, 0
     col = 0
     while t_total < budget_s and col < per_head.shape[1]:
