@@ -11,8 +11,8 @@
 //   dkdv_kernel    one CTA per 128-row key tile j (persistent, heaviest
 //                  first): for every query tile i it computes S^T = K_j Q_i^T
 //                  and dP^T = V_j dO_i^T on the tensor cores (keys on TMEM
-//                  lanes), one thread per key row forms P^T and dS^T in bf16
-//                  back into TMEM, and the tensor cores accumulate
+//                  lanes); the elementwise threads form P^T in bf16 over S^T,
+//                  then dS^T over dP^T, and the tensor cores accumulate
 //                  dV_j += P^T dO_i and dK_j += dS^T Q_i in TMEM.
 //   dq_kernel      one CTA per 128-row query tile i: for every key tile j,
 //                  S = Q_i K_j^T and dP = dO_i V_j^T, one thread per query
@@ -66,19 +66,7 @@ struct BCfg {
     // so that S of the next key tile is computed while the elementwise pass
     // works on this one.
     static constexpr uint32_t kColS1 = kColAcc0 + D;
-    // dK/dV kernel at d = 64: the two accumulators leave 128 columns, a
-    // second S^T buffer, so S^T of the next query tile is computed while the
-    // elementwise pass works on this one.
-    static constexpr bool kSDouble = kDkDv && D == 64;
-    static constexpr uint32_t kColS1DkDv = kColAcc0 + 2 * D;
 };
-
-// dK/dV kernel: the S^T buffer of the i-th query tile of a unit.
-template <int D>
-__device__ __forceinline__ uint32_t dkdv_s_col(int i)
-{
-    return (BCfg<D, true>::kSDouble && (i & 1)) ? BCfg<D, true>::kColS1DkDv : kColS;
-}
 
 // dq kernel: the S buffer of the i-th key tile of a unit.
 template <int D>
@@ -89,10 +77,12 @@ __device__ __forceinline__ uint32_t dq_s_col(int i)
 
 struct BBars {
     uint64_t res_full, res_empty;  // the CTA's resident pair (K_j,V_j or Q_i,dO_i)
-    uint64_t st_full[3], st_empty[3];  // dK/dV: (Q, dO) stages; dQ: K stages
-    uint64_t v_full[2], v_empty[2];    // dQ: V stages
+    uint64_t st_full[3], st_empty[3];  // dK/dV: Q stages; dQ: K stages
+    uint64_t v_full[2], v_empty[2];    // dK/dV: dO stages; dQ: V stages
     uint64_t s_full, p_full, o_full, o_empty;
-    uint64_t dp_free;  // dkdv: the elementwise pass has dP^T in registers
+    // dkdv: P^T of the tile written (p_full then means dS^T written), and
+    // dP^T of the tile computed (s_full then means S^T computed).
+    uint64_t p1_full, dp_full;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -213,7 +203,7 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
     using C = BCfg<D, kDkDv>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
-    uint32_t res_phase = 0, pos = 0, kpos = 0, vpos = 0;
+    uint32_t res_phase = 0, kpos = 0, vpos = 0;
     bool ok = true;
     int res_issued = 0;
     for (int r = 0; ok; ++r) {
@@ -272,23 +262,37 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
                 ++vpos;
             }
         } else {
-            for (int t = lo; ok && t < hi; ++t, ++pos) {
-                const uint32_t stage = pos & 1, phase = (pos >> 1) & 1;
+            // Q(t) and dO(t) share a stage of the two-stage ring but are
+            // released separately: dO after dV(t), Q after dK(t).  kpos and
+            // vpos count the Q and dO tiles issued.
+            for (int t = lo; ok && t < hi; ++t) {
+                const uint32_t stage = kpos & 1, phase = (kpos >> 1) & 1;
+                const uint32_t dst = smem + (2 + 2 * stage) * C::kTileBytes;
                 if (!warp_wait(smem_addr(&b.st_empty[stage]), phase ^ 1, abort)) {
                     ok = false;
                     break;
                 }
                 if (leader) {
                     const uint32_t full = smem_addr(&b.st_full[stage]);
-                    const uint32_t dst = smem + (2 + 2 * stage) * C::kTileBytes;
-                    mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+                    mbar_arrive_expect_tx(full, C::kTileBytes);
 #pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c) {
+                    for (int c = 0; c < C::kChunks; ++c)
                         tma_load_3d(dst + c * kChunkBytes, sb0, full, 64 * c, t * kTile, bh);
+                }
+                ++kpos;
+                if (!warp_wait(smem_addr(&b.v_empty[stage]), phase ^ 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    const uint32_t full = smem_addr(&b.v_full[stage]);
+                    mbar_arrive_expect_tx(full, C::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
                         tma_load_3d(dst + C::kTileBytes + c * kChunkBytes, sb1, full, 64 * c,
                                     t * kTile, bh);
-                    }
                 }
+                ++vpos;
             }
         }
     }
@@ -297,8 +301,10 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
             fail(p, b, kRoleLoad);
         // Let the copies already issued land before the CTA exits.
         if constexpr (kDkDv) {
-            for (uint32_t q = pos > 2 ? pos - 2 : 0; q < pos; ++q)
+            for (uint32_t q = kpos > 2 ? kpos - 2 : 0; q < kpos; ++q)
                 mbar_wait(smem_addr(&b.st_full[q & 1]), (q >> 1) & 1, kWaitLimitNs / 8, nullptr);
+            for (uint32_t q = vpos > 2 ? vpos - 2 : 0; q < vpos; ++q)
+                mbar_wait(smem_addr(&b.v_full[q & 1]), (q >> 1) & 1, kWaitLimitNs / 8, nullptr);
         } else {
             for (uint32_t q = kpos > 3 ? kpos - 3 : 0; q < kpos; ++q)
                 mbar_wait(smem_addr(&b.st_full[q % 3]), (q / 3) & 1, kWaitLimitNs / 8, nullptr);
@@ -414,64 +420,74 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
             }
             pos += hi - lo;
         } else {
-            // dkdv: dP^T(t+1) is issued as soon as the elementwise pass holds
-            // dP^T(t) in registers; after P^T(t) and dS^T(t) (interleaved in
-            // the S^T columns) come dV += P^T dO and dK += dS^T Q, then
-            // S^T(t+1) over them.
+            // dkdv: the elementwise pass writes P^T(t) over the S^T columns
+            // and then dS^T(t) over the dP^T columns (the first 16 of every
+            // 32), so S^T(t+1) follows dV(t) and dP^T(t+1) follows dK(t): the
+            // pass forms P^T of the next tile while dK(t) and dP^T(t+1) run.
+            // dO(t) is released after dV(t), Q(t) after dK(t).
             if (hi <= lo)
                 continue;
-            auto wait_stage = [&](int t) {
+            auto wait_q = [&](int t) {
                 const uint32_t at = pos + (t - lo);
                 return warp_wait(smem_addr(&b.st_full[at & 1]), (at >> 1) & 1, abort);
             };
-            ok = wait_stage(lo);
+            auto wait_do = [&](int t) {
+                const uint32_t at = pos + (t - lo);
+                return warp_wait(smem_addr(&b.v_full[at & 1]), (at >> 1) & 1, abort);
+            };
+            ok = wait_q(lo);
             if (!ok)
                 break;
             tc_fence_after();
-            if (leader) {
-                mma_nt<D>(tmem + dkdv_s_col<D>(0), a0, stage_smem(pos));        // S^T = K Q^T
-                mma_nt<D>(tmem + kColDP, a1, stage_smem(pos) + C::kTileBytes);  // dP^T = V dO^T
-            }
+            if (leader)
+                mma_nt<D>(tmem + kColS, a0, stage_smem(pos));  // S^T = K Q^T
             commit(b.s_full);
+            ok = wait_do(lo);
+            if (!ok)
+                break;
+            tc_fence_after();
+            if (leader)
+                mma_nt<D>(tmem + kColDP, a1, stage_smem(pos) + C::kTileBytes);  // dP^T = V dO^T
+            commit(b.dp_full);
             if (lo == hi - 1)
                 commit(b.res_empty);
             for (int t = lo; ok && t < hi; ++t) {
                 const uint32_t at = pos + (t - lo);
                 const bool next = t + 1 < hi;
+                const uint32_t q_t = stage_smem(at), do_t = q_t + C::kTileBytes;
+                ok = warp_wait(smem_addr(&b.p1_full), dp_phase, abort);
+                dp_phase ^= 1;
+                if (!ok)
+                    break;
+                tc_fence_after();
+                if (leader)  // dV += P^T dO
+                    mma_tn_il<D>(tmem + kColAcc0, tmem + kColS, 0u, do_t, t > lo);
+                commit(b.v_empty[at & 1]);
                 if (next) {
-                    ok = warp_wait(smem_addr(&b.dp_free), dp_phase, abort);
-                    dp_phase ^= 1;
-                    if (ok)
-                        ok = wait_stage(t + 1);
+                    ok = wait_q(t + 1);
                     if (!ok)
                         break;
                     tc_fence_after();
                     if (leader)
-                        mma_nt<D>(tmem + kColDP, a1, stage_smem(at + 1) + C::kTileBytes);
-                    if constexpr (C::kSDouble) {  // S^T(t+1) into the other buffer
-                        if (leader)
-                            mma_nt<D>(tmem + dkdv_s_col<D>(t + 1 - lo), a0, stage_smem(at + 1));
-                        commit(b.s_full);
-                        if (t + 1 == hi - 1)
-                            commit(b.res_empty);
-                    }
+                        mma_nt<D>(tmem + kColS, a0, stage_smem(at + 1));  // S^T(t+1)
+                    commit(b.s_full);
                 }
                 ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
                 s_phase ^= 1;
                 if (!ok)
                     break;
                 tc_fence_after();
-                if (leader) {
-                    const uint32_t q_t = stage_smem(at), do_t = q_t + C::kTileBytes;
-                    const uint32_t col = dkdv_s_col<D>(t - lo);
-                    mma_tn_il<D>(tmem + kColAcc0, tmem + col, 0u, do_t, t > lo);      // dV += P^T dO
-                    mma_tn_il<D>(tmem + C::kColAcc1, tmem + col, 16u, q_t, t > lo);   // dK += dS^T Q
-                }
+                if (leader)  // dK += dS^T Q
+                    mma_tn_il<D>(tmem + C::kColAcc1, tmem + kColDP, 0u, q_t, t > lo);
                 commit(b.st_empty[at & 1]);
-                if (!C::kSDouble && next) {
+                if (next) {
+                    ok = wait_do(t + 1);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
                     if (leader)
-                        mma_nt<D>(tmem + kColS, a0, stage_smem(at + 1));  // S^T(t+1)
-                    commit(b.s_full);
+                        mma_nt<D>(tmem + kColDP, a1, stage_smem(at + 1) + C::kTileBytes);
+                    commit(b.dp_full);
                     if (t + 1 == hi - 1)
                         commit(b.res_empty);  // resident pair no longer read
                 }
@@ -501,7 +517,7 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
     const int r = warp * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     constexpr int kHalfChunks = kTile / 64;  // 32-column chunks per half
-    uint32_t s_phase = 0, of_phase = 0;
+    uint32_t s_phase = 0, of_phase = 0, dp_phase = 0;
     int xbuf = 0;
     bool ok = true;
     for (int rr = 0; ok; ++rr) {
@@ -548,26 +564,23 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                     c_hi = r;  // key t*128+c <= query own*128+r
             }
             c_hi = min(c_hi, p.N - 1 - col0);
-            const uint32_t col_s = kDkDv ? dkdv_s_col<D>(t - lo) : dq_s_col<D>(t - lo);
+            const uint32_t col_s = kDkDv ? kColS : dq_s_col<D>(t - lo);
             // Element mask only on the diagonal tile and the ragged last one
             // (the branch is uniform across the warp).
             const bool masked = (p.causal && t == own) || col0 + kTile > p.N;
             const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
             const uint64_t row_nl2 = f2_pack(-my_lse2, -my_lse2), row_nd = f2_pack(-my_d, -my_d);
-            // 16 column pairs of one 32-column chunk: p = 2^(s*scale*log2e -
-            // lse*log2e) and dS = p (dP - D), two columns per packed
-            // instruction; returns P and dS packed to bf16 pairs.
+            // dq: 16 column pairs of one 32-column chunk: p = 2^(s*scale*log2e -
+            // lse*log2e) and dS = p (dP - D) of this thread's query row, two
+            // columns per packed instruction; returns dS packed to bf16 pairs
+            // (and P, unused there).
             auto pairs = [&](int ch, const uint32_t *sr, const uint32_t *dr, uint32_t *pk,
                              uint32_t *dk, auto masked_tag) {
                 constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int c = ch * 32 + 2 * i;
-                    uint64_t nl2 = row_nl2, nd = row_nd;
-                    if (kDkDv) {
-                        nl2 = *reinterpret_cast<const uint64_t *>(&x.lse2[xbuf][c]);
-                        nd = *reinterpret_cast<const uint64_t *>(&x.dd[xbuf][c]);
-                    }
+                    const uint64_t nl2 = row_nl2, nd = row_nd;
                     float x0, x1;
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
                                      sl2x2, nl2),
@@ -587,36 +600,82 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                     dk[i] = pack2(d0, d1);
                 }
             };
-            if constexpr (kDkDv) {
-                // This half of the dP^T row into registers first, so that the
-                // MMA warp can compute dP^T of the next query tile meanwhile.
-                uint32_t dr[kTile / 2];
+            // The dK/dV kernel's two phases over one chunk: probs forms p (kept
+            // as fp32) and P packed; grads forms dS = p (dP - D) packed.
+            auto probs = [&](int ch, const uint32_t *sr, float *pf, uint32_t *pk,
+                             auto masked_tag) {
+                constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-                for (int c = 0; c < kHalfChunks; ++c)
-                    tmem_ld32(tmem + lane_off + kColDP + (half * kHalfChunks + c) * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&dr[c * 32]));
-                tmem_wait_ld();
-                if (t + 1 < hi) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_addr(&b.dp_free));
+                for (int i = 0; i < 16; ++i) {
+                    const int c = ch * 32 + 2 * i;
+                    const uint64_t nl2 = *reinterpret_cast<const uint64_t *>(&x.lse2[xbuf][c]);
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                     sl2x2, nl2),
+                              x0, x1);
+                    float p0 = ex2(x0), p1 = ex2(x1);
+                    if constexpr (kMasked) {
+                        p0 = (c >= c_lo && c <= c_hi) ? p0 : 0.f;
+                        p1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? p1 : 0.f;
+                    }
+                    pf[2 * i] = p0;
+                    pf[2 * i + 1] = p1;
+                    pk[i] = pack2(p0, p1);
                 }
-                // P^T and dS^T of chunk ch go into that chunk's own S^T
-                // columns: 16 of P^T pairs, then 16 of dS^T pairs.
+            };
+            auto grads = [&](int ch, const float *pf, const uint32_t *dr, uint32_t *dk) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = ch * 32 + 2 * i;
+                    const uint64_t nd = *reinterpret_cast<const uint64_t *>(&x.dd[xbuf][c]);
+                    float d0, d1;
+                    f2_unpack(f2_mul(f2_pack(pf[2 * i], pf[2 * i + 1]),
+                                     f2_add(f2_pack(__uint_as_float(dr[2 * i]),
+                                                    __uint_as_float(dr[2 * i + 1])),
+                                            nd)),
+                              d0, d1);
+                    dk[i] = pack2(d0, d1);
+                }
+            };
+            if constexpr (kDkDv) {
+                // Phase 1: P^T of this half's chunks, kept in registers and
+                // written over the first 16 columns of each S^T chunk; then
+                // dV and S^T of the next tile may run.
+                float pr[kHalfChunks][32];
 #pragma unroll
                 for (int hc = 0; hc < kHalfChunks; ++hc) {
                     const int ch = half * kHalfChunks + hc;
-                    uint32_t sr[32], pk[16], dk[16];
+                    uint32_t sr[32], pk[16];
                     __syncwarp();
-                    tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
+                    tmem_ld32(tmem + lane_off + kColS + ch * 32, sr);
                     tmem_wait_ld();
                     if (masked)
-                        pairs(ch, sr, &dr[hc * 32], pk, dk, std::true_type{});
+                        probs(ch, sr, pr[hc], pk, std::true_type{});
                     else
-                        pairs(ch, sr, &dr[hc * 32], pk, dk, std::false_type{});
-                    tmem_st16(tmem + lane_off + col_s + ch * 32, pk);
-                    tmem_st16(tmem + lane_off + col_s + ch * 32 + 16, dk);
+                        probs(ch, sr, pr[hc], pk, std::false_type{});
+                    tmem_st16(tmem + lane_off + kColS + ch * 32, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&b.p1_full));
+                // Phase 2: dS^T = P^T (dP^T - D) over the first 16 columns of
+                // each of this half's dP^T chunks.
+                ok = mbar_wait(smem_addr(&b.dp_full), dp_phase, kWaitLimitNs, abort);
+                dp_phase ^= 1;
+                if (!ok)
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int hc = 0; hc < kHalfChunks; ++hc) {
+                    const int ch = half * kHalfChunks + hc;
+                    uint32_t dr[32], dk[16];
+                    __syncwarp();
+                    tmem_ld32(tmem + lane_off + kColDP + ch * 32, dr);
+                    tmem_wait_ld();
+                    grads(ch, pr[hc], dr, dk);
+                    tmem_st16(tmem + lane_off + kColDP + ch * 32, dk);
                 }
             } else {
 #pragma unroll 1
@@ -716,7 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&b.p_full), kElemWarps);
         mbar_init(smem_addr(&b.o_full), 1);
         mbar_init(smem_addr(&b.o_empty), kElemWarps);
-        mbar_init(smem_addr(&b.dp_free), kElemWarps);
+        mbar_init(smem_addr(&b.p1_full), kElemWarps);
+        mbar_init(smem_addr(&b.dp_full), 1);
         mbar_init(smem_addr(&b.drain), 1);
         b.abort = 0;
         fence_barrier_init();
