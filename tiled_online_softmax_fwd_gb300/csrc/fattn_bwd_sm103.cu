@@ -268,18 +268,7 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
             for (int t = lo; ok && t < hi; ++t) {
                 const uint32_t stage = kpos & 1, phase = (kpos >> 1) & 1;
                 const uint32_t dst = smem + (2 + 2 * stage) * C::kTileBytes;
-                if (!warp_wait(smem_addr(&b.st_empty[stage]), phase ^ 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                if (leader) {
-                    const uint32_t full = smem_addr(&b.st_full[stage]);
-                    mbar_arrive_expect_tx(full, C::kTileBytes);
-#pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(dst + c * kChunkBytes, sb0, full, 64 * c, t * kTile, bh);
-                }
-                ++kpos;
+                // dO first: its slot is released (after dV) before Q's (after dK).
                 if (!warp_wait(smem_addr(&b.v_empty[stage]), phase ^ 1, abort)) {
                     ok = false;
                     break;
@@ -293,6 +282,18 @@ __device__ void bwd_load(const BParams &p, BBars &b, uint32_t smem, const CUtens
                                     t * kTile, bh);
                 }
                 ++vpos;
+                if (!warp_wait(smem_addr(&b.st_empty[stage]), phase ^ 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    const uint32_t full = smem_addr(&b.st_full[stage]);
+                    mbar_arrive_expect_tx(full, C::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(dst + c * kChunkBytes, sb0, full, 64 * c, t * kTile, bh);
+                }
+                ++kpos;
             }
         }
     }
