@@ -83,6 +83,7 @@ struct BBars {
     // dkdv: P^T of the tile written (p_full then means dS^T written), and
     // dP^T of the tile computed (s_full then means S^T computed).
     uint64_t p1_full, dp_full;
+    uint64_t dp_free;  // dq: the elementwise pass holds dP in registers
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -349,9 +350,10 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
         if (!ok)
             break;
         if constexpr (!kDkDv) {
-            // dq: S(t+1) goes into the other S buffer before P(t) is ready,
-            // and dP(t+1) follows as soon as the elementwise pass of t has
-            // read dP(t); dQ += dS(t) K_t comes after it.  K(t) sits in the
+            // dq: S(t+1) goes into the other S buffer before dS(t) is ready,
+            // and dP(t+1) follows as soon as the elementwise pass of t holds
+            // dP(t) in registers (dp_free); dQ += dS(t) K_t once dS(t) is
+            // written.  K(t) sits in the
             // three-stage K ring until dQ(t), V(t) in the two-stage V ring
             // until dP(t).  Position pos is tile lo in both rings.
             if (hi <= lo)
@@ -397,8 +399,10 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
                     if (leader)
                         mma_nt<D>(tmem + dq_s_col<D>(t + 1 - lo), a0, k_tile(t + 1));
                 }
-                ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
-                s_phase ^= 1;
+                if (next) {
+                    ok = warp_wait(smem_addr(&b.dp_free), dp_phase, abort);
+                    dp_phase ^= 1;
+                }
                 if (ok && next)
                     ok = wait_v(t + 1);
                 if (!ok)
@@ -412,6 +416,11 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
                     if (t + 1 == hi - 1)
                         commit(b.res_empty);  // resident pair no longer read
                 }
+                ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
+                s_phase ^= 1;
+                if (!ok)
+                    break;
+                tc_fence_after();
                 if (leader)  // dQ += dS K (dS in the first 16 columns of each chunk)
                     mma_tn_il<D>(tmem + kColAcc0, tmem + dq_s_col<D>(t - lo), 0u, k_tile(t),
                                  t > lo);
@@ -679,17 +688,30 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                     tmem_st16(tmem + lane_off + kColDP + ch * 32, dk);
                 }
             } else {
-#pragma unroll 1
-                for (int ch = half * kHalfChunks; ch < (half + 1) * kHalfChunks; ++ch) {
-                    uint32_t sr[32], dr[32], pk[16], dk[16];
+                // This half of the dP row into registers first, so that dP of
+                // the next key tile is computed meanwhile.
+                uint32_t dr[kHalfChunks][32];
+#pragma unroll
+                for (int hc = 0; hc < kHalfChunks; ++hc)
+                    tmem_ld32(tmem + lane_off + kColDP + (half * kHalfChunks + hc) * 32, dr[hc]);
+                tmem_wait_ld();
+                if (t + 1 < hi) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_addr(&b.dp_free));
+                }
+#pragma unroll
+                for (int hc = 0; hc < kHalfChunks; ++hc) {
+                    const int ch = half * kHalfChunks + hc;
+                    uint32_t sr[32], pk[16], dk[16];
                     __syncwarp();
                     tmem_ld32(tmem + lane_off + col_s + ch * 32, sr);
-                    tmem_ld32(tmem + lane_off + kColDP + ch * 32, dr);
                     tmem_wait_ld();
                     if (masked)
-                        pairs(ch, sr, dr, pk, dk, std::true_type{});
+                        pairs(ch, sr, dr[hc], pk, dk, std::true_type{});
                     else
-                        pairs(ch, sr, dr, pk, dk, std::false_type{});
+                        pairs(ch, sr, dr[hc], pk, dk, std::false_type{});
                     // dS over the first half of its own chunk of S (the
                     // other warpgroup may still be reading its chunks).
                     tmem_st16(tmem + lane_off + col_s + ch * 32, dk);
@@ -778,6 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&b.o_empty), kElemWarps);
         mbar_init(smem_addr(&b.p1_full), kElemWarps);
         mbar_init(smem_addr(&b.dp_full), 1);
+        mbar_init(smem_addr(&b.dp_free), kElemWarps);
         mbar_init(smem_addr(&b.drain), 1);
         b.abort = 0;
         fence_barrier_init();
