@@ -546,15 +546,20 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
         }
         for (int t = lo; ok && t < hi; ++t) {
             if (kDkDv) {
-                // lse and D of the 128 queries of tile t, shared through smem
-                // (double-buffered; a barrier of both warpgroups publishes
-                // them): warpgroup 0 fetches lse, warpgroup 1 fetches D.
-                const int qrow = t * kTile + r;
-                if (half == 0)
-                    x.lse2[xbuf][r] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
+                // lse and D of this warpgroup's 64 queries of tile t, shared
+                // through smem (double-buffered; a barrier of the warpgroup
+                // alone publishes them, so the two warpgroups never wait for
+                // each other here): threads 0-63 fetch lse, 64-127 fetch D.
+                const int q = half * 64 + (r & 63);
+                const int qrow = t * kTile + q;
+                if (r < 64)
+                    x.lse2[xbuf][q] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
                 else
-                    x.dd[xbuf][r] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                    x.dd[xbuf][q] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
+                if (half == 0)
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                else
+                    asm volatile("bar.sync 2, 128;" ::: "memory");
             }
             ok = mbar_wait(smem_addr(&b.s_full), s_phase, kWaitLimitNs, abort);
             s_phase ^= 1;
