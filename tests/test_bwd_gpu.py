@@ -47,6 +47,9 @@ for N in (1, 17, 128, 129, 300, 513):
         for causal in (False, True):
             CASES.append((1, 2, N, d, causal))
 CASES += [(2, 3, 256, 128, True), (1, 1, 1024, 64, False), (3, 2, 700, 128, True)]
+# Several work units per CTA (640 key tiles and 640 query tiles over the
+# SMs), so every pipeline crosses unit boundaries, checked element by element.
+CASES += [(8, 20, 512, 64, True), (4, 40, 384, 128, True), (4, 40, 300, 128, False)]
 
 
 @pytest.mark.parametrize("B,H,N,d,causal", CASES,
