@@ -577,14 +577,16 @@ def run_gpu(args, world, rank, local):
     with ClockSampler(local) as clocks:
         t_wall0 = time.perf_counter()
         if big:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(args.steps):
+            # One event between consecutive steps: the total gives the value,
+            # the gaps give the per-step quantiles.
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+            evs[0].record(stream)
+            for i in range(args.steps):
                 step()
-            e1.record(stream)
+                evs[i + 1].record(stream)
             torch.cuda.synchronize()
-            kernel_ms = e0.elapsed_time(e1) / args.steps
+            kernel_ms = evs[0].elapsed_time(evs[-1]) / args.steps
+            step_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
         else:
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
@@ -656,8 +658,9 @@ def run_gpu(args, world, rank, local):
         "device_status": status,
     }
     if step_ms is not None:
-        # Steps timed one by one (L2 flushed before each): quantiles of the
-        # step time and the achieved bandwidth of the algorithmic bytes.
+        # Per-step times (L2 flushed before each step, or inputs larger than
+        # L2 back to back): quantiles of the step time and the achieved
+        # bandwidth of the algorithmic bytes.
         def quantile(f):
             return step_ms[min(len(step_ms) - 1, int(f * len(step_ms)))]
         line["step_quantiles_ms"] = {"p20": quantile(0.2), "p50": quantile(0.5),
