@@ -84,6 +84,10 @@ struct BBars {
     // dP^T of the tile computed (s_full then means S^T computed).
     uint64_t p1_full, dp_full;
     uint64_t dp_free;  // dq: the elementwise pass holds dP in registers
+    // dkdv: per warpgroup, its four warps have stored lse and D of the tile
+    // (a bounded wait, unlike a hardware barrier, cannot hang if a warp has
+    // left the loop after a timed-out wait).
+    uint64_t grp[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -527,7 +531,7 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
     const int r = warp * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     constexpr int kHalfChunks = kTile / 64;  // 32-column chunks per half
-    uint32_t s_phase = 0, of_phase = 0, dp_phase = 0;
+    uint32_t s_phase = 0, of_phase = 0, dp_phase = 0, grp_phase = 0;
     int xbuf = 0;
     bool ok = true;
     for (int rr = 0; ok; ++rr) {
@@ -547,7 +551,7 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
         for (int t = lo; ok && t < hi; ++t) {
             if (kDkDv) {
                 // lse and D of this warpgroup's 64 queries of tile t, shared
-                // through smem (double-buffered; a barrier of the warpgroup
+                // through smem (double-buffered; an mbarrier of the warpgroup
                 // alone publishes them, so the two warpgroups never wait for
                 // each other here): threads 0-63 fetch lse, 64-127 fetch D.
                 const int q = half * 64 + (r & 63);
@@ -556,10 +560,13 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
                     x.lse2[xbuf][q] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
                 else
                     x.dd[xbuf][q] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
-                if (half == 0)
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                else
-                    asm volatile("bar.sync 2, 128;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&b.grp[half]));
+                ok = mbar_wait(smem_addr(&b.grp[half]), grp_phase, kWaitLimitNs, abort);
+                grp_phase ^= 1;
+                if (!ok)
+                    break;
             }
             ok = mbar_wait(smem_addr(&b.s_full), s_phase, kWaitLimitNs, abort);
             s_phase ^= 1;
@@ -806,6 +813,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&b.p1_full), kElemWarps);
         mbar_init(smem_addr(&b.dp_full), 1);
         mbar_init(smem_addr(&b.dp_free), kElemWarps);
+        mbar_init(smem_addr(&b.grp[0]), kElemWarps / 2);
+        mbar_init(smem_addr(&b.grp[1]), kElemWarps / 2);
         mbar_init(smem_addr(&b.drain), 1);
         b.abort = 0;
         fence_barrier_init();
