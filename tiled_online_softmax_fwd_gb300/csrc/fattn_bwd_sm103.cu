@@ -548,18 +548,29 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
             my_lse2 = p.lse[head + row] * kLog2e;
             my_d = p.dvec[head + row];
         }
+        // dkdv: lse and D of this warpgroup's 64 queries of a tile (threads
+        // 0-63 take lse, 64-127 take D), fetched one tile ahead so that the
+        // global loads are in flight while the previous tile runs (nothing
+        // uses the loaded value until the next tile: no arithmetic on it
+        // here, which would wait for the load at once).
+        const int xq = half * 64 + (r & 63);
+        const float *xsrc = (r < 64 ? p.lse : p.dvec) + head;
+        auto fetch = [&](int tt) {
+            const int qrow = tt * kTile + xq;
+            return qrow < p.N ? xsrc[qrow] : 0.f;
+        };
+        float xnext = (kDkDv && lo < hi) ? fetch(lo) : 0.f;
         for (int t = lo; ok && t < hi; ++t) {
             if (kDkDv) {
-                // lse and D of this warpgroup's 64 queries of tile t, shared
-                // through smem (double-buffered; an mbarrier of the warpgroup
-                // alone publishes them, so the two warpgroups never wait for
-                // each other here): threads 0-63 fetch lse, 64-127 fetch D.
-                const int q = half * 64 + (r & 63);
-                const int qrow = t * kTile + q;
+                // Shared through smem as -lse*log2e and -D (double-buffered;
+                // an mbarrier of the warpgroup alone publishes them, so the
+                // two warpgroups never wait for each other here).
                 if (r < 64)
-                    x.lse2[xbuf][q] = qrow < p.N ? -p.lse[head + qrow] * kLog2e : 0.f;
+                    x.lse2[xbuf][xq] = -xnext * kLog2e;
                 else
-                    x.dd[xbuf][q] = qrow < p.N ? -p.dvec[head + qrow] : 0.f;
+                    x.dd[xbuf][xq] = -xnext;
+                if (t + 1 < hi)
+                    xnext = fetch(t + 1);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&b.grp[half]));
