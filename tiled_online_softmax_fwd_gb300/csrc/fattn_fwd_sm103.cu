@@ -1222,7 +1222,10 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
 //   O   = sum_s w_s O_s,  w_s = 2^lr_s / sum_s' 2^lr_s'
 // Slots with no key tile for the row's Q tile are skipped (the same ranges
 // as unit_at / cta_unit).  One warp per row; lane l owns D/32 consecutive
-// columns.
+// columns.  Blocks of four rows: with the registers a batch of eight slots
+// needs, 128-thread blocks fill the SMs' warp slots where 256-thread ones
+// left a partial second wave.  Each slot's range is computed on its own, so
+// the loads of a batch do not wait on one another's index arithmetic.
 //
 // Key-tile range [j0, je) of partial slot sp of head bh's pair (false: no
 // such slot).
@@ -1247,17 +1250,24 @@ __device__ __forceinline__ bool slot_range(const Params &p, int bh, int fmax, in
 }
 
 template <int D, bool kF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
     combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_l, const Params p)
 {
     constexpr int kCols = D / 32;
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+    const long long row = static_cast<long long>(blockIdx.x) * 4 + threadIdx.x / 32;
     const long long rows = static_cast<long long>(p.BH) * p.Nq;
     if (row >= rows)
         return;
     const int lane = threadIdx.x & 31;
-    const int bh = static_cast<int>(row / p.Nq);
-    const int i = static_cast<int>(row % p.Nq);
+    int bh, i;
+    if (rows <= 0x7fffffffLL) {  // 32-bit division
+        const uint32_t r32 = static_cast<uint32_t>(row), nq = static_cast<uint32_t>(p.Nq);
+        bh = static_cast<int>(r32 / nq);
+        i = static_cast<int>(r32 - static_cast<uint32_t>(bh) * nq);
+    } else {
+        bh = static_cast<int>(row / p.Nq);
+        i = static_cast<int>(row % p.Nq);
+    }
     const int qt = i / kBM, pair = p.single ? qt : qt / 2;
     const int fmax = unit_tiles(p, pair), fown = key_tiles(p, qt);
     // Launched as a programmatic dependent of the forward grid: wait for it
@@ -1384,14 +1394,14 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
         return e;
     const long long rows = static_cast<long long>(p.BH) * p.Nq;
-    const long long blocks = (rows + 7) / 8;
+    const long long blocks = (rows + 3) / 4;
     if (blocks > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     // Programmatic dependent launch: the merge grid is set up while the
     // forward grid drains and waits for it in griddepcontrol.wait.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
