@@ -1224,8 +1224,7 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
 // as unit_at / cta_unit).  One warp per row; lane l owns D/32 consecutive
 // columns.  Blocks of four rows: with the registers a batch of eight slots
 // needs, 128-thread blocks fill the SMs' warp slots where 256-thread ones
-// left a partial second wave.  Each slot's range is computed on its own, so
-// the loads of a batch do not wait on one another's index arithmetic.
+// left a partial second wave.
 //
 // Key-tile range [j0, je) of partial slot sp of head bh's pair (false: no
 // such slot).
@@ -1273,47 +1272,58 @@ __global__ void __launch_bounds__(128)
     // Launched as a programmatic dependent of the forward grid: wait for it
     // to finish (and its partials to be visible) before reading them.
     grid_dependency_wait();
-    // Online merge over the slots, kBatch at a time: all loads of a batch are
-    // issued before any of them is used.  A slot whose range held no key of
-    // this row (l = 0, partial lse -inf) contributes nothing.
+    // Online merge over the slots in slot order.  The slots' key ranges depend
+    // only on the row's Q tile: each lane works out one slot of a group of 32,
+    // and a ballot gives the group's slots that hold keys of this row; only
+    // those are read, kBatch loads issued before any of them is used.  A slot
+    // whose range held no key of this row (l = 0, partial lse -inf, possible
+    // in the decode shape) contributes nothing.
     constexpr int kBatch = 8;
     float mx_e = -INFINITY, mx_r = -INFINITY, se = 0.f, sr = 0.f;
     float acc[kCols];
 #pragma unroll
     for (int c = 0; c < kCols; ++c)
         acc[c] = 0.f;
-    bool more = true;
-    for (int sp0 = 0; more; sp0 += kBatch) {
-        float2 ll[kBatch];
-        float o[kBatch][kCols];
+    for (int sg = 0;; sg += 32) {
+        int j0 = 0, je = 0;
+        const bool exists = slot_range(p, bh, fmax, sg + lane, j0, je);
+        unsigned live = __ballot_sync(0xffffffffu, exists && min(je, fown) > j0);
+        // Slots exist up to a count, so a group with a missing slot is the last.
+        const bool last = __ballot_sync(0xffffffffu, exists) != 0xffffffffu;
+        while (live != 0) {
+            float2 ll[kBatch];
+            float o[kBatch][kCols];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            int j0 = 0, je = 0;
-            more = more && slot_range(p, bh, fmax, sp0 + u, j0, je);
-            ll[u] = make_float2(-INFINITY, -INFINITY);
-            if (more && min(je, fown) > j0) {
-                const size_t srow = static_cast<size_t>(sp0 + u) * rows + row;
-                ll[u] = ws_l[srow];
-                const float *src = ws_o + srow * D + lane * kCols;
+            for (int u = 0; u < kBatch; ++u) {
+                ll[u] = make_float2(-INFINITY, -INFINITY);
+                if (live != 0) {
+                    const int sp = sg + __ffs(live) - 1;
+                    live &= live - 1;
+                    const size_t srow = static_cast<size_t>(sp) * rows + row;
+                    ll[u] = ws_l[srow];
+                    const float *src = ws_o + srow * D + lane * kCols;
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c)
+                        o[u][c] = src[c];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (ll[u].x == -INFINITY)
+                    continue;
+                const float ne = fmaxf(mx_e, ll[u].x), nr = fmaxf(mx_r, ll[u].y);
+                se = se * ex2(mx_e - ne) + ex2(ll[u].x - ne);
+                const float a = ex2(mx_r - nr), w = ex2(ll[u].y - nr);
+                sr = sr * a + w;
 #pragma unroll
                 for (int c = 0; c < kCols; ++c)
-                    o[u][c] = src[c];
+                    acc[c] = fmaf(w, o[u][c], acc[c] * a);
+                mx_e = ne;
+                mx_r = nr;
             }
         }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            if (ll[u].x == -INFINITY)
-                continue;
-            const float ne = fmaxf(mx_e, ll[u].x), nr = fmaxf(mx_r, ll[u].y);
-            se = se * ex2(mx_e - ne) + ex2(ll[u].x - ne);
-            const float a = ex2(mx_r - nr), w = ex2(ll[u].y - nr);
-            sr = sr * a + w;
-#pragma unroll
-            for (int c = 0; c < kCols; ++c)
-                acc[c] = fmaf(w, o[u][c], acc[c] * a);
-            mx_e = ne;
-            mx_r = nr;
-        }
+        if (last)
+            break;
     }
     const float inv = 1.f / sr;
     uint16_t *dst = static_cast<uint16_t *>(p.o) + (bh / p.H) * p.o_sb + (bh % p.H) * p.o_sh +
