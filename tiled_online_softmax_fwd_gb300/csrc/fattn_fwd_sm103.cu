@@ -97,6 +97,10 @@ struct Cfg {
     static constexpr bool kOnes = !kF16 && D == 64;
     static constexpr uint32_t kOnesOffset = (kQTiles + kStages) * kTileBytes;
     static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
+    // Epilogue staging of the one-tile kernel: 4 KB (32 rows x 128 bytes) for
+    // each of its 4 softmax warps.
+    static constexpr uint32_t kStageOffset = kTilesBytes;
+    static constexpr uint32_t kBarsOffset = kStageOffset + (kQTiles == 1 ? 4 * 4096 : 0);
     static constexpr uint32_t kON = D + (kOnes ? 16 : 0);  // O accumulator columns
     // P V in two halves (keys 0-63 as soon as their P is written): faster at
     // d = 64, where the softmax dominates (1101 -> 1148 TFLOP/s on B2 H8
@@ -649,10 +653,39 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
     }
 }
 
+// Staged row stores (the one-tile kernel, where the epilogue holds up the
+// next unit: the tensor cores have no second Q tile to work on meanwhile).
+// Thread r of a warp (row r of the warp's 32) puts a 128-byte piece of its row
+// into row r of the warp's staging area, 16-byte granule g at position
+// g ^ (r % 8), so the 8 threads of a store phase hit 8 different bank groups;
+// then 8 lanes per row copy the pieces out as whole 128-byte lines, 4 rows per
+// instruction, instead of 32 rows' 16-byte pieces per instruction.
+__device__ __forceinline__ void stage_put(uint8_t *stage, int lane, int g, uint4 v)
+{
+    reinterpret_cast<uint4 *>(stage + lane * 128)[g ^ (lane & 7)] = v;
+}
+
+__device__ __forceinline__ void stage_flush(const uint8_t *stage, int lane, char *dst0,
+                                            long long row_bytes, int live_rows)
+{
+    __syncwarp();
+    const int g = lane % 8;
+#pragma unroll
+    for (int pass = 0; pass < 8; ++pass) {
+        const int rr = pass * 4 + lane / 8;
+        const uint4 x = reinterpret_cast<const uint4 *>(stage + rr * 128)[g ^ (rr & 7)];
+        if (rr < live_rows)
+            *reinterpret_cast<uint4 *>(dst0 + rr * row_bytes + g * 16) = x;
+    }
+    __syncwarp();
+}
+
 // Epilogue of one row after the unit's last P V: O / l_round in bf16 (fp16)
 // and lse = ln2 * (m + log2 l); in split mode the fp32 partial O and the two
-// base-2 partial lse go to the workspace instead, for the combine kernel.
-template <int D, bool kF16, bool kOnes>
+// base-2 partial lse go to the workspace instead, for the combine kernel.  kStaged:
+// through the staging area (warp w, among the CTA's first warps, uses its
+// w-th 4 KB), for D a multiple of 64.
+template <int D, bool kF16, bool kOnes, bool kStaged = false>
 __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uint32_t t_o, int row,
                                              float m, float l, float l_round)
 {
@@ -667,7 +700,57 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
     const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
     const bool live = row < p.Nq;
     const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
-    if (p.splits == 1) {
+    if constexpr (kStaged) {
+        static_assert(D % 64 == 0, "staged rows are whole 128-byte pieces");
+        extern __shared__ __align__(1024) uint8_t smem_raw[];
+        const uint32_t raw = smem_addr(smem_raw);
+        uint8_t *stage = smem_raw + (((raw + 1023u) & ~1023u) - raw) +
+                         Cfg<D, kF16>::kStageOffset + (threadIdx.x / 32) * 4096;
+        const int lane = threadIdx.x & 31;
+        const int row0 = row - lane;  // the warp's first row
+        const int live_rows = min(32, p.Nq - row0);
+        if (p.splits == 1) {  // 64 columns (128 bytes) a piece
+            char *dst0 = reinterpret_cast<char *>(
+                static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb + (u.bh % p.H) * p.o_sh +
+                static_cast<long long>(row0) * p.o_sn);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(t_o + c * 32, o);
+                tmem_wait_ld();
+                auto f = [&](int i) { return __uint_as_float(o[i]) * inv_l; };
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    stage_put(stage, lane, (c % 2) * 4 + i,
+                              make_uint4(pack2<kF16>(f(8 * i), f(8 * i + 1)),
+                                         pack2<kF16>(f(8 * i + 2), f(8 * i + 3)),
+                                         pack2<kF16>(f(8 * i + 4), f(8 * i + 5)),
+                                         pack2<kF16>(f(8 * i + 6), f(8 * i + 7))));
+                if (c % 2 == 1)
+                    stage_flush(stage, lane, dst0 + (c / 2) * 128, p.o_sn * 2, live_rows);
+            }
+            if (live)
+                p.lse[grow] = (m + log2f(l)) * kLn2;
+        } else {  // 32 fp32 columns (128 bytes) a piece
+            const size_t srow0 = static_cast<size_t>(u.split) * p.BH * p.Nq + grow - lane;
+            char *dst0 = reinterpret_cast<char *>(p.ws_o + srow0 * D);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(t_o + c * 32, o);
+                tmem_wait_ld();
+                auto f = [&](int i) { return __float_as_uint(__uint_as_float(o[i]) * inv_l); };
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    stage_put(stage, lane, i, make_uint4(f(4 * i), f(4 * i + 1), f(4 * i + 2), f(4 * i + 3)));
+                stage_flush(stage, lane, dst0 + c * 128, static_cast<long long>(D) * 4, live_rows);
+            }
+            if (live)
+                p.ws_l[srow0 + lane] = make_float2(m + log2f(l), m + log2f(l_norm));
+        }
+    } else if (p.splits == 1) {
         uint16_t *orow = static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb +
                          (u.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
 #pragma unroll 1
@@ -834,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t smem_base = (raw + 1023u) & ~1023u;
-    Bars &b = *reinterpret_cast<Bars *>(smem_raw + (smem_base - raw) + C::kTilesBytes);
+    Bars &b = *reinterpret_cast<Bars *>(smem_raw + (smem_base - raw) + C::kBarsOffset);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
 
@@ -1131,7 +1214,7 @@ __device__ void run_softmax_single(const Params &p, Bars &b, uint32_t tmem)
         if (!ok)
             break;
         tc_fence_after();
-        epilogue_row<D, kF16, C::kOnes>(p, u, t_o, row, m, l, l_round);
+        epilogue_row<D, kF16, C::kOnes, true>(p, u, t_o, row, m, l, l_round);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -1150,7 +1233,7 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t smem_base = (raw + 1023u) & ~1023u;
-    Bars &b = *reinterpret_cast<Bars *>(smem_raw + (smem_base - raw) + C::kTilesBytes);
+    Bars &b = *reinterpret_cast<Bars *>(smem_raw + (smem_base - raw) + C::kBarsOffset);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
 
@@ -1383,7 +1466,7 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
         return cudaErrorInvalidConfiguration;
     p.units = static_cast<int>(min(units, 0x7fffffffLL));
     p.sl2 = a.scale * kLog2e;
-    const size_t smem = C::kTilesBytes + sizeof(Bars) + 1024;
+    const size_t smem = C::kBarsOffset + sizeof(Bars) + 1024;
     cudaError_t e;
     if constexpr (D == 256)
         e = cudaFuncSetAttribute(fwd_single_kernel<D, kF16>,
