@@ -52,7 +52,9 @@ __global__ void __launch_bounds__(1024, 1) mufu_kernel(float seed, unsigned long
 // One thread issues `iters` rounds of MMAs of one mode; with `stream_tmem`
 // warps 2..9 meanwhile load 128 TMEM columns and store 64 per round, as the
 // softmax does.  Modes: 0 S (SS 128x128, K = 128), 1 P V (TS 128x128,
-// K = 128), 2 both, 3 SS 128x256, 4 P V with N = 64, 5 P V with N = 80.
+// K = 128), 2 both, 3 SS 128x256, 4 P V with N = 64, 5 P V with N = 80,
+// 6 and 7 the same two P V shapes with P read from shared memory (SS; A laid
+// out like Q in mode 0, B like V in modes 4 and 5).
 __global__ void __launch_bounds__(320, 1) mma_kernel(int mode, int iters, int stream_tmem,
                                                      unsigned long long *cycles)
 {
@@ -135,6 +137,13 @@ __global__ void __launch_bounds__(320, 1) mma_kernel(int mode, int iters, int st
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + 256, tmem + 128 + kk * 8, smem_desc(b + kk * 2048, kBox, 1024),
                            id_pv80, 1);
+            if (mode == 6 || mode == 7)
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                    mma_ss(tmem + 256, smem_desc(a + off, 16, 1024),
+                           smem_desc(b + kk * 2048, mode == 6 ? 1024 : kBox, 1024),
+                           mode == 6 ? id_pv64 : id_pv80, 1);
+                }
         }
         mma_commit(smem_addr(&done));
         const bool ok = mbar_wait(smem_addr(&done), 0, 2000000000ull, nullptr);
@@ -186,11 +195,13 @@ int main()
     const int smem = kBoxes * kBox + 1024;
     cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     const char *names[] = {"s_ss_128x128x16", "pv_ts_128x128x16", "s_and_pv", "s_ss_128x256x16",
-                           "pv_ts_128x64x16", "pv_ts_128x80x16"};
+                           "pv_ts_128x64x16", "pv_ts_128x80x16", "pv_ss_128x64x16",
+                           "pv_ss_128x80x16"};
     const double flops[] = {128.0 * 128 * 32, 128.0 * 128 * 32, 128.0 * 128 * 32,
-                            128.0 * 256 * 32, 128.0 * 64 * 32,  128.0 * 80 * 32};
+                            128.0 * 256 * 32, 128.0 * 64 * 32,  128.0 * 80 * 32,
+                            128.0 * 64 * 32,  128.0 * 80 * 32};
     for (int stream_tmem = 0; stream_tmem < 2; ++stream_tmem)
-        for (int mode = 0; mode < 6; ++mode) {
+        for (int mode = 0; mode < 8; ++mode) {
             if (stream_tmem && mode != 2)
                 continue;
             const int iters = 2000;
