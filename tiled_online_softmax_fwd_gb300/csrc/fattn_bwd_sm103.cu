@@ -84,6 +84,13 @@ struct BBars {
     // dP^T of the tile computed (s_full then means S^T computed).
     uint64_t p1_full, dp_full;
     uint64_t dp_free;  // dq: the elementwise pass holds dP in registers
+    // dq: dS of the CTA's n-th key tile written (all eight warps), on
+    // dq_full[n % 2].  dP is released early (dp_free), so a warp can finish
+    // tile n and write dS of tile n + 1 while another still writes dS of
+    // tile n; one barrier would then complete tile n's phase with arrivals
+    // of tile n + 1.  The skew is at most one tile (tile n + 2 needs dP of
+    // n + 1 released by every warp), so two barriers keep the tiles apart.
+    uint64_t dq_full[2];
     // dkdv: per warpgroup, its four warps have stored lse and D of the tile
     // (a bounded wait, unlike a hardware barrier, cannot hang if a warp has
     // left the loop after a timed-out wait).
@@ -332,6 +339,7 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
     uint32_t res_phase = 0, s_phase = 0, oe_phase = 0, dp_phase = 0, pos = 0;
+    uint32_t n_tile = 0;  // dq: key tiles of this CTA so far (dq_full[n % 2])
     bool ok = true;
     auto commit = [&](uint64_t &bar) {
         if (leader)
@@ -420,8 +428,8 @@ __device__ void bwd_mma(const BParams &p, BBars &b, uint32_t smem, uint32_t tmem
                     if (t + 1 == hi - 1)
                         commit(b.res_empty);  // resident pair no longer read
                 }
-                ok = warp_wait(smem_addr(&b.p_full), s_phase, abort);
-                s_phase ^= 1;
+                ok = warp_wait(smem_addr(&b.dq_full[n_tile & 1]), (n_tile >> 1) & 1, abort);
+                ++n_tile;
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -532,6 +540,7 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     constexpr int kHalfChunks = kTile / 64;  // 32-column chunks per half
     uint32_t s_phase = 0, of_phase = 0, dp_phase = 0, grp_phase = 0;
+    uint32_t n_tile = 0;  // dq: key tiles of this CTA so far (dq_full[n % 2])
     int xbuf = 0;
     bool ok = true;
     for (int rr = 0; ok; ++rr) {
@@ -744,7 +753,8 @@ __device__ void bwd_elem(const BParams &p, BBars &b, BXch &x, uint32_t tmem)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_addr(&b.p_full));
+                mbar_arrive(smem_addr(kDkDv ? &b.p_full : &b.dq_full[n_tile & 1]));
+            ++n_tile;
             xbuf ^= 1;
         }
         if (!ok)
@@ -824,6 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&b.p1_full), kElemWarps);
         mbar_init(smem_addr(&b.dp_full), 1);
         mbar_init(smem_addr(&b.dp_free), kElemWarps);
+        mbar_init(smem_addr(&b.dq_full[0]), kElemWarps);
+        mbar_init(smem_addr(&b.dq_full[1]), kElemWarps);
         mbar_init(smem_addr(&b.grp[0]), kElemWarps / 2);
         mbar_init(smem_addr(&b.grp[1]), kElemWarps / 2);
         mbar_init(smem_addr(&b.drain), 1);
