@@ -5,22 +5,31 @@ method is held to:
         upcast, minus the fp64 oracle)
   lse : max |delta| <= 1e-3
 
-Reading of the O bound for a bf16 output.  Where one bf16 ulp of the exact
-value is coarser than the bound -- |O_ref| >= 2, where neighbouring bf16
-numbers are 2^-6 = 0.0156 apart or more -- no finite-precision kernel can
-promise 1e-2: it would have to round correctly even when the exact value sits
-next to a rounding midpoint.  There the bound is read as faithful rounding,
-|delta| < 1 ulp(O_ref) (one of the two bf16 neighbours of the exact value).
-Every element with |O_ref| < 2 is held to |delta| <= 1e-2 as stated.  The
-split depends only on the oracle's value, never on the GPU's output, and the
-plain maximum over all elements is reported next to it ("o_max_all").
+Reading of the O bounds for a bf16 output.  The output is rounded to bf16
+("Triton hand-written kernels: vector add -> tiled GEMM -> FlashAttention
+core", section 4, stores O in the 16-bit input type), so even the correctly
+rounded value of the exact O is off by its rounding floor
+|O_ref - rne_bf16(O_ref)|, up to half a bf16 ulp: 0.0078 for |O| in [2, 4),
+0.0156 for |O| in [4, 8).
 
-The mean bound 1e-3 is applied as stated to the five workloads.  The extra
-cases that exercise masks and ragged tails with very few keys per row have
-outputs of order 1, whose bf16 rounding alone averages close to 1e-3; for
-those (``mean_rule="floor"``) the mean bound is max(1e-3, 2 x the oracle's
-own mean rounding floor), i.e. the kernel may add at most as much error on
-average as the unavoidable output rounding.
+  * Max bound.  An element is exempt from 1e-2 only when its own floor
+    exceeds 1e-2, i.e. when no bf16 number lies within 1e-2 of the exact
+    value.  Such elements are held to one bf16 ulp of O_ref instead (one of
+    the two bf16 neighbours of the exact value).  Every other element --
+    including every element with |O_ref| < 4 -- is held to 1e-2 as stated.
+    The split depends on the oracle's value only, never on the GPU output.
+  * Mean bound.  1e-3 as stated.  The one exception is a case whose output
+    rounding alone uses more than half of it (the oracle's own mean floor
+    > 5e-4: tiny problems whose rows average a handful of keys, so that |O|
+    is of order one); asked for with ``mean_rule="floor"``, such a case is
+    held to max(1e-3, 2 x its mean floor), i.e. the kernel may add at most as
+    much error on average as the unavoidable output rounding.  Below that
+    floor the stated bound applies whatever the caller asked for, so the
+    looser rule is taken case by case from the oracle's floor.
+
+Reported next to the gate: the plain maximum over all elements, the maximum
+over |O_ref| < 2, the number of elements above 1e-2 in all, among the
+non-exempt ones (must be 0) and among |O_ref| in [2, 4).
 """
 from __future__ import annotations
 
@@ -30,6 +39,9 @@ import torch
 O_MAX_TOL = 1e-2
 O_MEAN_TOL = 1e-3
 LSE_MAX_TOL = 1e-3
+# The mean floor above which the output rounding alone takes more than half
+# of the stated mean bound.
+FLOOR_MEAN_LIMIT = O_MEAN_TOL / 2
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
@@ -43,33 +55,44 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(np.floor(np.log2(ax)) - 7)
 
 
+def _np64(x, shape):
+    if isinstance(x, torch.Tensor):
+        x = x.to(torch.float64).cpu().numpy()
+    return np.asarray(x, dtype=np.float64).reshape(shape)
+
+
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, mean_rule: str = "stated") -> dict:
     """o_gpu [R, d] (bf16 tensor or array), lse_gpu [R]; refs in float64."""
-    og = o_gpu.to(torch.float64).cpu().numpy() if isinstance(o_gpu, torch.Tensor) else o_gpu
-    lg = lse_gpu.to(torch.float64).cpu().numpy() if isinstance(lse_gpu, torch.Tensor) else lse_gpu
-    og = np.asarray(og, dtype=np.float64).reshape(o_ref.shape)
-    lg = np.asarray(lg, dtype=np.float64).reshape(lse_ref.shape)
+    og = _np64(o_gpu, o_ref.shape)
+    lg = _np64(lse_gpu, lse_ref.shape)
     delta = np.abs(og - o_ref)
     floor = np.abs(o_ref - bf16_round(o_ref))
-    ulp = bf16_ulp(o_ref)
-    unattainable = ulp > O_MAX_TOL  # |O_ref| >= 2
-    attain_delta = delta[~unattainable]
+    aref = np.abs(o_ref)
+    exempt = floor > O_MAX_TOL
+    gated = delta[~exempt]
+    lt2 = delta[aref < 2]
+    beyond = delta > O_MAX_TOL
     r = {
         "rows": int(o_ref.shape[0]) if o_ref.ndim else 0,
         "finite": bool(np.all(np.isfinite(og)) and np.all(np.isfinite(lg))),
-        "o_max": float(attain_delta.max()) if attain_delta.size else 0.0,
+        "o_max": float(gated.max()) if gated.size else 0.0,
         "o_max_all": float(delta.max()) if delta.size else 0.0,
+        "o_max_lt2": float(lt2.max()) if lt2.size else 0.0,
         "o_mean": float(delta.mean()) if delta.size else 0.0,
         "lse_max": float(np.abs(lg - lse_ref).max()) if lg.size else 0.0,
         "floor_max": float(floor.max()) if floor.size else 0.0,
         "floor_mean": float(floor.mean()) if floor.size else 0.0,
-        "unattainable": int(unattainable.sum()),
-        "unattainable_ulp_ok": bool(np.all(delta[unattainable] < ulp[unattainable])),
-        "beyond_bound": int((delta > O_MAX_TOL).sum()),
+        "exempt": int(exempt.sum()),
+        "exempt_ulp_ok": bool(np.all(delta[exempt] <= bf16_ulp(o_ref[exempt]))),
+        "beyond_bound": int(beyond.sum()),
+        "beyond_bound_gated": int((beyond & ~exempt).sum()),
+        "beyond_bound_2_4": int((beyond & (aref >= 2) & (aref < 4)).sum()),
     }
-    r["mean_tol"] = O_MEAN_TOL if mean_rule == "stated" else max(O_MEAN_TOL, 2 * r["floor_mean"])
+    loose = mean_rule == "floor" and r["floor_mean"] > FLOOR_MEAN_LIMIT
+    r["mean_rule"] = "floor" if loose else "stated"
+    r["mean_tol"] = max(O_MEAN_TOL, 2 * r["floor_mean"]) if loose else O_MEAN_TOL
     r["ok"] = (r["finite"] and r["o_max"] <= O_MAX_TOL and r["o_mean"] <= r["mean_tol"]
-               and r["lse_max"] <= LSE_MAX_TOL and r["unattainable_ulp_ok"])
+               and r["lse_max"] <= LSE_MAX_TOL and r["exempt_ulp_ok"])
     return r
 
 
@@ -79,4 +102,4 @@ def assert_parity(r: dict, what: str = ""):
     tol = r.get("mean_tol", O_MEAN_TOL)
     assert r["o_mean"] <= tol, "%s: O mean|d| %.3e > %.2e (%s)" % (what, r["o_mean"], tol, r)
     assert r["lse_max"] <= LSE_MAX_TOL, "%s: lse max|d| %.3e > %.0e (%s)" % (what, r["lse_max"], LSE_MAX_TOL, r)
-    assert r["unattainable_ulp_ok"], "%s: an element with |O| >= 2 is off by 1 ulp or more (%s)" % (what, r)
+    assert r["exempt_ulp_ok"], "%s: an element with a rounding floor > 1e-2 is off by more than 1 ulp (%s)" % (what, r)

@@ -4,13 +4,13 @@ import numpy as np
 from tests.parity import bf16_round, bf16_ulp, compare
 
 
-def _case(o_ref_vals, o_gpu_vals, lse_delta=0.0, pad=200):
+def _case(o_ref_vals, o_gpu_vals, lse_delta=0.0, pad=200, mean_rule="stated"):
     """One row; `pad` exactly represented elements dilute the mean so that
     the max rules can be probed on their own."""
     o_ref = np.array(list(o_ref_vals) + [0.25] * pad, dtype=np.float64).reshape(1, -1)
     o_gpu = np.array(list(o_gpu_vals) + [0.25] * pad, dtype=np.float64).reshape(1, -1)
     lse_ref = np.zeros(1)
-    return compare(o_gpu, lse_ref + lse_delta, o_ref, lse_ref)
+    return compare(o_gpu, lse_ref + lse_delta, o_ref, lse_ref, mean_rule=mean_rule)
 
 
 def test_bf16_helpers():
@@ -22,7 +22,7 @@ def test_bf16_helpers():
 
 
 def test_exact_bf16_output_passes():
-    ref = [0.1234, -1.75, 2.3542, -4.1776]
+    ref = [0.1234, -1.75, 2.3542, -4.1776, 5.0115]
     r = _case(ref, bf16_round(np.array(ref)))
     assert r["ok"], r
 
@@ -34,15 +34,44 @@ def test_bound_is_absolute_below_two():
     assert r["ok"]
 
 
-def test_faithful_rounding_at_or_above_two():
-    # |O| >= 2: one ulp (>= 0.0156) is coarser than 1e-2; either bf16
-    # neighbour of the exact value is accepted, nothing farther.
-    r = _case([-2.3542], [-2.34375])           # the other neighbour, |d| = 0.0104
-    assert r["ok"] and r["beyond_bound"] == 1 and r["o_max"] == 0.0
-    r = _case([-2.3542], [-2.3542 + 2 ** -6])  # a full ulp away
-    assert not r["ok"]
-    r = _case([4.1776], [4.1776 + 0.03])       # ulp = 2^-5 = 0.03125
-    assert r["ok"]
+def test_two_to_four_is_held_to_the_stated_bound():
+    # Neighbours of 2.3542 are 2.34375 (0.0104 away) and 2.359375 (0.0052):
+    # its floor is 0.0052 <= 1e-2, so only the near one passes.
+    r = _case([-2.3542], [-2.359375])
+    assert r["ok"] and r["exempt"] == 0
+    r = _case([-2.3542], [-2.34375])
+    assert not r["ok"] and r["beyond_bound_gated"] == 1 and r["beyond_bound_2_4"] == 1
+    # 2.0070: both neighbours (2.0 at 0.0070, 2.015625 at 0.0086) are within 1e-2.
+    assert _case([2.0070], [2.0])["ok"]
+    assert _case([2.0070], [2.015625])["ok"]
+
+
+def test_exempt_only_where_the_floor_exceeds_the_bound():
+    # 4.0115: nearest bf16 is 4.0, 0.0115 away, so no bf16 output meets 1e-2;
+    # held to one ulp (2^-5) instead: either neighbour passes, nothing farther.
+    r = _case([4.0115], [4.0])
+    assert r["ok"] and r["exempt"] == 1 and r["beyond_bound"] == 1 and r["o_max"] == 0.0
+    assert _case([4.0115], [4.03125])["ok"]
+    assert not _case([4.0115], [4.0625])["ok"]
+    # 4.005: floor 0.005, so the far neighbour (0.026 away) fails.
+    r = _case([4.005], [4.03125])
+    assert not r["ok"] and r["exempt"] == 0 and r["beyond_bound_gated"] == 1
+    assert _case([4.005], [4.0])["ok"]
+
+
+def test_mean_rule_follows_the_oracle_floor():
+    # Every element of order one, off by 1.5e-3: the stated mean bound fails.
+    ref = np.linspace(0.3, 0.9, 64) + 1e-3 / 3
+    gpu = ref + 1.5e-3
+    r = _case(ref, gpu, pad=0)
+    assert not r["ok"] and r["mean_rule"] == "stated"
+    # Asked for the floor rule, such a case gets it only when its own mean
+    # floor is above 5e-4.
+    r = _case(ref, gpu, pad=0, mean_rule="floor")
+    assert r["floor_mean"] > 5e-4 and r["mean_rule"] == "floor" and r["ok"], r
+    small = np.linspace(0.01, 0.06, 64) + 1e-5
+    r = _case(small, small + 1.5e-3, pad=0, mean_rule="floor")
+    assert r["floor_mean"] <= 5e-4 and r["mean_rule"] == "stated" and not r["ok"]
 
 
 def test_lse_and_mean_bounds():

@@ -62,10 +62,9 @@ class Workload:
 WORKLOADS = {
     "B1_H1_N256_d64": Workload("B1_H1_N256_d64", 1, 1, 256, 64, False, 0),
     "B1_H1_N4096_d64": Workload("B1_H1_N4096_d64", 1, 1, 4096, 64, False, 1),
-    "B4_H16_N4096_d128_causal": Workload("B4_H16_N4096_d128_causal", 4, 16, 4096, 128, True, 2,
-                                         rows_per_head=512),
+    "B4_H16_N4096_d128_causal": Workload("B4_H16_N4096_d128_causal", 4, 16, 4096, 128, True, 2),
     "B1_H32_N16384_d128_causal_sigma3": Workload("B1_H32_N16384_d128_causal_sigma3", 1, 32, 16384,
-                                                 128, True, 3, sigma_qk=3.0, rows_per_head=1024),
+                                                 128, True, 3, sigma_qk=3.0),
     "B2_H8_N65536_d64": Workload("B2_H8_N65536_d64", 2, 8, 65536, 64, False, 4,
                                  rows_per_head=1024),
 }
@@ -167,14 +166,17 @@ def sample_rows(B: int, H: int, N: int, per_head: int, generator: torch.Generato
     return torch.cat(out) if out else torch.zeros(0, dtype=torch.int64)
 
 
-def make_workload(w: Workload, dtype=torch.bfloat16):
+def make_workload(w: Workload, dtype=torch.bfloat16, sample_per_head: int | None = None):
     """q, k, v (bf16 unless ``dtype`` says otherwise, CPU) and the checked row
-    ids (None when all rows are checked)."""
+    ids (None when all rows are checked).  ``sample_per_head`` asks for that
+    many seeded rows per head instead, drawn the same way (timing samples and
+    checks that cannot afford every row)."""
     g = torch.Generator("cpu").manual_seed(w.seed)
     q, k, v = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, generator=g, dtype=dtype)
+    per = sample_per_head if sample_per_head is not None else w.rows_per_head
     rows = None
-    if w.rows_per_head is not None:
-        rows = sample_rows(w.B, w.H, w.N, w.rows_per_head, g)
+    if per is not None:
+        rows = sample_rows(w.B, w.H, w.N, per, g)
     return q, k, v, rows
 
 
