@@ -56,7 +56,8 @@ typedef enum fattn_status {
     FATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, misalignment, overlap */
     FATTN_ERR_UNSUPPORTED = 2, /* d not supported by the call, tensor too large, device is not sm_103 */
     FATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; see fattn_last_cuda_error() */
-    FATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a pipeline wait (see fattn_get_device_status) */
+    FATTN_ERR_TIMEOUT = 4,     /* a kernel gave up on a pipeline wait (see fattn_get_device_status) */
+    FATTN_ERR_RANGE = 5        /* a non-finite output row, e.g. from |V| >= 65520 (see attn_fwd) */
 } fattn_status_t;
 
 /*
@@ -71,6 +72,20 @@ typedef enum fattn_status {
  *   scale   : multiplies Q.K before masking and softmax (usually 1/sqrt(d))
  *   causal  : 1 keeps keys j <= i for query i, 0 keeps all keys
  *   stream  : CUDA stream the kernel is enqueued on
+ *
+ * Precision.  Scores, row max, row sums and the output accumulator are fp32.
+ * P, the probabilities that enter the second product, is rounded to fp16 (not
+ * to bf16, the inputs' type): with bf16 P the bf16 output misses the stated
+ * 1e-2 bound on peaked rows whose |O| is in [2, 4), where one bf16 ulp is
+ * 0.0156 and P's rounding moves O across a rounding midpoint.  Both operands
+ * of a tensor-core product share one type, so each V tile is converted to
+ * fp16 on chip.  That is exact for |v| < 65520; a V element of larger
+ * magnitude becomes infinite in the product.  Any output row that comes out
+ * non-finite -- from such a V element, or from non-finite inputs -- makes
+ * the kernel record FATTN_ERR_RANGE in the device status word (those rows
+ * of o are then not meaningful).  For V beyond that range use
+ * attn_fwd_strided with dtype 2 (P in bf16).  O is divided by the fp32 row
+ * sum and rounded to bf16 (nearest even).
  *
  * Returns FATTN_OK once the kernel is enqueued, or an error status without
  * enqueuing anything.  A pipeline timeout inside the kernel is not reported
@@ -228,8 +243,12 @@ size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causa
  * (checked by nesting: its strides sorted by size, each at least the span
  * of the smaller dimensions) and o must not overlap q, k, v or lse (checked
  * over each tensor's address span).  lse stays contiguous fp32 [B][H][Nq].
- * dtype: 0 = bf16 q, k, v, o; 1 = fp16 (as attn_fwd_fp16: P rounded to fp16,
- * O normalised by the fp32 sum); anything else gives FATTN_ERR_INVALID_ARG.
+ * dtype: 0 = bf16 q, k, v, o (P in fp16, as attn_fwd); 1 = fp16 (as
+ * attn_fwd_fp16: P rounded to fp16, O normalised by the fp32 sum); 2 = bf16
+ * with P rounded to bf16, for V of any bf16 magnitude (O normalised by the row
+ * sum of the rounded P, so the rounding of each tile's largest p cancels; its
+ * bf16 output can miss the 1e-2 bound by up to one ulp where |O| >= 2);
+ * anything else gives FATTN_ERR_INVALID_ARG.
  * Everything else -- shapes, the causal alignment, num_splits, the workspace
  * (attn_fwd_kv_workspace_size) and the errors -- is attn_fwd_kv's.  A
  * stride array that is NULL gives FATTN_ERR_INVALID_ARG.
@@ -307,10 +326,16 @@ int fattn_last_cuda_error(void);
  * current device, after synchronising `stream`.
  *
  * *status receives 0 when no kernel reported a problem since the last read,
- * otherwise a nonzero code: bits 0..7 = FATTN_ERR_TIMEOUT, bits 8..15 = the
- * role that gave up (1 load, 2 mma, 3 softmax, 4 epilogue, 5 self-test),
- * bits 16..31 = the CTA index.  Returns FATTN_ERR_TIMEOUT if *status is nonzero, FATTN_OK if it
- * is zero, or FATTN_ERR_INVALID_ARG / FATTN_ERR_CUDA.
+ * otherwise the first code recorded: bits 0..7 = FATTN_ERR_TIMEOUT or
+ * FATTN_ERR_RANGE, bits 8..15 = the role that reported it (1 load, 2 mma,
+ * 3 softmax, 4 epilogue, 5 self-test, 6 V conversion), bits 16..31 = the CTA
+ * index.  Returns the status in bits 0..7 (FATTN_ERR_TIMEOUT or
+ * FATTN_ERR_RANGE) if *status is nonzero, FATTN_OK if it is zero, or
+ * FATTN_ERR_INVALID_ARG / FATTN_ERR_CUDA.
+ *
+ * The library keeps per-device state for the life of the process (the
+ * helper streams of attn_fwd_host, the scratch address of
+ * attn_fwd_split_noalloc); it is not valid after cudaDeviceReset.
  */
 fattn_status_t fattn_get_device_status(int *status, struct CUstream_st *stream);
 

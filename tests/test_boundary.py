@@ -53,6 +53,7 @@ def test_status_strings_and_version(lib):
     assert lib.fattn_status_string(0) == b"FATTN_OK"
     assert lib.fattn_status_string(1) == b"FATTN_ERR_INVALID_ARG"
     assert lib.fattn_status_string(4) == b"FATTN_ERR_TIMEOUT"
+    assert lib.fattn_status_string(5) == b"FATTN_ERR_RANGE"
     assert lib.fattn_status_string(99) == b"FATTN_UNKNOWN_STATUS"
     assert fattn.version().startswith("libfattn")
 
@@ -193,7 +194,7 @@ def test_strided_arguments_are_checked(lib):
     def call(qs=dense, ks=dense, vs=dense, os_=dense, p=ptrs, causal=0, dtype=0):
         return f(*p, B, H, N, N, d, qs, ks, vs, os_, 0.125, causal, 1, None, 0, dtype, None)
     assert call(qs=None) == INVALID
-    assert call(dtype=2) == INVALID
+    assert call(dtype=3) == INVALID and call(dtype=-1) == INVALID
     assert call(os_=L3(H * N * d, N * d, d + 4)) == INVALID       # not a multiple of 8
     assert call(ks=L3(H * N * d, 0, d)) == INVALID                # zero stride, extent 3
     assert call(os_=L3(H * N * d, N * d, 32)) == INVALID          # o rows overlap (32 < d)

@@ -1,0 +1,127 @@
+"""GPU tests of the precision contract of the bf16 forward pass.
+
+attn_fwd rounds P to fp16 and converts each V tile to fp16 on chip (both
+operands of a tensor-core product share one type).  Checked here:
+  * peaked rows with |O| in [2, 4) meet the stated 1e-2 bound (with bf16 P
+    they cross a rounding midpoint: the reason for fp16 P);
+  * a V element beyond the fp16 range is reported as FATTN_ERR_RANGE in the
+    device status word (role 4, the epilogue), never silently;
+  * the bf16-P variant (attn_fwd_strided dtype 2) takes V of any bf16
+    magnitude and agrees with the oracle within its own bound: 1e-2 below
+    |O| = 2 and one bf16 ulp from there on, plus P's relative rounding for
+    inputs far outside the unit scale;
+  * every split count and entry point gives attn_fwd's bits.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import assert_parity, bf16_ulp, compare
+from tiled_online_softmax_fwd_gb300 import build as fbuild
+from tiled_online_softmax_fwd_gb300 import fattn
+from tiled_online_softmax_fwd_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+RANGE, ROLE_EPILOGUE = 5, 4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not os.path.exists(fattn.library_path()):
+        fbuild.build()
+    lib = fattn.load()
+    torch.cuda.synchronize()
+    fattn.device_status()  # start from a clear status word
+    yield lib
+
+
+def _peaked_case(seed, B=1, H=4, N=2048, d=128):
+    """Wide logits (sigma 4) and value rows scaled to put many |O| in [2, 4)."""
+    q, k, v = make_qkv(B, H, N, d, seed=seed, sigma_qk=4.0)
+    v = (v.float() * 2.5).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (96, True), (128, True), (256, True)])
+def test_peaked_rows_meet_the_stated_bound(d, causal):
+    q, k, v = _peaked_case(600 + d, d=d, N=1024 if d == 256 else 2048)
+    scale = fattn.default_scale(d)
+    o, lse = fattn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    # Outputs of order 2-4: the rounding floor alone (mean ~2e-3) exceeds the
+    # stated mean bound, so the floor rule applies to the mean.
+    r = compare(o.cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref, mean_rule="floor")
+    a = np.abs(o_ref)
+    assert ((a >= 2) & (a < 4)).sum() > 1000, "the case must exercise |O| in [2, 4)"
+    assert_parity(r, "peaked d%d" % d)
+    assert r["beyond_bound_gated"] == 0 and r["beyond_bound_2_4"] == 0, r
+    assert fattn.device_status() == 0
+
+
+def _bf16p(dq, dk, dv, causal, scale, splits=1):
+    return fattn.attn_fwd_strided(dq, dk, dv, causal=causal, scale=scale, num_splits=splits,
+                                  bf16_p=True)
+
+
+def test_v_beyond_fp16_range_is_reported():
+    q, k, v = make_qkv(1, 2, 700, 128, seed=611)
+    v[0, 1, 300, 5] = 7.0e4  # bf16 70144: beyond fp16's 65504
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    fattn.attn_fwd(dq, dk, dv, causal=True)
+    torch.cuda.synchronize()
+    word = fattn.device_status()
+    assert word & 0xff == RANGE and (word >> 8) & 0xff == ROLE_EPILOGUE, hex(word)
+    assert fattn.device_status() == 0  # reading clears it
+    # The bf16-P variant takes the same inputs: no status, oracle agreement.
+    scale = fattn.default_scale(128)
+    o, lse = _bf16p(dq, dk, dv, True, scale)
+    torch.cuda.synchronize()
+    assert fattn.device_status() == 0
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, True)
+    og = o.cpu().double().numpy().reshape(o_ref.shape)
+    assert np.all(np.isfinite(og))
+    err = np.abs(og - o_ref)
+    # bf16 P: relative rounding 2^-8 of each weight, times |v| <= 7e4, plus
+    # the output's own rounding (one ulp of O_ref).
+    bound = 2.0 ** -8 * np.abs(v.double().numpy()).max() + bf16_ulp(o_ref) + 1e-2
+    assert np.all(err <= bound)
+    assert np.abs(lse.cpu().double().numpy().reshape(-1) - lse_ref).max() <= 1e-3
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,splits", [(2, 3, 777, 64, False, 1),
+                                                   (1, 4, 1000, 128, True, 1),
+                                                   (2, 2, 513, 96, True, 3),
+                                                   (1, 2, 600, 256, True, 2)])
+def test_bf16p_variant_matches_oracle(B, H, N, d, causal, splits):
+    q, k, v = make_qkv(B, H, N, d, seed=620 + N + d, sigma_qk=2.0)
+    scale = fattn.default_scale(d)
+    o, lse = _bf16p(q.cuda(), k.cuda(), v.cuda(), causal, scale, splits)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    r = compare(o.cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref, mean_rule="floor")
+    # Its bound: 1e-2 below |O| = 2, one bf16 ulp of O_ref from there on.
+    og = o.cpu().double().numpy().reshape(o_ref.shape)
+    a = np.abs(o_ref)
+    assert r["finite"] and r["o_max_lt2"] <= 1e-2, r
+    assert np.all(np.abs(og - o_ref)[a >= 2] < bf16_ulp(o_ref[a >= 2])), r
+    assert r["o_mean"] <= r["mean_tol"] and r["lse_max"] <= 1e-3, r
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_entry_points_give_attn_fwd_bits(d):
+    """Contiguous strides and one split through the strided, key-value and
+    split entry points are the same kernel: identical bits."""
+    q, k, v = make_qkv(2, 3, 900, d, seed=630 + d, sigma_qk=3.0)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = fattn.attn_fwd(dq, dk, dv, causal=True)
+    o2, l2 = fattn.attn_fwd_strided(dq, dk, dv, causal=True, num_splits=1)
+    o3, l3 = fattn.attn_fwd_kv(dq, dk, dv, causal=True, num_splits=1)
+    o4, l4 = fattn.attn_fwd_split(dq, dk, dv, causal=True, num_splits=1)
+    torch.cuda.synchronize()
+    for o, l in ((o2, l2), (o3, l3), (o4, l4)):
+        assert torch.equal(o, o1) and torch.equal(l, l1)

@@ -277,7 +277,9 @@ fattn_status_t check_layout(const void *q, const void *k, const void *v, const v
     return FATTN_OK;
 }
 
-enum class Kernel { kTcgen05, kTcgen05F16, kSimt };
+// kTcgen05: bf16, P in fp16 (V converted on chip); kTcgen05F16: fp16;
+// kTcgen05Bf16P: bf16, P in bf16; kSimt: the fp32 cross-check kernel.
+enum class Kernel { kTcgen05, kTcgen05F16, kTcgen05Bf16P, kSimt };
 
 // Every check of a forward call with N queries and Nk keys per head.  On
 // FATTN_OK, *empty tells whether there is any work, and (when there is)
@@ -321,6 +323,7 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
     fattn::FwdArgs a{q, k, v, o, lse, B, H, N, d, scale, causal};
     const bool f16 = which == Kernel::kTcgen05F16;
     a.f16 = f16 ? 1 : 0;
+    a.bf16p = which == Kernel::kTcgen05Bf16P ? 1 : 0;
     a.Nk = Nk;
     cudaError_t e;
     if (which == Kernel::kSimt) {
@@ -581,7 +584,7 @@ fattn_status_t attn_fwd_strided(const void *q, const void *k, const void *v, voi
                                 float scale, int causal, int num_splits, void *workspace,
                                 size_t workspace_bytes, int dtype, struct CUstream_st *stream)
 {
-    if (!q_strides || !k_strides || !v_strides || !o_strides || (dtype != 0 && dtype != 1))
+    if (!q_strides || !k_strides || !v_strides || !o_strides || dtype < 0 || dtype > 2)
         return FATTN_ERR_INVALID_ARG;
     Layout L;
     for (int i = 0; i < 3; ++i) {
@@ -604,7 +607,8 @@ fattn_status_t attn_fwd_strided(const void *q, const void *k, const void *v, voi
     }
     return forward_split(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, workspace,
                          workspace_bytes, stream, &L,
-                         dtype == 1 ? Kernel::kTcgen05F16 : Kernel::kTcgen05);
+                         dtype == 1 ? Kernel::kTcgen05F16
+                                    : (dtype == 2 ? Kernel::kTcgen05Bf16P : Kernel::kTcgen05));
 }
 
 size_t attn_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal,
@@ -877,6 +881,7 @@ const char *fattn_status_string(fattn_status_t status)
     case FATTN_ERR_UNSUPPORTED: return "FATTN_ERR_UNSUPPORTED";
     case FATTN_ERR_CUDA: return "FATTN_ERR_CUDA";
     case FATTN_ERR_TIMEOUT: return "FATTN_ERR_TIMEOUT";
+    case FATTN_ERR_RANGE: return "FATTN_ERR_RANGE";
     }
     return "FATTN_UNKNOWN_STATUS";
 }
@@ -892,7 +897,9 @@ fattn_status_t fattn_get_device_status(int *status, struct CUstream_st *stream)
     if (e != cudaSuccess)
         return cuda_fail(e);
     *status = static_cast<int>(word);
-    return word == 0 ? FATTN_OK : FATTN_ERR_TIMEOUT;
+    if (word == 0)
+        return FATTN_OK;
+    return (word & 0xffu) == FATTN_ERR_RANGE ? FATTN_ERR_RANGE : FATTN_ERR_TIMEOUT;
 }
 
 fattn_status_t fattn_selftest_wait_timeout(unsigned int limit_us, struct CUstream_st *stream)

@@ -70,9 +70,9 @@ using namespace ptx;
 
 constexpr int kBM = 128;  // query rows per Q tile (= MMA M = TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpConv = 10;  // and 11 (kPrecBf16)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kRescaleLog2 = 8.0f;
@@ -80,8 +80,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kChunkBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 box
 
-template <int D, bool kF16 = false>
+// Precision modes.  Inputs and output are bf16 or fp16; P, the 16-bit
+// probabilities that enter the P V product, is fp16 or bf16.  Both operands
+// of one tensor-core product have one type, so for bf16 inputs with fp16 P
+// the V tiles are converted to fp16 in shared memory (exactly, for |v| below
+// 65520) by two converter warps before the P V product reads them.
+constexpr int kPrecBf16 = 0;    // bf16 q, k, v, o; P in fp16 (V converted)
+constexpr int kPrecF16 = 1;     // fp16 q, k, v, o; P in fp16
+constexpr int kPrecBf16P = 2;   // bf16 q, k, v, o; P in bf16 (V of any bf16 magnitude)
+
+template <int D, int kPrec = kPrecBf16>
 struct Cfg {
+    static constexpr bool kInF16 = kPrec == kPrecF16;    // q, k, v, o in fp16
+    static constexpr bool kPF16 = kPrec != kPrecBf16P;   // P (and V in P V) in fp16
+    static constexpr bool kConv = kPrec == kPrecBf16;    // converter warps
+    // Threads: the two-tile kernel has 8 softmax warps, a TMA warp and an
+    // MMA warp; the one-tile kernel 4, 1 and 1; both add 2 converter warps.
+    static constexpr int kThreads = (D == 256 ? 192 : 320) + (kConv ? 64 : 0);
     // 128-byte swizzle atoms along d.  d = 96 takes two: the tensor map's
     // 64-column box reads columns 96..127 as zeros, which no MMA uses (the
     // S product stops at K = 96, the P V product has N = 96).
@@ -93,8 +108,8 @@ struct Cfg {
     static constexpr int kStages = kChunks == 4 ? 2 : (kChunks == 2 ? 4 : 8);  // K/V ring
     // Ones column: P V runs with N = D + 16 against V extended by a constant
     // atom whose first column is 1.0, so O column D accumulates l_round.
-    // Needs 2 * (128 + D + 16) <= 512 TMEM columns; used for bf16, d = 64.
-    static constexpr bool kOnes = !kF16 && D == 64;
+    // Needs 2 * (128 + D + 16) <= 512 TMEM columns; used for bf16 P, d = 64.
+    static constexpr bool kOnes = !kPF16 && D == 64;
     static constexpr uint32_t kOnesOffset = (kQTiles + kStages) * kTileBytes;
     static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
     // Epilogue staging of the one-tile kernel: 4 KB (32 rows x 128 bytes) for
@@ -117,6 +132,8 @@ struct Bars {
     uint64_t p_half[2];  // two-tile kernel: P of the first 64 keys written
     uint64_t drain;
     uint64_t pv_done;  // single-tile kernel: completion of each P V
+    uint64_t v_ready[8];  // converter warps: the V tile in this stage is fp16
+    uint64_t v_full[8];   // single-tile kernel: a V copy landed (K copies use kv_full)
     uint32_t tmem_base;
     int abort;
     // Stream-K range of this CTA (see cta_unit): first head, its first key
@@ -372,16 +389,152 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
     }
 }
 
+// ------------------------------------------------------------------ V conversion
+// kPrecBf16: the P V product runs in fp16 (both operands of one product share
+// one type), so every V tile is rewritten in place from bf16 to fp16 after its
+// copy lands and before the product reads it.  Element order and swizzle are
+// unchanged (both types are 2 bytes).  The conversion is exact for |v| <
+// 65520 (fp16 has three more significand bits than bf16; the smallest bf16
+// magnitudes become fp16 subnormals, off by at most 2^-25); a larger
+// magnitude becomes infinite, which makes the rows that weigh it non-finite:
+// the epilogue records FATTN_ERR_RANGE for any non-finite output row (see
+// epilogue_row).  Three instructions a pair of elements: two to widen the
+// bf16 halves to fp32, one to round both to fp16.  Two converter warps share
+// each tile.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+{
+    __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w)
+{
+    return make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                      bf16x2_to_f16x2(w.w));
+}
+
+constexpr int kConvThreads = 64;
+
+// Eight 16-byte steps in flight per thread over kVecs consecutive granules.
+template <int kVecs>
+__device__ __forceinline__ void convert_linear(uint4 *tile, int tid)
+{
+    constexpr int kBatch = 8;
+    static_assert(kVecs % (kConvThreads * kBatch) == 0, "whole batches per thread");
+#pragma unroll 1
+    for (int base = tid; base < kVecs; base += kConvThreads * kBatch) {
+        uint4 w[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            w[i] = tile[base + i * kConvThreads];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            tile[base + i * kConvThreads] = bf16x8_to_f16x8(w[i]);
+    }
+}
+
+// A whole tile: its 64-column boxes of 128 rows x 128 bytes.  At d = 96 the
+// second box holds columns 64..95 in its logical granules 0-3 (granule g of
+// row r sits at g ^ (r % 8)) and the copy's zero fill in 4-7, which no
+// product reads: only the used half is converted.  Each 8-lane store phase
+// covers rows r and r + 4, whose granules 0-3 land on complementary halves
+// of the banks.
+template <int D, uint32_t kTileBytes>
+__device__ __forceinline__ void convert_tile(uint8_t *tile, int tid)
+{
+    if constexpr (D % 64 == 0) {
+        convert_linear<kTileBytes / 16>(reinterpret_cast<uint4 *>(tile), tid);
+    } else {
+        static_assert(D == 96 && kTileBytes == 2 * kChunkBytes, "d = 96: two boxes");
+        convert_linear<kChunkBytes / 16>(reinterpret_cast<uint4 *>(tile), tid);
+        uint8_t *box = tile + kChunkBytes;
+        constexpr int kBatch = 8;
+#pragma unroll 1
+        for (int base = tid; base < kBM * 4; base += kConvThreads * kBatch) {
+            uint4 w[kBatch];
+            uint4 *at[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int x = base + i * kConvThreads, k = x / 8, e = x % 8;
+                const int r = (k / 4) * 8 + k % 4 + (e / 4) * 4, g = e % 4;
+                at[i] = reinterpret_cast<uint4 *>(box + r * 128 + ((g ^ (r & 7)) << 4));
+                w[i] = *at[i];
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                *at[i] = bf16x8_to_f16x8(w[i]);
+        }
+    }
+}
+
+// Converter warp cw (0 or 1).  Visits the V tiles in the producer's order:
+// the two-tile kernel's ring holds K_j and V_j alternately over an even
+// number of stages, so V copies always land on the odd stages, whose
+// kv_full phases are all V copies; the one-tile kernel loads K_0, K_1, then
+// V_i and K_(i+2) alternately, its V copies completing on v_full (one phase
+// bit per stage).  For each V tile it waits for the copy, converts its share,
+// makes the writes visible to the tensor cores (async proxy) and arrives on
+// v_ready of the stage.
+template <int D, int kPrec>
+__device__ void run_convert(const Params &p, Bars &b, uint8_t *tiles, int cw)
+{
+    using C = Cfg<D, kPrec>;
+    const volatile int *abort = &b.abort;
+    const int lane = threadIdx.x & 31;
+    const int tid = cw * 32 + lane;
+    uint32_t pos = 0, vbits = 0;
+    bool ok = true;
+    auto convert = [&](uint32_t stage) {
+        convert_tile<D, C::kTileBytes>(tiles + (C::kQTiles + stage) * C::kTileBytes, tid);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&b.v_ready[stage]));
+    };
+    for (int r = 0; ok; ++r) {
+        Unit u;
+        if (!cta_unit(p, b, r, u))
+            break;
+        if constexpr (C::kQTiles == 2) {
+            for (int i = 0; ok && i < u.n_max; ++i) {
+                const uint32_t at = pos + 2 * i + 1;
+                const uint32_t stage = at % C::kStages;
+                ok = mbar_wait(smem_addr(&b.kv_full[stage]), (at / C::kStages) & 1, kWaitLimitNs,
+                               abort);
+                if (ok)
+                    convert(stage);
+            }
+            pos += 2 * u.n_max;
+        } else {
+            const int n = u.n[0];
+            if (n == 0)
+                continue;
+            pos += n > 1 ? 2 : 1;  // K_0 (and K_1)
+            for (int i = 0; ok && i < n; ++i) {
+                const uint32_t stage = pos % C::kStages;
+                ok = mbar_wait(smem_addr(&b.v_full[stage]), (vbits >> stage) & 1u, kWaitLimitNs,
+                               abort);
+                vbits ^= 1u << stage;
+                if (ok)
+                    convert(stage);
+                pos += i + 2 < n ? 2 : 1;  // V_i (and K_(i+2))
+            }
+        }
+    }
+    if (!ok && lane == 0)
+        record_failure(b, kRoleConvert);
+}
+
 // ------------------------------------------------------------------ MMA issue
 // S = Q K^T: both operands K-major (d contiguous), 128-byte swizzled, 8-row
 // groups 1024 bytes apart.  Each K = 16 step moves 32 bytes along d inside a
 // 64-column box, or to the next 16 KB box.  The start address occupies the
 // low 14 bits of the descriptor's low word and never carries out of them
 // (shared memory is below 256 KB), so a step is one 32-bit add.
-template <int D, bool kF16>
+template <int D, int kPrec>
 __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem)
 {
-    constexpr uint32_t idesc = idesc_f32acc(kBM, kBN, false, kF16);
+    constexpr uint32_t idesc = idesc_f32acc(kBM, kBN, false, Cfg<D, kPrec>::kInF16);
     constexpr uint32_t hi = smem_desc_hi(1024);
     const uint32_t a_lo = smem_desc_lo(q_smem, 16), b_lo = smem_desc_lo(k_smem, 16);
 #pragma unroll
@@ -398,12 +551,12 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32
 // tensor memory, 8 columns (16 keys of bf16 pairs) per K = 16 step.
 // With the ones column (Cfg::kOnes, d = 64) N = 80: the MMA's second atom
 // along N is the constant ones atom, so LBO is its distance from this stage.
-template <int D, bool kF16, int kK0 = 0, int kK1 = kBN / 16>
+template <int D, int kPrec, int kK0 = 0, int kK1 = kBN / 16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_smem,
                                          uint32_t ones_smem, bool accumulate)
 {
-    using C = Cfg<D, kF16>;
-    constexpr uint32_t idesc = idesc_f32acc(kBM, C::kON, true, kF16);
+    using C = Cfg<D, kPrec>;
+    constexpr uint32_t idesc = idesc_f32acc(kBM, C::kON, true, C::kPF16);
     constexpr uint32_t kVLbo = D > 64 ? kChunkBytes : 1024;
     constexpr uint32_t hi = smem_desc_hi(1024);
     const uint32_t b_lo = smem_desc_lo(v_smem, C::kOnes ? ones_smem - v_smem : kVLbo);
@@ -414,10 +567,10 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint3
                  kk > 0 ? 1u : acc0);
 }
 
-template <int D, bool kF16>
+template <int D, int kPrec>
 __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t tmem)
 {
-    using C = Cfg<D, kF16>;
+    using C = Cfg<D, kPrec>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
     uint32_t q_phase[2] = {0, 0}, p_phase[2] = {0, 0}, ph_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
@@ -429,6 +582,19 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
         return warp_wait(smem_addr(&b.kv_full[at % C::kStages]), (at / C::kStages) & 1, abort);
     };
     auto kv_smem = [&](uint32_t at) { return smem_base + (2 + kv_stage(at)) * C::kTileBytes; };
+    // A V tile is ready once copied (and, with converter warps, converted);
+    // v_ready keeps one phase bit per stage.
+    uint32_t vr_bits = 0;
+    auto v_wait = [&](uint32_t at) {
+        if constexpr (!C::kConv) {
+            return kv_wait(at);
+        } else {
+            const uint32_t st = at % C::kStages;
+            const bool r = warp_wait(smem_addr(&b.v_ready[st]), (vr_bits >> st) & 1u, abort);
+            vr_bits ^= 1u << st;
+            return r;
+        }
+    };
     auto commit = [&](uint64_t &bar) {
         if (leader)
             mma_commit(smem_addr(&bar));
@@ -456,7 +622,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
             if (u.n[t] == 0)
                 continue;
             if (leader)
-                issue_s<D, kF16>(tmem + (t == 0 ? 0u : 128u), smem_base + t * C::kTileBytes,
+                issue_s<D, kPrec>(tmem + (t == 0 ? 0u : 128u), smem_base + t * C::kTileBytes,
                            kv_smem(base));
             commit(b.s_full[t]);
             if (u.n[t] == 1)
@@ -470,7 +636,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
             const uint32_t at_v = base + 2 * (j - 1) + 1;
             const uint32_t at_k = base + 2 * j;
             const bool has_k = j < u.n_max;
-            ok = kv_wait(at_v) && (!has_k || kv_wait(at_k));
+            ok = v_wait(at_v) && (!has_k || kv_wait(at_k));
             if (!ok)
                 break;
             for (int t = 0; t < 2 && ok; ++t) {
@@ -496,7 +662,7 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
                 const uint32_t col_o = t == 0 ? C::kColO0 : C::kColO1;
                 if (C::kHalfP) {
                     if (leader)
-                        issue_pv<D, kF16, 0, kBN / 32>(tmem + col_o, tmem + col_s, kv_smem(at_v),
+                        issue_pv<D, kPrec, 0, kBN / 32>(tmem + col_o, tmem + col_s, kv_smem(at_v),
                                                        smem_base + C::kOnesOffset, j - 1 > 0);
                     ok = warp_wait(smem_addr(&b.p_full[t]), p_phase[t], abort);
                     p_phase[t] ^= 1;
@@ -504,16 +670,16 @@ __device__ void run_mma(const Params &p, Bars &b, uint32_t smem_base, uint32_t t
                         break;
                     tc_fence_after();
                     if (leader)
-                        issue_pv<D, kF16, kBN / 32, kBN / 16>(tmem + col_o, tmem + col_s,
+                        issue_pv<D, kPrec, kBN / 32, kBN / 16>(tmem + col_o, tmem + col_s,
                                                               kv_smem(at_v),
                                                               smem_base + C::kOnesOffset, true);
                 } else if (leader) {
-                    issue_pv<D, kF16>(tmem + col_o, tmem + col_s, kv_smem(at_v),
+                    issue_pv<D, kPrec>(tmem + col_o, tmem + col_s, kv_smem(at_v),
                                       smem_base + C::kOnesOffset, j - 1 > 0);
                 }
                 if (j < u.n[t]) {
                     if (leader)
-                        issue_s<D, kF16>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
+                        issue_s<D, kPrec>(tmem + col_s, smem_base + t * C::kTileBytes, kv_smem(at_k));
                     commit(b.s_full[t]);
                     if (j == u.n[t] - 1)
                         commit(b.q_empty[t]);
@@ -548,7 +714,7 @@ struct NoHook {
     __device__ __forceinline__ void operator()(float) const {}
 };
 
-template <int D, bool kF16, bool kOnes, class Pre = NoHook, class Mid = NoHook>
+template <int D, int kPrec, bool kOnes, class Pre = NoHook, class Mid = NoHook>
 __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int r, int j,
                                               int first_vis, bool first, float m, float &m_new,
                                               float &l, float &l_round, Pre pre = Pre(),
@@ -606,7 +772,7 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
             f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, negm), x0,
                       x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
-            pk[i] = pack2<kF16>(p0, p1);
+            pk[i] = pack2<Cfg<D, kPrec>::kPF16>(p0, p1);
             sum_exact[i & 1] = f2_add(sum_exact[i & 1], f2_pack(p0, p1));
         }
         tmem_st16(t_s + c * 16, pk);
@@ -618,7 +784,7 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
     f2_unpack(sum_exact[1], e2, e3);
     const float esum = (e0 + e1) + (e2 + e3);
     l = l * alpha + esum;
-    if constexpr (!kF16 && !kOnes) {
+    if constexpr (!Cfg<D, kPrec>::kPF16 && !kOnes) {
         // The tile's largest p, from the same fused multiply-add and
         // exponential as its P element, and its bf16 rounding error.
         const float pt = ex2(fmaf(smax, p.sl2, -m_new));
@@ -680,12 +846,22 @@ __device__ __forceinline__ void stage_flush(const uint8_t *stage, int lane, char
     __syncwarp();
 }
 
+// The epilogue's check for non-finite output (kPrecBf16): adds o * 0 over a
+// chunk of the O row, four chains; the sum stays 0 while every value is
+// finite and becomes NaN at the first infinity or NaN.
+__device__ __forceinline__ void nonfinite_acc(const uint32_t (&o)[32], float (&acc)[4])
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        acc[i % 4] = fmaf(__uint_as_float(o[i]), 0.f, acc[i % 4]);
+}
+
 // Epilogue of one row after the unit's last P V: O / l_round in bf16 (fp16)
 // and lse = ln2 * (m + log2 l); in split mode the fp32 partial O and the two
 // base-2 partial lse go to the workspace instead, for the combine kernel.  kStaged:
 // through the staging area (warp w, among the CTA's first warps, uses its
 // w-th 4 KB), for D a multiple of 64.
-template <int D, bool kF16, bool kOnes, bool kStaged = false>
+template <int D, int kPrec, bool kOnes, bool kStaged = false>
 __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uint32_t t_o, int row,
                                              float m, float l, float l_round)
 {
@@ -696,16 +872,25 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
         l_round = __uint_as_float(tmem_ld1(t_o + D));
         tmem_wait_ld();
     }
-    const float l_norm = kF16 ? l : l_round;
+    constexpr bool kOutF16 = Cfg<D, kPrec>::kInF16;
+    const float l_norm = Cfg<D, kPrec>::kPF16 ? l : l_round;
     const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
     const bool live = row < p.Nq;
     const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
+    // With V converted to fp16 (kPrecBf16), a V element of magnitude 65520
+    // or more turns into an infinity: a non-finite output row (which
+    // non-finite inputs also give) records FATTN_ERR_RANGE.
+    float nf[4] = {0.f, 0.f, 0.f, 0.f};
+    auto check = [&](const uint32_t (&o)[32]) {
+        if constexpr (Cfg<D, kPrec>::kConv)
+            nonfinite_acc(o, nf);
+    };
     if constexpr (kStaged) {
         static_assert(D % 64 == 0, "staged rows are whole 128-byte pieces");
         extern __shared__ __align__(1024) uint8_t smem_raw[];
         const uint32_t raw = smem_addr(smem_raw);
         uint8_t *stage = smem_raw + (((raw + 1023u) & ~1023u) - raw) +
-                         Cfg<D, kF16>::kStageOffset + (threadIdx.x / 32) * 4096;
+                         Cfg<D, kPrec>::kStageOffset + (threadIdx.x / 32) * 4096;
         const int lane = threadIdx.x & 31;
         const int row0 = row - lane;  // the warp's first row
         const int live_rows = min(32, p.Nq - row0);
@@ -719,14 +904,15 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
                 __syncwarp();
                 tmem_ld32(t_o + c * 32, o);
                 tmem_wait_ld();
+                check(o);
                 auto f = [&](int i) { return __uint_as_float(o[i]) * inv_l; };
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     stage_put(stage, lane, (c % 2) * 4 + i,
-                              make_uint4(pack2<kF16>(f(8 * i), f(8 * i + 1)),
-                                         pack2<kF16>(f(8 * i + 2), f(8 * i + 3)),
-                                         pack2<kF16>(f(8 * i + 4), f(8 * i + 5)),
-                                         pack2<kF16>(f(8 * i + 6), f(8 * i + 7))));
+                              make_uint4(pack2<kOutF16>(f(8 * i), f(8 * i + 1)),
+                                         pack2<kOutF16>(f(8 * i + 2), f(8 * i + 3)),
+                                         pack2<kOutF16>(f(8 * i + 4), f(8 * i + 5)),
+                                         pack2<kOutF16>(f(8 * i + 6), f(8 * i + 7))));
                 if (c % 2 == 1)
                     stage_flush(stage, lane, dst0 + (c / 2) * 128, p.o_sn * 2, live_rows);
             }
@@ -741,6 +927,7 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
                 __syncwarp();
                 tmem_ld32(t_o + c * 32, o);
                 tmem_wait_ld();
+                check(o);
                 auto f = [&](int i) { return __float_as_uint(__uint_as_float(o[i]) * inv_l); };
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -759,10 +946,11 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
             __syncwarp();
             tmem_ld32(t_o + c * 32, o);
             tmem_wait_ld();
+            check(o);
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                pk[i] = pack2<kF16>(__uint_as_float(o[2 * i]) * inv_l,
+                pk[i] = pack2<kOutF16>(__uint_as_float(o[2 * i]) * inv_l,
                                     __uint_as_float(o[2 * i + 1]) * inv_l);
             if (live) {
                 uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
@@ -782,6 +970,7 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
             __syncwarp();
             tmem_ld32(t_o + c * 32, o);
             tmem_wait_ld();
+            check(o);
             if (live) {
                 float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
 #pragma unroll
@@ -795,12 +984,20 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
         if (live)
             p.ws_l[srow] = make_float2(m + log2f(l), m + log2f(l_norm));
     }
+    if constexpr (Cfg<D, kPrec>::kConv) {
+        const float acc = (nf[0] + nf[1]) + (nf[2] + nf[3]);
+        if (live && acc != acc) {
+            const uint32_t code = 5u /* FATTN_ERR_RANGE */ | (kRoleEpilogue << 8) |
+                                  ((blockIdx.x & 0xffffu) << 16);
+            atomicCAS(&g_fattn_status, 0u, code);
+        }
+    }
 }
 
-template <int D, bool kF16>
+template <int D, int kPrec>
 __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
 {
-    using C = Cfg<D, kF16>;
+    using C = Cfg<D, kPrec>;
     const volatile int *abort = &b.abort;
     const int warp = (threadIdx.x / 32) & 3;
     const int lane = threadIdx.x & 31;
@@ -850,7 +1047,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                             mbar_arrive(smem_addr(&b.p_half[t]));
                     }
                 };
-                const float alpha = softmax_tile<D, kF16, C::kOnes>(
+                const float alpha = softmax_tile<D, kPrec, C::kOnes>(
                     p, t_s, r, j, first_vis, first, m, m_new, l, l_round, pre, mid);
                 if (rescale)
                     rescale_o<D, C::kOnes>(t_o, alpha);
@@ -864,7 +1061,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
                     mbar_arrive(smem_addr(&b.p_full[t]));
                 }
             } else {
-                const float alpha = softmax_tile<D, kF16, C::kOnes>(p, t_s, r, j, first_vis, first,
+                const float alpha = softmax_tile<D, kPrec, C::kOnes>(p, t_s, r, j, first_vis, first,
                                                                     m, m_new, l, l_round);
                 if (!first && __any_sync(0xffffffffu, m_new != m))
                     rescale_o<D, C::kOnes>(t_o, alpha);
@@ -883,7 +1080,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         if (!ok)
             break;
         tc_fence_after();
-        epilogue_row<D, kF16, C::kOnes>(p, u, t_o, row, m, l, l_round);
+        epilogue_row<D, kPrec, C::kOnes>(p, u, t_o, row, m, l, l_round);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -908,12 +1105,12 @@ __device__ __forceinline__ void init_ones_atom(uint8_t *atom)
     fence_proxy_async_smem();
 }
 
-template <int D, bool kF16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int kPrec>
+__global__ void __launch_bounds__(Cfg<D, kPrec>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const Params p)
 {
-    using C = Cfg<D, kF16>;
+    using C = Cfg<D, kPrec>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t smem_base = (raw + 1023u) & ~1023u;
@@ -934,6 +1131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_addr(&b.kv_full[s]), 1);
             mbar_init(smem_addr(&b.kv_empty[s]), 1);
+            mbar_init(smem_addr(&b.v_ready[s]), 2);
         }
         mbar_init(smem_addr(&b.drain), 1);
         b.abort = 0;
@@ -964,11 +1162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = b.tmem_base;
 
     if (warp < 8) {
-        run_softmax<D, kF16>(p, b, tmem, warp / 4);
+        run_softmax<D, kPrec>(p, b, tmem, warp / 4);
     } else if (warp == kWarpLoad) {
         run_load<D>(p, b, smem_base, &mq, &mk, &mv);
     } else if (warp == kWarpMma) {
-        run_mma<D, kF16>(p, b, smem_base, tmem);
+        run_mma<D, kPrec>(p, b, smem_base, tmem);
+    } else if constexpr (C::kConv) {
+        run_convert<D, kPrec>(p, b, smem_raw + (smem_base - raw), warp - kWarpConv);
     }
     // The merge kernel of a split call (launched with programmatic stream
     // serialisation) may be scheduled now; it still waits for this grid to
@@ -993,9 +1193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 0-3 softmax (thread r owns row r), warp 4 TMA, warp 5 MMA.  K/V ring of two
 // 64 KB stages, filled in the order the MMAs consume it: K0, K1, then V(i)
 // and K(i+2) alternately.
-constexpr int kSingleThreads = 192;
 constexpr int kSingleWarpLoad = 4;
 constexpr int kSingleWarpMma = 5;
+constexpr int kSingleWarpConv = 6;  // and 7 (kPrecBf16)
 
 template <int D>
 __device__ void run_load_single(const Params &p, Bars &b, uint32_t smem_base,
@@ -1008,18 +1208,34 @@ __device__ void run_load_single(const Params &p, Bars &b, uint32_t smem_base,
     uint32_t q_phase = 0, pos = 0;
     int last_q_parity = -1;
     bool ok = true;
-    auto load_tile = [&](const CUtensorMap *m, int row, int hh, int bb) {
+    // K and V share the two stages irregularly (K_0, K_1, then V_i and
+    // K_(i+2) alternately), so K copies complete on kv_full and V copies on
+    // v_full: each barrier then sees only its own tiles, in order, and the
+    // next phase's parity is kept per stage and barrier.
+    uint32_t kbits = 0, vbits = 0, last_v = 0, used = 0;
+    auto load_tile = [&](const CUtensorMap *m, int row, int hh, int bb, bool is_v) {
         const uint32_t stage = pos % C::kStages;
         ok = warp_wait(smem_addr(&b.kv_empty[stage]), ((pos / C::kStages) & 1) ^ 1, abort);
-        if (ok && leader) {
-            const uint32_t full = smem_addr(&b.kv_full[stage]);
+        if (!ok)
+            return;
+        if (leader) {
+            const uint32_t full = smem_addr(is_v ? &b.v_full[stage] : &b.kv_full[stage]);
             mbar_arrive_expect_tx(full, C::kTileBytes);
             const uint32_t dst = smem_base + (C::kQTiles + stage) * C::kTileBytes;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_4d(dst + c * kChunkBytes, m, full, 64 * c, row, hh, bb);
         }
-        pos += ok ? 1 : 0;
+        const uint32_t bit = 1u << stage;
+        if (is_v) {
+            vbits ^= bit;
+            last_v |= bit;
+        } else {
+            kbits ^= bit;
+            last_v &= ~bit;
+        }
+        used |= bit;
+        ++pos;
     };
     for (int r = 0; ok; ++r) {
         Unit u;
@@ -1042,32 +1258,40 @@ __device__ void run_load_single(const Params &p, Bars &b, uint32_t smem_base,
         }
         last_q_parity = q_phase;
         q_phase ^= 1;
-        load_tile(mk, u.j0 * kBN, hh, bb);
+        load_tile(mk, u.j0 * kBN, hh, bb, false);
         if (ok && n > 1)
-            load_tile(mk, (u.j0 + 1) * kBN, hh, bb);
+            load_tile(mk, (u.j0 + 1) * kBN, hh, bb, false);
         for (int i = 0; ok && i < n; ++i) {
-            load_tile(mv, (u.j0 + i) * kBN, hh, bb);
+            load_tile(mv, (u.j0 + i) * kBN, hh, bb, true);
             if (ok && i + 2 < n)
-                load_tile(mk, (u.j0 + i + 2) * kBN, hh, bb);
+                load_tile(mk, (u.j0 + i + 2) * kBN, hh, bb, false);
         }
     }
     if (!ok) {
         if (leader)
             record_failure(b, kRoleLoad);
-        // Let the copies already issued land before the CTA exits.
-        const uint32_t first = pos > (uint32_t)C::kStages ? pos - C::kStages : 0;
-        for (uint32_t q = first; q < pos; ++q)
-            mbar_wait(smem_addr(&b.kv_full[q % C::kStages]), (q / C::kStages) & 1,
-                      kWaitLimitNs / 8, nullptr);
+        // Let the copies already issued land before the CTA exits: only the
+        // last copy into each stage can still be in flight.
+        for (int st = 0; st < C::kStages; ++st) {
+            const uint32_t bit = 1u << st;
+            if (!(used & bit))
+                continue;
+            if (last_v & bit)
+                mbar_wait(smem_addr(&b.v_full[st]), ((vbits & bit) ? 0u : 1u), kWaitLimitNs / 8,
+                          nullptr);
+            else
+                mbar_wait(smem_addr(&b.kv_full[st]), ((kbits & bit) ? 0u : 1u), kWaitLimitNs / 8,
+                          nullptr);
+        }
         if (last_q_parity >= 0)
             mbar_wait(smem_addr(&b.q_full[0]), last_q_parity, kWaitLimitNs / 8, nullptr);
     }
 }
 
-template <int D, bool kF16>
+template <int D, int kPrec>
 __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uint32_t tmem)
 {
-    using C = Cfg<D, kF16>;
+    using C = Cfg<D, kPrec>;
     const volatile int *abort = &b.abort;
     const bool leader = elect_one();
     uint32_t q_phase = 0, oe_phase = 0, p_phase[2] = {0, 0}, pos = 0;
@@ -1077,9 +1301,20 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
             mma_commit(smem_addr(&bar));
     };
     // Waits for the next ring position; returns its shared-memory address.
-    auto next_tile = [&](uint32_t &addr) {
+    // K tiles complete on kv_full, V tiles on v_full, or with converter warps
+    // on v_ready once converted; each keeps one phase bit per stage.
+    uint32_t kbits = 0, vbits = 0;
+    auto next_tile = [&](uint32_t &addr, bool is_v = false) {
         const uint32_t stage = pos % C::kStages;
-        ok = warp_wait(smem_addr(&b.kv_full[stage]), (pos / C::kStages) & 1, abort);
+        const uint32_t bit = 1u << stage;
+        if (is_v) {
+            const uint32_t bar = smem_addr(C::kConv ? &b.v_ready[stage] : &b.v_full[stage]);
+            ok = warp_wait(bar, (vbits & bit) ? 1u : 0u, abort);
+            vbits ^= bit;
+        } else {
+            ok = warp_wait(smem_addr(&b.kv_full[stage]), (kbits & bit) ? 1u : 0u, abort);
+            kbits ^= bit;
+        }
         addr = smem_base + (C::kQTiles + stage) * C::kTileBytes;
         return stage;
     };
@@ -1102,7 +1337,7 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
                 break;
             tc_fence_after();
             if (leader)
-                issue_s<D, kF16>(tmem + i * 128u, smem_base, k_addr);
+                issue_s<D, kPrec>(tmem + i * 128u, smem_base, k_addr);
             commit(b.s_full[i]);
             commit(b.kv_empty[stage]);
             ++pos;
@@ -1119,12 +1354,12 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
             }
             uint32_t v_addr = 0, stage = 0;
             if (ok)
-                stage = next_tile(v_addr);
+                stage = next_tile(v_addr, true);
             if (!ok)
                 break;
             tc_fence_after();
             if (leader)
-                issue_pv<D, kF16>(tmem + C::kColO0, tmem + buf * 128u, v_addr,
+                issue_pv<D, kPrec>(tmem + C::kColO0, tmem + buf * 128u, v_addr,
                                   smem_base + C::kOnesOffset, i > 0);
             commit(b.pv_done);
             commit(b.kv_empty[stage]);
@@ -1136,7 +1371,7 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
                     break;
                 tc_fence_after();
                 if (leader)
-                    issue_s<D, kF16>(tmem + buf * 128u, smem_base, k_addr);
+                    issue_s<D, kPrec>(tmem + buf * 128u, smem_base, k_addr);
                 commit(b.s_full[buf]);
                 commit(b.kv_empty[ks]);
                 ++pos;
@@ -1154,10 +1389,10 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
     mbar_wait(smem_addr(&b.drain), 0, kWaitLimitNs, nullptr);
 }
 
-template <int D, bool kF16>
+template <int D, int kPrec>
 __device__ void run_softmax_single(const Params &p, Bars &b, uint32_t tmem)
 {
-    using C = Cfg<D, kF16>;
+    using C = Cfg<D, kPrec>;
     const volatile int *abort = &b.abort;
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -1187,7 +1422,7 @@ __device__ void run_softmax_single(const Params &p, Bars &b, uint32_t tmem)
             tc_fence_after();
             __syncwarp();
             float m_new;
-            const float alpha = softmax_tile<D, kF16, C::kOnes>(p, tmem + lane_off + buf * 128u, r,
+            const float alpha = softmax_tile<D, kPrec, C::kOnes>(p, tmem + lane_off + buf * 128u, r,
                                                                 j, first_vis, first, m, m_new, l,
                                                                 l_round);
             if (!first && __any_sync(0xffffffffu, m_new != m)) {
@@ -1214,7 +1449,7 @@ __device__ void run_softmax_single(const Params &p, Bars &b, uint32_t tmem)
         if (!ok)
             break;
         tc_fence_after();
-        epilogue_row<D, kF16, C::kOnes, true>(p, u, t_o, row, m, l, l_round);
+        epilogue_row<D, kPrec, C::kOnes, true>(p, u, t_o, row, m, l, l_round);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -1224,12 +1459,12 @@ __device__ void run_softmax_single(const Params &p, Bars &b, uint32_t tmem)
         record_failure(b, kRoleSoftmax);
 }
 
-template <int D, bool kF16>
-__global__ void __launch_bounds__(kSingleThreads, 1)
+template <int D, int kPrec>
+__global__ void __launch_bounds__(Cfg<D, kPrec>::kThreads, 1)
     fwd_single_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                       const __grid_constant__ CUtensorMap mv, const Params p)
 {
-    using C = Cfg<D, kF16>;
+    using C = Cfg<D, kPrec>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t smem_base = (raw + 1023u) & ~1023u;
@@ -1249,6 +1484,8 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_addr(&b.kv_full[s]), 1);
             mbar_init(smem_addr(&b.kv_empty[s]), 1);
+            mbar_init(smem_addr(&b.v_ready[s]), 2);
+            mbar_init(smem_addr(&b.v_full[s]), 1);
         }
         mbar_init(smem_addr(&b.drain), 1);
         mbar_init(smem_addr(&b.pv_done), 1);
@@ -1280,11 +1517,13 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
     const uint32_t tmem = b.tmem_base;
 
     if (warp < 4)
-        run_softmax_single<D, kF16>(p, b, tmem);
+        run_softmax_single<D, kPrec>(p, b, tmem);
     else if (warp == kSingleWarpLoad)
         run_load_single<D>(p, b, smem_base, &mq, &mk, &mv);
     else if (warp == kSingleWarpMma)
-        run_mma_single<D, kF16>(p, b, smem_base, tmem);
+        run_mma_single<D, kPrec>(p, b, smem_base, tmem);
+    else if constexpr (C::kConv)
+        run_convert<D, kPrec>(p, b, smem_raw + (smem_base - raw), warp - kSingleWarpConv);
     grid_launch_dependents();  // see fwd_kernel
 
     tc_fence_before();
@@ -1331,11 +1570,12 @@ __device__ __forceinline__ bool slot_range(const Params &p, int bh, int fmax, in
     return true;
 }
 
-template <int D, bool kF16>
+template <int D, int kPrec>
 __global__ void __launch_bounds__(128)
     combine_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_l, const Params p)
 {
     constexpr int kCols = D / 32;
+    constexpr bool kOutF16 = Cfg<D, kPrec>::kInF16;
     const long long row = static_cast<long long>(blockIdx.x) * 4 + threadIdx.x / 32;
     const long long rows = static_cast<long long>(p.BH) * p.Nq;
     if (row >= rows)
@@ -1414,21 +1654,21 @@ __global__ void __launch_bounds__(128)
     if constexpr (kCols % 2 == 0) {
 #pragma unroll
         for (int c = 0; c < kCols; c += 2)
-            *reinterpret_cast<uint32_t *>(dst + c) = pack2<kF16>(acc[c] * inv, acc[c + 1] * inv);
+            *reinterpret_cast<uint32_t *>(dst + c) = pack2<kOutF16>(acc[c] * inv, acc[c + 1] * inv);
     } else {  // d = 96: three columns per lane, stored one by one
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
-            dst[c] = static_cast<uint16_t>(pack2<kF16>(acc[c] * inv, 0.f) & 0xffffu);
+            dst[c] = static_cast<uint16_t>(pack2<kOutF16>(acc[c] * inv, 0.f) & 0xffffu);
     }
     if (lane == 0)
         p.lse[row] = (mx_e + log2f(se)) * kLn2;
 }
 
-template <int D, bool kF16>
+template <int D, int kPrec>
 cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split, int num_sms,
                    cudaStream_t stream)
 {
-    using C = Cfg<D, kF16>;
+    using C = Cfg<D, kPrec>;
     Params p;
     p.o = a.o;
     p.lse = a.lse;
@@ -1469,21 +1709,21 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     const size_t smem = C::kBarsOffset + sizeof(Bars) + 1024;
     cudaError_t e;
     if constexpr (D == 256)
-        e = cudaFuncSetAttribute(fwd_single_kernel<D, kF16>,
+        e = cudaFuncSetAttribute(fwd_single_kernel<D, kPrec>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
     else
-        e = cudaFuncSetAttribute(fwd_kernel<D, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fwd_kernel<D, kPrec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
     p.grid = grid;
     if constexpr (D == 256)
-        fwd_single_kernel<D, kF16><<<grid, kSingleThreads, smem, stream>>>(maps.q, maps.k,
+        fwd_single_kernel<D, kPrec><<<grid, C::kThreads, smem, stream>>>(maps.q, maps.k,
                                                                           maps.v, p);
     else
-        fwd_kernel<D, kF16><<<grid, kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
+        fwd_kernel<D, kPrec><<<grid, C::kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
         return e;
     const long long rows = static_cast<long long>(p.BH) * p.Nq;
@@ -1502,7 +1742,7 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<D, kF16>, static_cast<const float *>(p.ws_o),
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, kPrec>, static_cast<const float *>(p.ws_o),
                               static_cast<const float2 *>(p.ws_l), p);
 }
 
@@ -1535,22 +1775,29 @@ FwdPlan plan_fwd_streamk(int B, int H, int N, int Nk, int causal, int num_sms)
     return FwdPlan{1, static_cast<int>(slots)};
 }
 
+template <int D>
+cudaError_t launch_prec(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split, int num_sms,
+                        cudaStream_t stream)
+{
+    if (a.f16)
+        return launch<D, kPrecF16>(a, maps, split, num_sms, stream);
+    if (a.bf16p)
+        return launch<D, kPrecBf16P>(a, maps, split, num_sms, stream);
+    return launch<D, kPrecBf16>(a, maps, split, num_sms, stream);
+}
+
 cudaError_t launch_fwd_sm103(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
                              int num_sms, cudaStream_t stream)
 {
     switch (a.d) {
     case 64:
-        return a.f16 ? launch<64, true>(a, maps, split, num_sms, stream)
-                     : launch<64, false>(a, maps, split, num_sms, stream);
+        return launch_prec<64>(a, maps, split, num_sms, stream);
     case 96:
-        return a.f16 ? launch<96, true>(a, maps, split, num_sms, stream)
-                     : launch<96, false>(a, maps, split, num_sms, stream);
+        return launch_prec<96>(a, maps, split, num_sms, stream);
     case 128:
-        return a.f16 ? launch<128, true>(a, maps, split, num_sms, stream)
-                     : launch<128, false>(a, maps, split, num_sms, stream);
+        return launch_prec<128>(a, maps, split, num_sms, stream);
     case 256:
-        return a.f16 ? launch<256, true>(a, maps, split, num_sms, stream)
-                     : launch<256, false>(a, maps, split, num_sms, stream);
+        return launch_prec<256>(a, maps, split, num_sms, stream);
     }
     return cudaErrorInvalidValue;
 }

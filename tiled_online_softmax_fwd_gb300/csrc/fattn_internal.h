@@ -17,7 +17,9 @@ struct FwdArgs {
     int B, H, N, d;
     float scale;
     int causal;
-    int f16 = 0;  // 1: fp16 q, k, v, o (P in fp16); 0: bf16
+    int f16 = 0;    // 1: fp16 q, k, v, o (P in fp16); 0: bf16
+    int bf16p = 0;  // bf16 only: 0 = P in fp16 (V converted to fp16 on chip),
+                    // 1 = P in bf16 (V of any bf16 magnitude)
     int Nk = 0;   // keys per head (N: queries per head); the queries are the
                   // last N key positions under the causal mask
     // Element strides of o for (batch, head, row); all 0 = contiguous.
@@ -59,7 +61,8 @@ enum DeviceRole : uint32_t {
     kRoleMma = 2,
     kRoleSoftmax = 3,
     kRoleEpilogue = 4,
-    kRoleSelfTest = 5
+    kRoleSelfTest = 5,
+    kRoleConvert = 6
 };
 
 // tcgen05 / TMA kernel: one persistent CTA per SM.

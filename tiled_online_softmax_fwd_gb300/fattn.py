@@ -20,7 +20,7 @@ _LIB_PATH = os.path.join(_HERE, "_build", "libfattn.so")
 
 FATTN_OK = 0
 STATUS_NAMES = {0: "FATTN_OK", 1: "FATTN_ERR_INVALID_ARG", 2: "FATTN_ERR_UNSUPPORTED",
-                3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT"}
+                3: "FATTN_ERR_CUDA", 4: "FATTN_ERR_TIMEOUT", 5: "FATTN_ERR_RANGE"}
 EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_fp16", "attn_fwd_host",
             "attn_fwd_kv", "attn_fwd_kv_workspace_size", "attn_fwd_simt", "attn_fwd_strided",
             "attn_fwd_split",
@@ -269,11 +269,14 @@ def attn_fwd_kv(q, k, v, causal: bool = False, scale: float | None = None,
 
 
 def attn_fwd_strided(q, k, v, causal: bool = False, scale: float | None = None,
-                     num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
+                     num_splits: int = 0, workspace=None, out=None, lse=None, stream=None,
+                     bf16_p: bool = False):
     """attn_fwd_kv on 4-D bf16 or fp16 views [B, H, Nq|Nk, d] with any
     strides whose last dimension is contiguous (libfattn attn_fwd_strided):
     e.g. q, k, v sliced from one packed projection output.  ``out`` may be a
-    strided view too; by default a contiguous one is allocated."""
+    strided view too; by default a contiguous one is allocated.  ``bf16_p``
+    (bf16 only) rounds P to bf16 instead of fp16, for V of any bf16
+    magnitude (dtype 2)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 \
                 or t.dtype not in (torch.bfloat16, torch.float16) or t.stride(3) != 1 \
@@ -306,7 +309,7 @@ def attn_fwd_strided(q, k, v, causal: bool = False, scale: float | None = None,
                                      strides(v), strides(out), float(scale),
                                      1 if causal else 0, int(num_splits),
                                      workspace.data_ptr() if need > 0 else 0, workspace.numel(),
-                                     1 if q.dtype == torch.float16 else 0,
+                                     1 if q.dtype == torch.float16 else (2 if bf16_p else 0),
                                      _stream_handle(stream, q.device))
     _check(st, "attn_fwd_strided")
     return out, lse
@@ -393,7 +396,7 @@ def device_status(stream=None, device=None) -> int:
     word = ctypes.c_int(0)
     with torch.cuda.device(dev):
         st = lib.fattn_get_device_status(ctypes.byref(word), _stream_handle(stream, dev))
-    if st not in (FATTN_OK, 4):
+    if st not in (FATTN_OK, 4, 5):
         _check(st, "fattn_get_device_status")
     return word.value
 
