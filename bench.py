@@ -160,6 +160,28 @@ def max_over_ranks(world, x: float) -> float:
     return float(t.item())
 
 
+def nvtx_range(push: bool, name: str = "attn_fwd timed steps"):
+    """Open or close an NVTX range (a no-op where torch has no NVTX)."""
+    try:
+        if push:
+            torch.cuda.nvtx.range_push(name)
+        else:
+            torch.cuda.nvtx.range_pop()
+    except Exception:
+        pass
+
+
+def arm_config(w, world: int, in_digest: str, fp16: bool = False) -> dict:
+    """The workload as both arms name it (the GPU arm and the oracle's
+    reference arm print the same dictionary)."""
+    big = w.io_bytes > L2_BYTES
+    return {"workload": w.name + ("_fp16" if fp16 else ""), **w.describe(),
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": ("inputs larger than L2 (%d MB)" % (w.io_bytes // 10**6)) if big
+                  else "L2 flushed (256 MiB write) before every step, outside the timed events",
+            "input_digest": in_digest}
+
+
 # ------------------------------------------------------------------ CPU oracle
 def oracle_rows_for_steps(w, rows_all, steps):
     """One seeded row per head for each step (cycling through the sample)."""
@@ -214,10 +236,8 @@ def run_reference(args, world, rank):
         return 0
     import oracle
     w = ALL_WORKLOADS[args.workload]
-    g = torch.Generator("cpu").manual_seed(w.seed)
-    from tiled_online_softmax_fwd_gb300.inputs import make_qkv, sample_rows
-    q, k, v = make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, generator=g)
-    rows_all = sample_rows(w.B, w.H, w.N, 1024, g)
+    q, k, v, rows_all = make_workload(w, sample_per_head=1024)
+    in_digest = digest(q, k, v)
     qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
     threads = oracle.default_threads()
     plan = oracle_rows_for_steps(w, rows_all, args.warmup + args.steps)
@@ -235,7 +255,7 @@ def run_reference(args, world, rank):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, **w.describe()},
+            "config": arm_config(w, world, in_digest),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -537,7 +557,8 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     fattn.load()
     w = ALL_WORKLOADS[args.workload]
-    q, k, v, rows_all = make_workload(w, dtype=torch.float16 if args.fp16 else torch.bfloat16)
+    q, k, v, rows_all = make_workload(w, dtype=torch.float16 if args.fp16 else torch.bfloat16,
+                                      sample_per_head=1024)
     in_digest = digest(q, k, v)
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
     do = torch.empty_like(dq)
@@ -575,6 +596,8 @@ def run_gpu(args, world, rank, local):
 
     step_ms = None
     with ClockSampler(local) as clocks:
+        # An NVTX range marks the timed steps for a profiler's timeline.
+        nvtx_range(True)
         t_wall0 = time.perf_counter()
         if big:
             # One event between consecutive steps: the total gives the value,
@@ -599,6 +622,7 @@ def run_gpu(args, world, rank, local):
             step_ms = sorted(a.elapsed_time(b) for a, b in evs)
             kernel_ms = sum(step_ms) / args.steps
         wall_ms = (time.perf_counter() - t_wall0) * 1e3 / args.steps
+        nvtx_range(False)
     barrier(world)
     torch.cuda.synchronize()
     status = fattn.device_status()
@@ -637,11 +661,8 @@ def run_gpu(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if args.fp16 else "bf16", "data": "synthetic",
-        "config": {"workload": w.name + ("_fp16" if args.fp16 else ""), **w.describe(), "parallelism": "replicas" if world > 1 else "single",
-                   "splits": splits,
-                   "l2": ("inputs larger than L2 (%d MB)" % (w.io_bytes // 10**6)) if big
-                         else "L2 flushed (256 MiB write) before every step, outside the timed events",
-                   "input_digest": in_digest},
+        "config": arm_config(w, world, in_digest, args.fp16),
+        "splits": splits,
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
@@ -669,9 +690,7 @@ def run_gpu(args, world, rank, local):
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q, k, v, rows_all if rows_all is not None else
-                                            torch.arange(w.B * w.H * w.N),
-                                            budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v, rows_all, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
     return 0
 
