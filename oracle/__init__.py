@@ -62,6 +62,9 @@ def _open(path: str):
         lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_attn_bwd.argtypes = [dp] * 7 + [i64] * 4 + [ctypes.c_double, ctypes.c_int,
                                                                 ctypes.c_int]
+        lib.oracle_attn_bwd_dkv_rows.restype = ctypes.c_int
+        lib.oracle_attn_bwd_dkv_rows.argtypes = [dp] * 6 + [i64] * 4 + [
+            ctypes.c_double, ctypes.c_int, ctypes.POINTER(i64), i64, ctypes.c_int]
         lib.oracle_attn_bwd_dq_rows.restype = ctypes.c_int
         lib.oracle_attn_bwd_dq_rows.argtypes = [dp] * 5 + [i64] * 4 + [
             ctypes.c_double, ctypes.c_int, ctypes.POINTER(i64), i64, ctypes.c_int]
@@ -221,6 +224,25 @@ def attn_bwd_dq_rows(q, k, v, dout, scale: float, causal: bool, rows, threads: i
     if rc != 0:
         raise RuntimeError("oracle_attn_bwd_dq_rows failed with code %d" % rc)
     return out
+
+
+def attn_bwd_dkv_rows(q, k, v, dout, scale: float, causal: bool, rows,
+                      threads: int | None = None):
+    """Exact fp64 dk and dv for the given global KEY rows (b*H + h)*N + j:
+    ([R, d], [R, d]).  Each head holding a selected key costs one pass over
+    all of its query rows."""
+    qd, kd, vd, dd = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    B, H, N, d = qd.shape
+    rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    dk = np.zeros((rows_arr.size, d))
+    dv = np.zeros((rows_arr.size, d))
+    rc = _load().oracle_attn_bwd_dkv_rows(
+        _ptr(qd), _ptr(kd), _ptr(vd), _ptr(dd), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+        1 if causal else 0, rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        rows_arr.size, int(threads) if threads else default_threads())
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd_dkv_rows failed with code %d" % rc)
+    return dk, dv
 
 
 def attn_fwd_kv(q, k, v, scale: float, causal: bool, rows=None, threads: int | None = None):

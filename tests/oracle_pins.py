@@ -347,10 +347,10 @@ def pin_bwd_finite_difference(attn_bwd, attn_fwd):
                                                                                  grads[name][idx])
 
 
-def pin_bwd_invariants(attn_bwd, attn_bwd_dq_rows):
+def pin_bwd_invariants(attn_bwd, attn_bwd_dq_rows, attn_bwd_dkv_rows=None):
     """Each row of dS sums to zero, so the key gradients sum to zero over the
     keys; the value gradients sum to the sum of dO over the rows (rows of P
-    sum to one); and the dq rows mode equals the full dq rows."""
+    sum to one); and the dq rows and dk/dv rows modes equal the full rows."""
     for causal in (False, True):
         B, H, N, d = 2, 2, 23, 4
         q = _bf16_exact((B, H, N, d), 51, 2.0)
@@ -363,6 +363,12 @@ def pin_bwd_invariants(attn_bwd, attn_bwd_dq_rows):
         rows = np.array([0, 7, 22, 23, 50, 91], dtype=np.int64)
         _close(attn_bwd_dq_rows(q, k, v, g, 0.4, causal, rows), dq.reshape(-1, d)[rows], 1e-13,
                "dq rows mode")
+        if attn_bwd_dkv_rows is not None:
+            # Keys of several heads, out of order and repeated.
+            keys = np.array([91, 0, 22, 45, 23, 7, 68, 91, 46], dtype=np.int64)
+            dk_r, dv_r = attn_bwd_dkv_rows(q, k, v, g, 0.4, causal, keys)
+            _close(dk_r, dk.reshape(-1, d)[keys], 1e-13, "dk rows mode")
+            _close(dv_r, dv.reshape(-1, d)[keys], 1e-13, "dv rows mode")
 
 
 # --------------------------------------------------------------------------- Nq != Nk

@@ -86,7 +86,7 @@ def test_fwd_kv_oracle_meets_pins():
 def test_bwd_oracle_meets_pins():
     pins.pin_bwd_autograd(oracle.attn_bwd)
     pins.pin_bwd_finite_difference(oracle.attn_bwd, oracle.attn_fwd)
-    pins.pin_bwd_invariants(oracle.attn_bwd, oracle.attn_bwd_dq_rows)
+    pins.pin_bwd_invariants(oracle.attn_bwd, oracle.attn_bwd_dq_rows, oracle.attn_bwd_dkv_rows)
 
 
 BWD_MUTANTS = {
@@ -99,6 +99,13 @@ BWD_MUTANTS = {
     "dv_uses_ds": ("dvh[j * d + c] += p[j] * doh[i * d + c];",
                    "dvh[j * d + c] += (p[j] - 0.5 * p[j] * p[j]) * doh[i * d + c];"),
     "dp_wrong_operand": ("dot += doi[c] * vh[j * d + c];", "dot += doi[c] * kh[j * d + c];"),
+    # the dk/dv rows mode
+    "dkv_ds_without_D": ("const double ds = p * (dp - jb->D[i]);", "const double ds = p * dp;"),
+    "dkv_D_unnormalised": ("jb->D[i] = acc / l;", "jb->D[i] = acc;"),
+    "dkv_causal_skips_diagonal": ("for (int64_t i = jb->causal ? j : 0; i < N; ++i) {",
+                                  "for (int64_t i = jb->causal ? j + 1 : 0; i < N; ++i) {"),
+    "dkv_dv_weight_unnormalised": ("const double p = exp(jb->scale * dot - jb->m[i]) / jb->l[i];",
+                                   "const double p = exp(jb->scale * dot - jb->m[i]);"),
 }
 
 
@@ -135,11 +142,22 @@ def test_bwd_planted_mistake_is_caught(name, mutant_dir):
                                            r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                            r.size, 1) == 0
         return out
+
+    def dkv_rows(q, k, v, dout, scale, causal, rows):
+        qd, kd, vd, dd = (oracle._as_f64(t) for t in (q, k, v, dout))
+        B, H, N, d = qd.shape
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        dk, dv = np.zeros((r.size, d)), np.zeros((r.size, d))
+        assert lib.oracle_attn_bwd_dkv_rows(*(oracle._ptr(t) for t in (qd, kd, vd, dd, dk, dv)),
+                                            B, H, N, d, float(scale), int(causal),
+                                            r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                            r.size, 1) == 0
+        return dk, dv
     failed = 0
     with np.errstate(all="ignore"):
         for run in (lambda: pins.pin_bwd_autograd(attn_bwd),
                     lambda: pins.pin_bwd_finite_difference(attn_bwd, oracle.attn_fwd),
-                    lambda: pins.pin_bwd_invariants(attn_bwd, dq_rows)):
+                    lambda: pins.pin_bwd_invariants(attn_bwd, dq_rows, dkv_rows)):
             try:
                 run()
             except AssertionError:
