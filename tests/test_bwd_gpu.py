@@ -69,11 +69,32 @@ def test_bwd_matches_oracle(B, H, N, d, causal):
     _check("dv", gv, rv)
 
 
-@pytest.mark.parametrize("name", ["B4_H16_N4096_d128_causal", "B1_H32_N16384_d128_causal_sigma3"])
-def test_bwd_full_size_sampled(name):
-    """Full-size workloads: dQ on the seeded sample of rows against the
-    oracle; dK and dV through invariants that hold at any size (each row of dS
-    sums to zero, so sum_j dK_j = 0; rows of P sum to one, so
+# Full-size workloads: (name, heads whose key rows dK/dV are checked).  Each
+# checked head costs the oracle one pass over all of its query rows.
+BWD_WORKLOADS = [("B4_H16_N4096_d128_causal", 4), ("B1_H32_N16384_d128_causal_sigma3", 2),
+                 ("B2_H8_N65536_d64", 1)]
+
+
+def _key_rows(w, heads, per_head, seed):
+    """Seeded key rows of `heads` seeded heads: the first and last key of
+    each (the last is seen by the fewest queries under the mask) and
+    per_head - 2 random others; global ids (b*H + h)*N + j."""
+    g = torch.Generator().manual_seed(seed)
+    hs = torch.randperm(w.B * w.H, generator=g)[:heads]
+    out = []
+    for h in hs.tolist():
+        js = torch.randperm(w.N - 2, generator=g)[:per_head - 2] + 1
+        out.append(torch.cat([torch.tensor([0, w.N - 1]), js]).sort().values + h * w.N)
+    return torch.cat(out)
+
+
+@pytest.mark.parametrize("name,heads", BWD_WORKLOADS, ids=[n for n, _ in BWD_WORKLOADS])
+def test_bwd_full_size_sampled(name, heads):
+    """Full-size workloads in the benchmark's launch configuration: dQ on 64
+    seeded query rows per head, and dK, dV on 64 seeded key rows of a few
+    seeded heads, element by element against the oracle; plus the
+    invariants that hold at any size over every head (each row of dS sums
+    to zero, so sum_j dK_j = 0; rows of P sum to one, so
     sum_j dV_j = sum_i dO_i), relative to the tensors' own magnitude."""
     w = WORKLOADS[name]
     q, k, v, rows = make_workload(w, sample_per_head=64)
@@ -83,9 +104,12 @@ def test_bwd_full_size_sampled(name):
     gq, gk, gv = fattn.attn_bwd(dq_, dk_, dv_, o, lse, dg, causal=w.causal, scale=w.scale)
     torch.cuda.synchronize()
     assert fattn.device_status() == 0
-    sel = rows
-    ref = oracle.attn_bwd_dq_rows(q, k, v, g, w.scale, w.causal, sel.numpy())
-    _check("dq rows", gq.reshape(-1, w.d)[sel.cuda()], ref)
+    ref = oracle.attn_bwd_dq_rows(q, k, v, g, w.scale, w.causal, rows.numpy())
+    _check("dq rows", gq.reshape(-1, w.d)[rows.cuda()], ref)
+    keys = _key_rows(w, heads, 64, seed=78)
+    rk, rv = oracle.attn_bwd_dkv_rows(q, k, v, g, w.scale, w.causal, keys.numpy())
+    _check("dk rows", gk.reshape(-1, w.d)[keys.cuda()], rk)
+    _check("dv rows", gv.reshape(-1, w.d)[keys.cuda()], rv)
     sk = gk.double().sum(dim=2)
     assert (sk.abs().max() / gk.double().abs().sum(dim=2).max()).item() <= 1e-2
     sv = gv.double().sum(dim=2)
