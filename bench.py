@@ -687,6 +687,22 @@ def run_gpu(args, world, rank, local):
         line["step_quantiles_ms"] = {"p20": quantile(0.2), "p50": quantile(0.5),
                                      "p80": quantile(0.8)}
         line["algorithmic_gbs_p50"] = w.io_bytes / (quantile(0.5) * 1e-3) / 1e9
+    if not big:
+        # The launch floor under the same timing: one 1-element kernel between
+        # the same events after the same L2 flush (median of as many steps).
+        x = torch.zeros(1, device=dev)
+        floor = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            x.add_(1.0)
+            b.record(stream)
+            torch.cuda.synchronize()
+            floor.append(a.elapsed_time(b))
+        floor.sort()
+        line["us_per_step_p50"] = step_ms[len(step_ms) // 2] * 1e3
+        line["launch_floor_us"] = floor[len(floor) // 2] * 1e3
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:

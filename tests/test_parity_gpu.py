@@ -44,8 +44,7 @@ def gpu_run(q, k, v, causal, scale, entry=fattn.attn_fwd):
     return o.cpu(), lse.cpu()
 
 
-def check_case(name, q, k, v, causal, scale, rows=None, entry=fattn.attn_fwd,
-               mean_rule="floor"):
+def check_case(name, q, k, v, causal, scale, rows=None, entry=fattn.attn_fwd):
     o, lse = gpu_run(q, k, v, causal, scale, entry)
     B, H, N, d = q.shape
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal, rows=rows)
@@ -53,7 +52,7 @@ def check_case(name, q, k, v, causal, scale, rows=None, entry=fattn.attn_fwd,
     if rows is not None:
         idx = torch.as_tensor(rows, dtype=torch.int64)
         of, lf = of[idx], lf[idx]
-    r = compare(of, lf, o_ref, lse_ref, mean_rule=mean_rule)
+    r = compare(of, lf, o_ref, lse_ref)
     report(name, r)
     assert_parity(r, name)
     return o, lse
@@ -108,7 +107,7 @@ def test_workload_matches_oracle(name):
     w = WORKLOADS[name]
     q, k, v, rows = make_workload(w)
     check_case("workload_" + name, q, k, v, w.causal, w.scale,
-               rows=None if rows is None else rows.numpy(), mean_rule="stated")
+               rows=None if rows is None else rows.numpy())
 
 
 @pytest.mark.parametrize("name", WORKLOAD_ORDER)
@@ -157,7 +156,7 @@ def test_zero_queries(causal):
         ref = vd.mean(dim=2, keepdim=True).expand(B, H, N, d)
         ref_lse = torch.full((B, H, N), float(np.log(N)), dtype=torch.float64)
     r = compare(o.reshape(-1, d), lse.reshape(-1), ref.reshape(-1, d).numpy(),
-                ref_lse.reshape(-1).numpy(), mean_rule="floor")
+                ref_lse.reshape(-1).numpy())
     report("zero_queries_c%d" % causal, r)
     assert_parity(r, "zero queries")
 
@@ -281,7 +280,7 @@ def test_split_matches_oracle(B, H, N, d, causal, splits):
     o1, l1 = fattn.attn_fwd(dq, dk, dv, causal=causal, scale=scale)
     torch.cuda.synchronize()
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, scale, causal)
-    r = compare(o.cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref, mean_rule="floor")
+    r = compare(o.cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref)
     report("split_B%dH%dN%dd%d_c%d_s%s" % (B, H, N, d, causal, splits), r)
     assert_parity(r, "split")
     assert (o.float() - o1.float()).abs().max().item() <= 2 ** -5

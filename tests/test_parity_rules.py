@@ -4,13 +4,13 @@ import numpy as np
 from tests.parity import bf16_round, bf16_ulp, compare
 
 
-def _case(o_ref_vals, o_gpu_vals, lse_delta=0.0, pad=200, mean_rule="stated"):
+def _case(o_ref_vals, o_gpu_vals, lse_delta=0.0, pad=200):
     """One row; `pad` exactly represented elements dilute the mean so that
     the max rules can be probed on their own."""
     o_ref = np.array(list(o_ref_vals) + [0.25] * pad, dtype=np.float64).reshape(1, -1)
     o_gpu = np.array(list(o_gpu_vals) + [0.25] * pad, dtype=np.float64).reshape(1, -1)
     lse_ref = np.zeros(1)
-    return compare(o_gpu, lse_ref + lse_delta, o_ref, lse_ref, mean_rule=mean_rule)
+    return compare(o_gpu, lse_ref + lse_delta, o_ref, lse_ref)
 
 
 def test_bf16_helpers():
@@ -60,18 +60,18 @@ def test_exempt_only_where_the_floor_exceeds_the_bound():
 
 
 def test_mean_rule_follows_the_oracle_floor():
-    # Every element of order one, off by 1.5e-3: the stated mean bound fails.
+    # Every element of order one, off by 1.5e-3: the floor (~7e-4 on average)
+    # is below the stated bound, so 1e-3 applies and the case fails.
     ref = np.linspace(0.3, 0.9, 64) + 1e-3 / 3
-    gpu = ref + 1.5e-3
-    r = _case(ref, gpu, pad=0)
-    assert not r["ok"] and r["mean_rule"] == "stated"
-    # Asked for the floor rule, such a case gets it only when its own mean
-    # floor is above 5e-4.
-    r = _case(ref, gpu, pad=0, mean_rule="floor")
-    assert r["floor_mean"] > 5e-4 and r["mean_rule"] == "floor" and r["ok"], r
-    small = np.linspace(0.01, 0.06, 64) + 1e-5
-    r = _case(small, small + 1.5e-3, pad=0, mean_rule="floor")
-    assert r["floor_mean"] <= 5e-4 and r["mean_rule"] == "stated" and not r["ok"]
+    r = _case(ref, ref + 1.5e-3, pad=0)
+    assert r["floor_mean"] <= 1e-3 and r["mean_rule"] == "stated" and not r["ok"]
+    # Elements of order 3-4, where the rounding floor alone averages above
+    # 1e-3: no bf16 output meets the stated mean, so 2 x the floor applies.
+    big = np.linspace(2.1, 3.9, 64) + 2 ** -9
+    r = _case(big, bf16_round(big), pad=0)
+    assert r["floor_mean"] > 1e-3 and r["mean_rule"] == "floor" and r["ok"], r
+    r = _case(big, big + 3 * r["floor_mean"], pad=0)
+    assert not r["ok"]
 
 
 def test_lse_and_mean_bounds():
