@@ -18,9 +18,11 @@
 //               alternate (ping-pong) so that one computes exponentials
 //               while the tensor core works on the other tile.  Each thread
 //               owns one query row: it reads its S row from TMEM, applies
-//               the causal / tail mask, updates m and l, writes P (bf16)
+//               the causal / tail mask, updates m and l, writes P (16-bit)
 //               back into TMEM over its S row, rescales its O row in TMEM
 //               when needed, and finally normalises and stores O and lse.
+//   warps 10-11 (bf16 inputs) V converters: each V tile is rewritten in
+//               place from bf16 to fp16 before the P V product reads it.
 // A work unit is two consecutive 128-row Q tiles of one (batch, head).  The
 // units are ordered heaviest first (for the causal mask the work of a Q tile
 // grows with its index) and dealt to the CTAs in a serpentine order so that
@@ -39,18 +41,23 @@
 // maximum exceeds it by more than kRescaleLog2 (so O and l need rescaling
 // rarely); until then p may exceed 1 by at most 2^kRescaleLog2.  This is
 // exact algebra: O and l always refer to the same m, so O / l and
-// lse = ln2 * (m + log2 l) are unchanged.  Two row sums are kept: l of the
-// fp32 probabilities, for lse, and l_round, which normalises O and stands for
-// the sum of the bf16-rounded probabilities that actually enter P V, so that
-// the rounding of a dominant p cancels in O / l_round.  For bf16 with d = 64
-// it is that sum exactly, formed by the tensor cores: V is extended by a
-// constant column of ones (its own 16 KB swizzle atom after the K/V ring), so
-// column d of the O accumulator is the row sum of the rounded P, summed in
-// fp32 and rescaled together with O (see Cfg::kOnes).  Otherwise l_round is l
-// minus the rounding error of the largest p of each key tile (the only terms
-// whose rounding can move O by more than the bf16 output rounding; the rest
-// are at most 2^-9 of the remaining weight and of random sign), which costs
-// one exponential per tile instead of a second sum over all 128 keys.
+// lse = ln2 * (m + log2 l) are unchanged.
+//
+// Precision of P (kPrec).  P is rounded to fp16 for bf16 and for fp16
+// inputs, and O is normalised by l, the fp32 sum of the unrounded p: with
+// P in bf16 the bf16 output of peaked rows misses a 1e-2 bound where |O| is
+// in [2, 4), since P's own rounding moves O across a rounding midpoint.  For
+// bf16 inputs V is converted to fp16 on chip (run_convert).  The bf16-P mode
+// (kPrecBf16P, for V beyond the fp16 range) keeps a second sum, l_round,
+// which normalises O and stands for the sum of the bf16-rounded
+// probabilities that enter P V, so that the rounding of a dominant p cancels
+// in O / l_round.  With d = 64 it is that sum exactly, formed by the tensor
+// cores: V is extended by a constant column of ones (its own 16 KB swizzle
+// atom after the K/V ring), so column d of the O accumulator is the row sum
+// of the rounded P, summed in fp32 and rescaled together with O (see
+// Cfg::kOnes).  Otherwise l_round is l minus the rounding error of the
+// largest p of each key tile, which costs one exponential per tile instead
+// of a second sum over all 128 keys.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <float.h>
