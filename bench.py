@@ -629,6 +629,7 @@ def run_gpu(args, world, rank, local):
     ms = max_over_ranks(world, kernel_ms)
     value = world * w.flops / (ms * 1e-3) / 1e12
     achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+    prepass = int(not args.fp16 and fattn.v_prepass_planned(w.N, w.d, w.causal))
 
     # End to end through the C ABI with host buffers (pinned), copies timed.
     e2e = None
@@ -669,11 +670,13 @@ def run_gpu(args, world, rank, local):
                      "traffic_source": traffic_src,
                      "algorithmic_flops_per_launch": w.flops,
                      "algorithmic_bytes_per_launch": w.io_bytes},
-        "gpu_launches": args.steps * (2 if splits > 1 else 1),
-        "kernel": "fattn %s<%d> (tcgen05/TMA, persistent)%s" % (
+        "v_prepass": prepass,
+        "gpu_launches": args.steps * (1 + (splits > 1) + prepass),
+        "kernel": "fattn %s<%d> (tcgen05/TMA, persistent)%s%s%s" % (
             "fwd_single_kernel" if w.d == 256 else "fwd_kernel", w.d,
-            " + combine_kernel, %d key-range splits; roofline.achieved uses the whole step" % splits
-            if splits > 1 else ""),
+            " + combine_kernel, %d key-range splits" % splits if splits > 1 else "",
+            " after v_to_f16_kernel (V pre-pass)" if prepass else "",
+            "; roofline.achieved uses the whole step" if splits > 1 or prepass else ""),
         "wall_ms_per_step": wall_ms,
         "clocks": clocks.summary(),
         "device_status": status,
@@ -729,8 +732,13 @@ def main():
     ap.add_argument("--fp16", action="store_true", help="fp16 inputs through attn_fwd_fp16")
     ap.add_argument("--split", default="auto", choices=["auto", "off"],
                     help="key-range split when the library recommends one (auto) or never")
+    ap.add_argument("--v-conversion", default="auto", choices=["auto", "on_chip", "prepass"],
+                    help="where bf16 calls round V to fp16 (fattn_set_v_conversion)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.impl != "reference":
+        from tiled_online_softmax_fwd_gb300 import fattn
+        fattn.set_v_conversion(args.v_conversion)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     if args.op and args.op.startswith("bwd_"):

@@ -36,7 +36,10 @@
  *     the stream has been synchronised.  Arguments are checked synchronously
  *     and nothing is enqueued when a check fails.  B*H*N == 0 is a no-op that
  *     returns FATTN_OK.
- *   - The library keeps no per-call allocations and no hidden workspace.
+ *   - The caller provides every buffer of a call.  The one memory the
+ *     library takes on its own is the scratch of the V pre-pass (see
+ *     fattn_set_v_conversion), stream-ordered on the call's stream from a
+ *     library-owned pool; attn_fwd_split_noalloc never takes it.
  *   - Calls are thread-safe; concurrent calls on different streams may run
  *     concurrently on the device.
  */
@@ -78,8 +81,9 @@ typedef enum fattn_status {
  * to bf16, the inputs' type): with bf16 P the bf16 output misses the stated
  * 1e-2 bound on peaked rows whose |O| is in [2, 4), where one bf16 ulp is
  * 0.0156 and P's rounding moves O across a rounding midpoint.  Both operands
- * of a tensor-core product share one type, so each V tile is converted to
- * fp16 on chip.  That is exact for |v| < 65520; a V element of larger
+ * of a tensor-core product share one type, so V is rounded to fp16 (on
+ * chip, or by a pre-pass: see fattn_set_v_conversion; the bits are the
+ * same).  That is exact for |v| < 65520; a V element of larger
  * magnitude becomes infinite in the product.  Any output row that comes out
  * non-finite -- from such a V element, or from non-finite inputs -- makes
  * the kernel record FATTN_ERR_RANGE in the device status word (those rows
@@ -121,8 +125,8 @@ fattn_status_t attn_fwd_fp16(const void *q, const void *k, const void *v, void *
  * enqueued on `stream`.  Calls are serialised inside the library.  Host
  * buffers should be page-locked (cudaHostAlloc / pinned) for asynchronous
  * full-bandwidth copies; pageable memory works but is slower.  Device
- * buffers follow attn_fwd's rules.  The library allocates no memory (the
- * helper streams and events are created once per device).  The return value
+ * buffers follow attn_fwd's rules.  The helper streams and events are
+ * created once per device; the V pre-pass scratch is as for attn_fwd.  The return value
  * includes any error raised while the streams drained.
  */
 fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host,
@@ -130,6 +134,51 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
                              void *dq, void *dk, void *dv, void *do_, float *dlse,
                              int B, int H, int N, int d, float scale, int causal,
                              struct CUstream_st *stream);
+
+/*
+ * V conversion.  For bf16 inputs with P in fp16 (attn_fwd, attn_fwd_split,
+ * attn_fwd_kv, attn_fwd_strided with dtype 0, attn_fwd_host) every V element
+ * is rounded to fp16 for the P V product, in one of two places:
+ *   - on chip: converter warps of the forward kernel round each V tile in
+ *     shared memory, once for every work unit that reads it; no memory is
+ *     taken;
+ *   - by a pre-pass: one more kernel rounds all of V once into device scratch
+ *     of B*H*Nk*d*2 bytes (Nk: keys per head), which the forward kernel then
+ *     reads instead of v.  The scratch is taken on `stream` from a
+ *     library-owned stream-ordered memory pool of the current device and
+ *     given back on `stream` after the forward kernel; the pool keeps what is
+ *     given back for later calls until fattn_trim_scratch.
+ * Both round with the same function, so the outputs are bit for bit the
+ * same.  fattn_set_v_conversion chooses for the whole process:
+ *   FATTN_V_CONVERT_AUTO (the default): the pre-pass where each V tile
+ *     would otherwise be rounded for many work units.  With T = ceil(N/128)
+ *     query tiles per head, units U = T for d = 256 and ceil(T/2) otherwise,
+ *     and visits = U/2 with the causal mask, U without: the pre-pass from 24
+ *     visits at d = 64, 8 at d = 96, 16 at d = 128 and 12 at d = 256 (where
+ *     it was measured to be faster on a GB300), on chip below;
+ *   FATTN_V_CONVERT_ON_CHIP: never the pre-pass, so no call takes memory;
+ *   FATTN_V_CONVERT_PREPASS: the pre-pass for every shape.
+ * Whatever the setting, a call converts on chip when `stream` is being
+ * captured into a CUDA graph or the scratch cannot be had (out of memory),
+ * and attn_fwd_split_noalloc always does.  Each call reads the setting once.
+ * Returns the previous setting, or -1 (nothing changed) for an unknown mode.
+ *
+ * fattn_v_prepass_planned: 1 if a call with N queries per head, head
+ * dimension d and mask `causal` would take the pre-pass under the current
+ * setting (scratch permitting), 0 if it converts on chip, -1 for an
+ * unsupported d, N < 0 or causal not 0 or 1.
+ *
+ * fattn_trim_scratch gives the pool's unused memory on every device back to
+ * the system (memory of calls still in flight stays).  FATTN_OK, or
+ * FATTN_ERR_CUDA.  Like all per-device state, the pools do not survive
+ * cudaDeviceReset.
+ */
+#define FATTN_V_CONVERT_AUTO 0
+#define FATTN_V_CONVERT_ON_CHIP 1
+#define FATTN_V_CONVERT_PREPASS 2
+int fattn_set_v_conversion(int mode);
+int fattn_v_prepass_planned(int N, int d, int causal);
+fattn_status_t fattn_trim_scratch(void);
 
 /*
  * Key-range split (split-KV).  When B*H*ceil(N/256) work units are fewer

@@ -225,3 +225,38 @@ def test_rowop_arguments_are_checked(lib):
         assert f(0, 0, 0, 16, 0, None) == OK                       # empty: no-op
     assert lib.fattn_softmax_rows(A, A + 8, 4, 4, 0, None) == INVALID   # partial overlap
     assert lib.fattn_row_sum(A, A + 8, 4, 4, 0, None) == INVALID        # sums inside input
+
+
+def test_v_conversion_setting(lib):
+    """Host-only: the setting is a process-wide integer, no device call."""
+    prev = lib.fattn_set_v_conversion(1)
+    assert prev in (0, 1, 2)
+    try:
+        assert lib.fattn_set_v_conversion(3) == -1 and lib.fattn_set_v_conversion(-1) == -1
+        assert lib.fattn_set_v_conversion(2) == 1  # the invalid calls changed nothing
+        assert lib.fattn_v_prepass_planned(128, 64, 0) == 1
+        assert lib.fattn_v_prepass_planned(0, 64, 0) == 0  # nothing to convert
+        assert lib.fattn_set_v_conversion(0) == 2
+        # Automatic: visits = units per head (halved under the causal mask)
+        # against 24 / 8 / 16 / 12 for d = 64 / 96 / 128 / 256.
+        # The first N that takes the pre-pass, per (d, causal): e.g. d = 64
+        # without the mask needs ceil(T/2) >= 24, T = ceil(N/128) >= 47.
+        first = {(64, 0): 46 * 128 + 1, (64, 1): 94 * 128 + 1, (96, 0): 14 * 128 + 1,
+                 (96, 1): 30 * 128 + 1, (128, 0): 30 * 128 + 1, (128, 1): 62 * 128 + 1,
+                 (256, 0): 11 * 128 + 1, (256, 1): 23 * 128 + 1}
+        for (d, causal), n in first.items():
+            assert lib.fattn_v_prepass_planned(n, d, causal) == 1, (n, d, causal)
+            assert lib.fattn_v_prepass_planned(n - 1, d, causal) == 0, (n - 1, d, causal)
+        for n, d, causal, want in [(16384, 128, 1, 1), (4096, 128, 1, 0), (256, 64, 0, 0),
+                                   (4096, 64, 0, 0), (65536, 64, 0, 1), (4096, 96, 1, 1),
+                                   (8192, 256, 1, 1)]:
+            assert lib.fattn_v_prepass_planned(n, d, causal) == want, (n, d, causal)
+        assert lib.fattn_v_prepass_planned(512, 80, 0) == -1
+        assert lib.fattn_v_prepass_planned(-1, 128, 0) == -1
+        assert lib.fattn_v_prepass_planned(512, 128, 2) == -1
+        assert fattn.set_v_conversion("on_chip") == "auto"
+        with pytest.raises(ValueError):
+            fattn.set_v_conversion("gpu")
+    finally:
+        lib.fattn_set_v_conversion(prev)
+

@@ -8,7 +8,8 @@ second call finds the first call's leftovers in the shared scratch):
   * against attn_fwd_split given a caller-allocated workspace: the same
     kernels, split count and merge order, so the bits must be identical;
   * against the fp64 oracle, with the tolerances of every parity test.
-Also: one split (no scratch at all, exactly attn_fwd), the largest shape whose
+Also: one split (no scratch at all, attn_fwd's bits, also where attn_fwd
+itself would round V in a pre-pass that needs memory), the largest shape whose
 scratch fits the array (32 bytes short of 32 MiB) and the next one up, which
 is refused.
 
@@ -71,14 +72,19 @@ def test_noalloc_matches_workspace_entry_point_and_oracle_twice(lib, B, H, N, d,
         assert_parity(r, "noalloc call %d" % call)
 
 
-def test_noalloc_single_split_is_attn_fwd(lib):
-    q, k, v = make_qkv(2, 2, 1000, 128, seed=911)
+@pytest.mark.parametrize("B,H,N,d", [(2, 2, 1000, 128), (1, 2, 3072, 256)])
+def test_noalloc_single_split_is_attn_fwd(lib, B, H, N, d):
+    """The no-allocation call always rounds V on chip; at d = 256 with 3072
+    queries attn_fwd takes the V pre-pass instead.  Same bits either way."""
+    q, k, v = make_qkv(B, H, N, d, seed=911)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
-    scale = fattn.default_scale(128)
-    ref_o, ref_l = fattn.attn_fwd(dq, dk, dv, causal=True, scale=scale)
-    o, lse = _outputs(dq)
-    assert _noalloc(lib, dq, dk, dv, o, lse, True, scale, 1) == OK
-    torch.cuda.synchronize()
+    scale = fattn.default_scale(d)
+    with fattn.v_conversion("auto"):
+        assert fattn.v_prepass_planned(N, d, True) == (d == 256)
+        ref_o, ref_l = fattn.attn_fwd(dq, dk, dv, causal=True, scale=scale)
+        o, lse = _outputs(dq)
+        assert _noalloc(lib, dq, dk, dv, o, lse, True, scale, 1) == OK
+        torch.cuda.synchronize()
     assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
 
 

@@ -8,6 +8,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "fattn.h"
@@ -28,6 +29,7 @@ struct DeviceInfo {
     bool probed = false;
     bool supported = false;
     int num_sms = 0;
+    int dev = -1;
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
@@ -54,6 +56,7 @@ fattn_status_t current_device(int *dev, DeviceInfo *info)
             return cuda_fail(e);
         d.supported = (major == 10 && minor == 3);  // the kernels are built for sm_103a only
         d.num_sms = sms;
+        d.dev = *dev;
         d.probed = true;
     }
     *info = d;
@@ -312,13 +315,88 @@ fattn_status_t validate(const void *q, const void *k, const void *v, const void 
     return FATTN_OK;
 }
 
+// ---------------------------------------------------------------- V pre-pass
+// For bf16 inputs with P in fp16, V is rounded to fp16 either on chip, per
+// work unit, by the forward kernel's converter warps, or once per call by a
+// pre-pass into scratch that the forward kernel then reads (the same bits
+// either way).  The scratch comes from one stream-ordered memory pool per
+// device, created on first use, which keeps freed blocks for the next call
+// (release threshold: unlimited), so a steady loop of calls maps no new
+// device memory; fattn_trim_scratch returns them.
+std::atomic<int> g_v_convert{FATTN_V_CONVERT_AUTO};
+std::mutex g_pool_mutex;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+// FATTN_V_CONVERT_AUTO: the pre-pass where it was measured to pay.  The
+// converter warps round each V tile once for every work unit that reads it
+// (a pair of 128-row Q tiles, one Q tile at d = 256), on average `visits`
+// times: the units per head, halved under the causal mask.  The pre-pass
+// costs a fixed 4 bytes of HBM traffic per V element and one more launch.
+// On one GB300 (bf16, L2 flushed) it was faster from these visits on and
+// slower below them: d = 64 from 24 (16: -0.4 %, 24: +2 %, 256: +4 %);
+// d = 96 from 8 (4: -3 % to +1 %, 8: +4.5 %); d = 128 from 16 (12: -1.5 %,
+// 16: +0.6 % causal and +3 % not, 32: +3 to +5 %); d = 256 from 12 (8: -1 %
+// to -6 %, 12: +13 %, 32: +36 %).
+bool want_prepass(int Nq, int d, int causal)
+{
+    if (Nq <= 0)
+        return false;
+    const int mode = g_v_convert.load(std::memory_order_relaxed);
+    if (mode != FATTN_V_CONVERT_AUTO)
+        return mode == FATTN_V_CONVERT_PREPASS;
+    const long long tiles = (static_cast<long long>(Nq) + 127) / 128;
+    const long long units = d == 256 ? tiles : (tiles + 1) / 2;
+    const long long visits2 = causal ? units : 2 * units;  // twice the visits
+    const long long need2 = d == 64 ? 48 : d == 96 ? 16 : d == 128 ? 32 : 24;
+    return visits2 >= need2;
+}
+
+// Scratch of `bytes` on `stream`, or nullptr where there is none to be had
+// (the stream is being captured into a graph, the pool cannot be created or
+// the device is out of memory): the caller then converts on chip.
+void *prepass_scratch(int dev, size_t bytes, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    cudaMemPool_t pool = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_pool_mutex);
+        if (g_pool[dev] == nullptr) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t created = nullptr;
+            if (cudaMemPoolCreate(&created, &props) != cudaSuccess) {
+                cudaGetLastError();
+                return nullptr;
+            }
+            uint64_t keep = UINT64_MAX;
+            cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep);
+            g_pool[dev] = created;
+        }
+        pool = g_pool[dev];
+    }
+    void *ptr = nullptr;
+    if (cudaMallocFromPoolAsync(&ptr, bytes, pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return ptr;
+}
+
 // Enqueue one validated forward call with N queries and Nk keys per head
 // (split.splits > 1: key-range split with the caller's scratch).
+// may_allocate false: no device memory is taken (V is converted on chip).
 fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const void *k,
                       const void *v, void *o, float *lse, int B, int H, int N, int Nk, int d,
                       float scale, int causal, cudaStream_t stream,
                       const fattn::FwdSplit &split = fattn::FwdSplit{1, nullptr, nullptr},
-                      const Layout *L = nullptr)
+                      const Layout *L = nullptr, bool may_allocate = true)
 {
     fattn::FwdArgs a{q, k, v, o, lse, B, H, N, d, scale, causal};
     const bool f16 = which == Kernel::kTcgen05F16;
@@ -341,17 +419,37 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
         a.o_sn = lay.o[2];
         fattn::FwdMaps maps;
         if ((s = make_map4(encode, &maps.q, q, N, d, H, B, lay.q, f16)) != FATTN_OK ||
-            (s = make_map4(encode, &maps.k, k, Nk, d, H, B, lay.k, f16)) != FATTN_OK ||
-            (s = make_map4(encode, &maps.v, v, Nk, d, H, B, lay.v, f16)) != FATTN_OK)
+            (s = make_map4(encode, &maps.k, k, Nk, d, H, B, lay.k, f16)) != FATTN_OK)
             return s;
-        e = fattn::launch_fwd_sm103(a, maps, split, info.num_sms, stream);
+        void *v16 = nullptr;
+        if (which == Kernel::kTcgen05 && may_allocate && want_prepass(N, d, causal))
+            v16 = prepass_scratch(info.dev, static_cast<size_t>(B) * H * Nk * d * 2, stream);
+        if (v16 != nullptr) {
+            const Layout dense = dense_layout(H, N, Nk, d);
+            a.v16 = v16;
+            a.v_sb = lay.v[0];
+            a.v_sh = lay.v[1];
+            a.v_sn = lay.v[2];
+            s = make_map4(encode, &maps.v, v16, Nk, d, H, B, dense.v, true);
+        } else {
+            s = make_map4(encode, &maps.v, v, Nk, d, H, B, lay.v, f16);
+        }
+        e = s == FATTN_OK ? fattn::launch_fwd_sm103(a, maps, split, info.num_sms, stream)
+                          : cudaSuccess;
+        if (v16 != nullptr) {
+            const cudaError_t ef = cudaFreeAsync(v16, stream);
+            if (e == cudaSuccess)
+                e = ef;
+        }
+        if (s != FATTN_OK)
+            return s;
     }
     return e == cudaSuccess ? FATTN_OK : cuda_fail(e);
 }
 
 fattn_status_t forward(Kernel which, const void *q, const void *k, const void *v, void *o,
                        float *lse, int B, int H, int N, int d, float scale, int causal,
-                       cudaStream_t stream)
+                       cudaStream_t stream, bool may_allocate = true)
 {
     bool empty = false;
     int dev = 0;
@@ -360,7 +458,8 @@ fattn_status_t forward(Kernel which, const void *q, const void *k, const void *v
         validate(q, k, v, o, lse, B, H, N, N, d, scale, causal, &empty, &dev, &info);
     if (s != FATTN_OK || empty)
         return s;
-    return launch(which, info, q, k, v, o, lse, B, H, N, N, d, scale, causal, stream);
+    return launch(which, info, q, k, v, o, lse, B, H, N, N, d, scale, causal, stream,
+                  fattn::FwdSplit{1, nullptr, nullptr}, nullptr, may_allocate);
 }
 
 constexpr int kMaxSplits = 64;
@@ -428,7 +527,7 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
                              int B, int H, int N, int Nk, int d, float scale, int causal,
                              int num_splits, void *workspace, size_t workspace_bytes,
                              cudaStream_t stream, const Layout *L = nullptr,
-                             Kernel which = Kernel::kTcgen05)
+                             Kernel which = Kernel::kTcgen05, bool may_allocate = true)
 {
     if (num_splits < 0 || num_splits > kMaxSplits)
         return FATTN_ERR_INVALID_ARG;
@@ -444,7 +543,7 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
         num_splits = auto_slots(B, H, N, Nk, d, causal, info.num_sms, &streamk);
     if (num_splits == 1)
         return launch(which, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream,
-                      fattn::FwdSplit{1, nullptr, nullptr}, L);
+                      fattn::FwdSplit{1, nullptr, nullptr}, L, may_allocate);
     const size_t need = split_ws_bytes(B, H, N, d, num_splits);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need)
         return FATTN_ERR_INVALID_ARG;
@@ -463,7 +562,8 @@ fattn_status_t forward_split(const void *q, const void *k, const void *v, void *
         num_splits, reinterpret_cast<float *>(ws),
         reinterpret_cast<float *>(ws + align_up(split_ws_o_bytes(B, H, N, d, num_splits), kWsAlign)),
         streamk};
-    return launch(which, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream, split, L);
+    return launch(which, info, q, k, v, o, lse, B, H, N, Nk, d, scale, causal, stream, split, L,
+                  may_allocate);
 }
 
 // ---------------------------------------------------------------- no-allocation split
@@ -648,8 +748,9 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
     fattn_status_t s = check_shape(B, H, N, d, scale, causal, &empty);
     if (s != FATTN_OK || empty)
         return s;
-    if (num_splits == 1)  // no scratch needed: exactly attn_fwd
-        return forward(Kernel::kTcgen05, q, k, v, o, lse, B, H, N, d, scale, causal, stream);
+    if (num_splits == 1)  // no scratch needed: attn_fwd's result (V converted on chip)
+        return forward(Kernel::kTcgen05, q, k, v, o, lse, B, H, N, d, scale, causal, stream,
+                       false);
     if (split_ws_bytes(B, H, N, d, num_splits) > kNoAllocScratchBytes)
         return FATTN_ERR_UNSUPPORTED;  // beyond the fixed scratch: use attn_fwd_split
     int dev = 0;
@@ -660,7 +761,34 @@ fattn_status_t attn_fwd_split_noalloc(const void *q, const void *k, const void *
     if ((s = noalloc_scratch(dev, &scratch)) != FATTN_OK)
         return s;
     return forward_split(q, k, v, o, lse, B, H, N, N, d, scale, causal, num_splits, scratch,
-                         kNoAllocScratchBytes, stream);
+                         kNoAllocScratchBytes, stream, nullptr, Kernel::kTcgen05, false);
+}
+
+int fattn_set_v_conversion(int mode)
+{
+    if (mode < FATTN_V_CONVERT_AUTO || mode > FATTN_V_CONVERT_PREPASS)
+        return -1;
+    return g_v_convert.exchange(mode);
+}
+
+int fattn_v_prepass_planned(int N, int d, int causal)
+{
+    if (N < 0 || (d != 64 && d != 96 && d != 128 && d != 256) || (causal != 0 && causal != 1))
+        return -1;
+    return want_prepass(N, d, causal) ? 1 : 0;
+}
+
+fattn_status_t fattn_trim_scratch(void)
+{
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    for (int dev = 0; dev < kMaxDevices; ++dev) {
+        if (g_pool[dev] == nullptr)
+            continue;
+        const cudaError_t e = cudaMemPoolTrimTo(g_pool[dev], 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+    }
+    return FATTN_OK;
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int N, int d)

@@ -95,12 +95,16 @@ constexpr uint32_t kChunkBytes = kBM * 64 * 2;  // one 128-row x 64-column bf16 
 constexpr int kPrecBf16 = 0;    // bf16 q, k, v, o; P in fp16 (V converted)
 constexpr int kPrecF16 = 1;     // fp16 q, k, v, o; P in fp16
 constexpr int kPrecBf16P = 2;   // bf16 q, k, v, o; P in bf16 (V of any bf16 magnitude)
+constexpr int kPrecBf16V16 = 3; // bf16 q, k, o; V rounded to fp16 beforehand; P in fp16
 
 template <int D, int kPrec = kPrecBf16>
 struct Cfg {
     static constexpr bool kInF16 = kPrec == kPrecF16;    // q, k, v, o in fp16
     static constexpr bool kPF16 = kPrec != kPrecBf16P;   // P (and V in P V) in fp16
     static constexpr bool kConv = kPrec == kPrecBf16;    // converter warps
+    // V rounded from bf16 to fp16 (on chip or by v_to_f16_kernel): an
+    // infinity from |v| >= 65520 is reported by the epilogue.
+    static constexpr bool kVRounded = kConv || kPrec == kPrecBf16V16;
     // Threads: the two-tile kernel has 8 softmax warps, a TMA warp and an
     // MMA warp; the one-tile kernel 4, 1 and 1; both add 2 converter warps.
     static constexpr int kThreads = (D == 256 ? 192 : 320) + (kConv ? 64 : 0);
@@ -336,6 +340,9 @@ __device__ void run_load(const Params &p, Bars &b, uint32_t smem_base, const CUt
     uint32_t pos = 0;  // K/V ring position (K_j, V_j alternate)
     bool ok = true;
     int last_q_parity[2] = {-1, -1};
+    // Launched behind the V pre-pass (kPrecBf16V16): its writes are visible
+    // after this wait.  Without a preceding dependent grid it returns at once.
+    grid_dependency_wait();
     for (int r = 0; ok; ++r) {
         Unit u;
         if (!cta_unit(p, b, r, u))
@@ -884,12 +891,12 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
     const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
     const bool live = row < p.Nq;
     const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
-    // With V converted to fp16 (kPrecBf16), a V element of magnitude 65520
+    // With V converted to fp16 (kPrecBf16, kPrecBf16V16), a V element of magnitude 65520
     // or more turns into an infinity: a non-finite output row (which
     // non-finite inputs also give) records FATTN_ERR_RANGE.
     float nf[4] = {0.f, 0.f, 0.f, 0.f};
     auto check = [&](const uint32_t (&o)[32]) {
-        if constexpr (Cfg<D, kPrec>::kConv)
+        if constexpr (Cfg<D, kPrec>::kVRounded)
             nonfinite_acc(o, nf);
     };
     if constexpr (kStaged) {
@@ -991,7 +998,7 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
         if (live)
             p.ws_l[srow] = make_float2(m + log2f(l), m + log2f(l_norm));
     }
-    if constexpr (Cfg<D, kPrec>::kConv) {
+    if constexpr (Cfg<D, kPrec>::kVRounded) {
         const float acc = (nf[0] + nf[1]) + (nf[2] + nf[3]);
         if (live && acc != acc) {
             const uint32_t code = 5u /* FATTN_ERR_RANGE */ | (kRoleEpilogue << 8) |
@@ -1220,6 +1227,7 @@ __device__ void run_load_single(const Params &p, Bars &b, uint32_t smem_base,
     // v_full: each barrier then sees only its own tiles, in order, and the
     // next phase's parity is kept per stage and barrier.
     uint32_t kbits = 0, vbits = 0, last_v = 0, used = 0;
+    grid_dependency_wait();  // see run_load
     auto load_tile = [&](const CUtensorMap *m, int row, int hh, int bb, bool is_v) {
         const uint32_t stage = pos % C::kStages;
         ok = warp_wait(smem_addr(&b.kv_empty[stage]), ((pos / C::kStages) & 1) ^ 1, abort);
@@ -1671,6 +1679,62 @@ __global__ void __launch_bounds__(128)
         p.lse[row] = (mx_e + log2f(se)) * kLn2;
 }
 
+// ------------------------------------------------------------------ V pre-pass
+// kPrecBf16V16: V rounded from bf16 to fp16 once, into a contiguous
+// [B][H][Nk][d] buffer that the forward grid's V tensor map reads, instead of
+// once per work unit in shared memory.  The rounding is bf16x2_to_f16x2, the
+// converter warps' own, so both routes give the same bits.  One 16-byte
+// granule (8 elements) per step and kVBatch steps in flight per thread, over
+// a single wave of CTAs; the grid lets the forward grid launch at once
+// (programmatic dependent launch), whose load warp waits for these writes in
+// griddepcontrol.wait before its first copy.
+struct VConv {
+    const uint4 *src;  // the caller's V
+    uint4 *dst;        // fp16 copy, contiguous
+    long long granules;          // B * H * Nk * d / 8
+    long long sb, sh, sn;        // strides of src (batch, head, row) in granules
+    int gpr;                     // granules per row, d / 8
+    int H, Nk;
+    int dense;                   // 1: src is contiguous as well
+};
+constexpr int kVBatch = 8;
+constexpr int kVThreads = 256;
+constexpr int kVBlocksPerSm = 2;
+
+__device__ __forceinline__ long long v_src_index(const VConv &c, long long g)
+{
+    if (c.dense)
+        return g;
+    const long long row = g / c.gpr;
+    const long long col = g - row * c.gpr;
+    const long long bh = row / c.Nk;
+    const long long n = row - bh * c.Nk;
+    const long long b = bh / c.H;
+    return b * c.sb + (bh - b * c.H) * c.sh + n * c.sn + col;
+}
+
+__global__ void __launch_bounds__(kVThreads) v_to_f16_kernel(VConv c)
+{
+    grid_launch_dependents();
+    const long long stride = static_cast<long long>(gridDim.x) * kVThreads;
+    for (long long base = static_cast<long long>(blockIdx.x) * kVThreads + threadIdx.x;
+         base < c.granules; base += stride * kVBatch) {
+        uint4 w[kVBatch];
+#pragma unroll
+        for (int i = 0; i < kVBatch; ++i) {
+            const long long g = base + i * stride;
+            if (g < c.granules)
+                w[i] = __ldcs(c.src + v_src_index(c, g));
+        }
+#pragma unroll
+        for (int i = 0; i < kVBatch; ++i) {
+            const long long g = base + i * stride;
+            if (g < c.granules)
+                c.dst[g] = bf16x8_to_f16x8(w[i]);
+        }
+    }
+}
+
 template <int D, int kPrec>
 cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split, int num_sms,
                    cudaStream_t stream)
@@ -1726,12 +1790,41 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
         return e;
     const int grid = static_cast<int>(units < num_sms ? units : num_sms);
     p.grid = grid;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    if constexpr (kPrec == kPrecBf16V16) {
+        VConv c;
+        c.src = static_cast<const uint4 *>(a.v);
+        c.dst = static_cast<uint4 *>(a.v16);
+        c.gpr = D / 8;
+        c.granules = static_cast<long long>(p.BH) * a.Nk * c.gpr;
+        c.H = a.H;
+        c.Nk = a.Nk;
+        c.sb = a.v_sb / 8;
+        c.sh = a.v_sh / 8;
+        c.sn = a.v_sn / 8;
+        c.dense = a.v_sn == D && a.v_sh == static_cast<long long>(a.Nk) * D &&
+                  (a.B == 1 || a.v_sb == static_cast<long long>(a.H) * a.Nk * D);
+        const long long want = (c.granules + kVThreads - 1) / kVThreads;
+        const long long cap = static_cast<long long>(num_sms) * kVBlocksPerSm;
+        v_to_f16_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kVThreads, 0,
+                          stream>>>(c);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
+    cudaLaunchConfig_t fcfg = {};
+    fcfg.gridDim = dim3(static_cast<unsigned>(grid));
+    fcfg.blockDim = dim3(C::kThreads);
+    fcfg.dynamicSmemBytes = smem;
+    fcfg.stream = stream;
+    fcfg.attrs = pdl;
+    fcfg.numAttrs = kPrec == kPrecBf16V16 ? 1 : 0;
     if constexpr (D == 256)
-        fwd_single_kernel<D, kPrec><<<grid, C::kThreads, smem, stream>>>(maps.q, maps.k,
-                                                                          maps.v, p);
+        e = cudaLaunchKernelEx(&fcfg, fwd_single_kernel<D, kPrec>, maps.q, maps.k, maps.v, p);
     else
-        fwd_kernel<D, kPrec><<<grid, C::kThreads, smem, stream>>>(maps.q, maps.k, maps.v, p);
-    if ((e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
+        e = cudaLaunchKernelEx(&fcfg, fwd_kernel<D, kPrec>, maps.q, maps.k, maps.v, p);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess || p.splits == 1)
         return e;
     const long long rows = static_cast<long long>(p.BH) * p.Nq;
     const long long blocks = (rows + 3) / 4;
@@ -1744,10 +1837,7 @@ cudaError_t launch(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &split,
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
+    cfg.attrs = pdl;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, combine_kernel<D, kPrec>, static_cast<const float *>(p.ws_o),
                               static_cast<const float2 *>(p.ws_l), p);
@@ -1790,6 +1880,8 @@ cudaError_t launch_prec(const FwdArgs &a, const FwdMaps &maps, const FwdSplit &s
         return launch<D, kPrecF16>(a, maps, split, num_sms, stream);
     if (a.bf16p)
         return launch<D, kPrecBf16P>(a, maps, split, num_sms, stream);
+    if (a.v16)
+        return launch<D, kPrecBf16V16>(a, maps, split, num_sms, stream);
     return launch<D, kPrecBf16>(a, maps, split, num_sms, stream);
 }
 

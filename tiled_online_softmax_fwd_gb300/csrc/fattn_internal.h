@@ -24,6 +24,11 @@ struct FwdArgs {
                   // last N key positions under the causal mask
     // Element strides of o for (batch, head, row); all 0 = contiguous.
     long long o_sb = 0, o_sh = 0, o_sn = 0;
+    // bf16 with fp16 P only: non-null = V pre-pass.  The caller's V (v,
+    // element strides v_sb, v_sh, v_sn, each a multiple of 8) is rounded to
+    // fp16 into v16, contiguous [B][H][Nk][d], which FwdMaps::v then reads.
+    void *v16 = nullptr;
+    long long v_sb = 0, v_sh = 0, v_sn = 0;
 };
 
 // Tensor maps over Q, K, V.  The forward kernel takes 4-D maps (d, N or Nk,

@@ -27,7 +27,9 @@ EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_fp16", 
             "attn_fwd_split_count", "attn_fwd_split_noalloc", "attn_fwd_split_workspace_size",
             "fattn_status_string",
             "fattn_last_cuda_error", "fattn_get_device_status", "fattn_row_sum",
-            "fattn_selftest_wait_timeout", "fattn_softmax_rows", "fattn_version"]
+            "fattn_selftest_wait_timeout", "fattn_set_v_conversion", "fattn_softmax_rows",
+            "fattn_trim_scratch", "fattn_v_prepass_planned", "fattn_version"]
+V_CONVERT = {"auto": 0, "on_chip": 1, "prepass": 2}
 
 _lib = None
 _lock = threading.Lock()
@@ -103,6 +105,12 @@ def load():
             f.argtypes = [vp, vp, ip, ip, ip, vp]
         lib.fattn_version.restype = ctypes.c_char_p
         lib.fattn_version.argtypes = []
+        lib.fattn_set_v_conversion.restype = ctypes.c_int
+        lib.fattn_set_v_conversion.argtypes = [ip]
+        lib.fattn_trim_scratch.restype = ctypes.c_int
+        lib.fattn_trim_scratch.argtypes = []
+        lib.fattn_v_prepass_planned.restype = ctypes.c_int
+        lib.fattn_v_prepass_planned.argtypes = [ip, ip, ip]
         _lib = lib
         return lib
 
@@ -200,7 +208,8 @@ def attn_fwd_split(q, k, v, causal: bool = False, scale: float | None = None,
     (default: the library's choice for the device) and merged by a combine
     kernel.  ``workspace`` is a CUDA uint8 tensor of at least
     split_workspace_size(...) bytes; when omitted, one is allocated here with
-    torch (the library itself never allocates)."""
+    torch (the library itself takes only the V pre-pass scratch, see
+    set_v_conversion)."""
     _validate(q, k, v)
     B, H, N, d = q.shape
     if scale is None:
@@ -454,6 +463,44 @@ def row_sum(x, out=None, stream=None):
 
 def version() -> str:
     return load().fattn_version().decode()
+
+
+def set_v_conversion(mode: str) -> str:
+    """Where bf16 calls with fp16 P round V to fp16: "auto", "on_chip" or
+    "prepass" (fattn_set_v_conversion).  Returns the previous setting."""
+    if mode not in V_CONVERT:
+        raise ValueError("mode must be one of %s" % sorted(V_CONVERT))
+    prev = load().fattn_set_v_conversion(V_CONVERT[mode])
+    return {v: k for k, v in V_CONVERT.items()}[prev]
+
+
+def v_prepass_planned(N: int, d: int, causal: bool) -> bool:
+    """Whether a bf16 call with N queries per head, head dimension d and the
+    given mask takes the V pre-pass under the current setting
+    (fattn_v_prepass_planned)."""
+    r = load().fattn_v_prepass_planned(N, d, 1 if causal else 0)
+    if r < 0:
+        raise ValueError("unsupported N=%d, d=%d" % (N, d))
+    return r == 1
+
+
+class v_conversion:
+    """Context manager: set_v_conversion(mode) inside, the previous setting after."""
+
+    def __init__(self, mode: str):
+        self.mode = mode
+
+    def __enter__(self):
+        self.prev = set_v_conversion(self.mode)
+        return self
+
+    def __exit__(self, *exc):
+        set_v_conversion(self.prev)
+
+
+def trim_scratch():
+    """Give the V pre-pass pool's unused device memory back (fattn_trim_scratch)."""
+    _check(load().fattn_trim_scratch(), "fattn_trim_scratch")
 
 
 def raw_call(entry: str, *args) -> int:
