@@ -67,9 +67,9 @@ def measured_peak():
         return FALLBACK_PEAK_TFLOPS, "fallback 1.9 PFLOP/s bf16 (no MEASURED_PEAKS.json)"
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu summary of this kernel source
-    and workload (null when none matches the current source)."""
+def profiled_traffic(workload: str, key: str = "dram_bytes_per_launch"):
+    """DRAM bytes per launch (`key`) from a committed ncu summary of this
+    kernel source and workload (null when none matches the current source)."""
     want = kernel_source_hash()
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         groups = []  # a "workload" key starts a new group of bench-key fields
@@ -83,7 +83,7 @@ def profiled_traffic(workload: str):
         for fields in groups:
             if fields.get("workload") == workload and fields.get("kernel_source") == want:
                 try:
-                    return int(float(fields["dram_bytes_per_launch"])), os.path.basename(path)
+                    return int(float(fields[key])), os.path.basename(path)
                 except (KeyError, ValueError):
                     pass
     return None, None
@@ -681,6 +681,11 @@ def run_gpu(args, world, rank, local):
         "clocks": clocks.summary(),
         "device_status": status,
     }
+    if prepass:
+        # The V pre-pass's own DRAM traffic per call (the roofline's traffic
+        # is the forward kernel's).
+        line["roofline"]["traffic_v_prepass"] = profiled_traffic(
+            w.name, "v_prepass_dram_bytes_per_launch")[0]
     if step_ms is not None:
         # Per-step times (L2 flushed before each step, or inputs larger than
         # L2 back to back): quantiles of the step time and the achieved
