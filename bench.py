@@ -629,7 +629,8 @@ def run_gpu(args, world, rank, local):
     ms = max_over_ranks(world, kernel_ms)
     value = world * w.flops / (ms * 1e-3) / 1e12
     achieved = w.flops / (kernel_ms * 1e-3) / 1e12
-    prepass = int(not args.fp16 and fattn.v_prepass_planned(w.N, w.d, w.causal))
+    v_route = "none" if args.fp16 else fattn.v_conversion_route(w.N, w.d, w.causal)
+    prepass = int(v_route == "prepass")
 
     # End to end through the C ABI with host buffers (pinned), copies timed.
     e2e = None
@@ -670,7 +671,7 @@ def run_gpu(args, world, rank, local):
                      "traffic_source": traffic_src,
                      "algorithmic_flops_per_launch": w.flops,
                      "algorithmic_bytes_per_launch": w.io_bytes},
-        "v_prepass": prepass,
+        "v_conversion": v_route,
         "gpu_launches": args.steps * (1 + (splits > 1) + prepass),
         "kernel": "fattn %s<%d> (tcgen05/TMA, persistent)%s%s%s" % (
             "fwd_single_kernel" if w.d == 256 else "fwd_kernel", w.d,

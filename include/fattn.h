@@ -163,9 +163,9 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
  * and attn_fwd_split_noalloc always does.  Each call reads the setting once.
  * Returns the previous setting, or -1 (nothing changed) for an unknown mode.
  *
- * fattn_v_prepass_planned: 1 if a call with N queries per head, head
- * dimension d and mask `causal` would take the pre-pass under the current
- * setting (scratch permitting), 0 if it converts on chip, -1 for an
+ * fattn_v_conversion_route: where a call with N queries per head, head
+ * dimension d and mask `causal` rounds V under the current setting (scratch
+ * permitting): FATTN_V_CONVERT_ON_CHIP or FATTN_V_CONVERT_PREPASS; -1 for an
  * unsupported d, N < 0 or causal not 0 or 1.
  *
  * fattn_trim_scratch gives the pool's unused memory on every device back to
@@ -177,7 +177,7 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
 #define FATTN_V_CONVERT_ON_CHIP 1
 #define FATTN_V_CONVERT_PREPASS 2
 int fattn_set_v_conversion(int mode);
-int fattn_v_prepass_planned(int N, int d, int causal);
+int fattn_v_conversion_route(int N, int d, int causal);
 fattn_status_t fattn_trim_scratch(void);
 
 /*

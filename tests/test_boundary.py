@@ -234,8 +234,9 @@ def test_v_conversion_setting(lib):
     try:
         assert lib.fattn_set_v_conversion(3) == -1 and lib.fattn_set_v_conversion(-1) == -1
         assert lib.fattn_set_v_conversion(2) == 1  # the invalid calls changed nothing
-        assert lib.fattn_v_prepass_planned(128, 64, 0) == 1
-        assert lib.fattn_v_prepass_planned(0, 64, 0) == 0  # nothing to convert
+        ON_CHIP, PREPASS = 1, 2
+        assert lib.fattn_v_conversion_route(128, 64, 0) == PREPASS
+        assert lib.fattn_v_conversion_route(0, 64, 0) == ON_CHIP  # nothing to convert
         assert lib.fattn_set_v_conversion(0) == 2
         # Automatic: visits = units per head (halved under the causal mask)
         # against 24 / 8 / 16 / 12 for d = 64 / 96 / 128 / 256.
@@ -245,15 +246,15 @@ def test_v_conversion_setting(lib):
                  (96, 1): 30 * 128 + 1, (128, 0): 30 * 128 + 1, (128, 1): 62 * 128 + 1,
                  (256, 0): 11 * 128 + 1, (256, 1): 23 * 128 + 1}
         for (d, causal), n in first.items():
-            assert lib.fattn_v_prepass_planned(n, d, causal) == 1, (n, d, causal)
-            assert lib.fattn_v_prepass_planned(n - 1, d, causal) == 0, (n - 1, d, causal)
+            assert lib.fattn_v_conversion_route(n, d, causal) == PREPASS, (n, d, causal)
+            assert lib.fattn_v_conversion_route(n - 1, d, causal) == ON_CHIP, (n - 1, d, causal)
         for n, d, causal, want in [(16384, 128, 1, 1), (4096, 128, 1, 0), (256, 64, 0, 0),
                                    (4096, 64, 0, 0), (65536, 64, 0, 1), (4096, 96, 1, 1),
                                    (8192, 256, 1, 1)]:
-            assert lib.fattn_v_prepass_planned(n, d, causal) == want, (n, d, causal)
-        assert lib.fattn_v_prepass_planned(512, 80, 0) == -1
-        assert lib.fattn_v_prepass_planned(-1, 128, 0) == -1
-        assert lib.fattn_v_prepass_planned(512, 128, 2) == -1
+            assert lib.fattn_v_conversion_route(n, d, causal) == (PREPASS if want else ON_CHIP), (n, d)
+        assert lib.fattn_v_conversion_route(512, 80, 0) == -1
+        assert lib.fattn_v_conversion_route(-1, 128, 0) == -1
+        assert lib.fattn_v_conversion_route(512, 128, 2) == -1
         assert fattn.set_v_conversion("on_chip") == "auto"
         with pytest.raises(ValueError):
             fattn.set_v_conversion("gpu")

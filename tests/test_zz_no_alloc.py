@@ -80,7 +80,7 @@ def test_noalloc_single_split_is_attn_fwd(lib, B, H, N, d):
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     scale = fattn.default_scale(d)
     with fattn.v_conversion("auto"):
-        assert fattn.v_prepass_planned(N, d, True) == (d == 256)
+        assert (fattn.v_conversion_route(N, d, True) == "prepass") == (d == 256)
         ref_o, ref_l = fattn.attn_fwd(dq, dk, dv, causal=True, scale=scale)
         o, lse = _outputs(dq)
         assert _noalloc(lib, dq, dk, dv, o, lse, True, scale, 1) == OK

@@ -82,6 +82,8 @@ fattn_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 bool overlap(const void *a, size_t na, const void *b, size_t nb)
 {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -337,19 +339,24 @@ cudaMemPool_t g_pool[kMaxDevices] = {};
 // d = 96 from 8 (4: -3 % to +1 %, 8: +4.5 %); d = 128 from 16 (12: -1.5 %,
 // 16: +0.6 % causal and +3 % not, 32: +3 to +5 %); d = 256 from 12 (8: -1 %
 // to -6 %, 12: +13 %, 32: +36 %).
-bool want_prepass(int Nq, int d, int causal)
+enum class VRoute { kOnChip, kPrepass };
+
+VRoute v_route(int Nq, int d, int causal)
 {
     if (Nq <= 0)
-        return false;
+        return VRoute::kOnChip;
     const int mode = g_v_convert.load(std::memory_order_relaxed);
-    if (mode != FATTN_V_CONVERT_AUTO)
-        return mode == FATTN_V_CONVERT_PREPASS;
+    if (mode == FATTN_V_CONVERT_PREPASS)
+        return VRoute::kPrepass;
+    if (mode == FATTN_V_CONVERT_ON_CHIP)
+        return VRoute::kOnChip;
     const long long tiles = (static_cast<long long>(Nq) + 127) / 128;
     const long long units = d == 256 ? tiles : (tiles + 1) / 2;
     const long long visits2 = causal ? units : 2 * units;  // twice the visits
     const long long need2 = d == 64 ? 48 : d == 96 ? 16 : d == 128 ? 32 : 24;
-    return visits2 >= need2;
+    return visits2 >= need2 ? VRoute::kPrepass : VRoute::kOnChip;
 }
+
 
 // Scratch of `bytes` on `stream`, or nullptr where there is none to be had
 // (the stream is being captured into a graph, the pool cannot be created or
@@ -422,7 +429,7 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
             (s = make_map4(encode, &maps.k, k, Nk, d, H, B, lay.k, f16)) != FATTN_OK)
             return s;
         void *v16 = nullptr;
-        if (which == Kernel::kTcgen05 && may_allocate && want_prepass(N, d, causal))
+        if (which == Kernel::kTcgen05 && may_allocate && v_route(N, d, causal) == VRoute::kPrepass)
             v16 = prepass_scratch(info.dev, static_cast<size_t>(B) * H * Nk * d * 2, stream);
         if (v16 != nullptr) {
             const Layout dense = dense_layout(H, N, Nk, d);
@@ -465,7 +472,6 @@ fattn_status_t forward(Kernel which, const void *q, const void *k, const void *v
 constexpr int kMaxSplits = 64;
 constexpr size_t kWsAlign = 256;
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Scratch layout of a split call: fp32 partial O, then (256-byte aligned) the
 // base-2 partial lse pairs.
@@ -771,11 +777,12 @@ int fattn_set_v_conversion(int mode)
     return g_v_convert.exchange(mode);
 }
 
-int fattn_v_prepass_planned(int N, int d, int causal)
+int fattn_v_conversion_route(int N, int d, int causal)
 {
     if (N < 0 || (d != 64 && d != 96 && d != 128 && d != 256) || (causal != 0 && causal != 1))
         return -1;
-    return want_prepass(N, d, causal) ? 1 : 0;
+    return v_route(N, d, causal) == VRoute::kPrepass ? FATTN_V_CONVERT_PREPASS
+                                                     : FATTN_V_CONVERT_ON_CHIP;
 }
 
 fattn_status_t fattn_trim_scratch(void)

@@ -481,7 +481,9 @@ __device__ __forceinline__ void convert_tile(uint8_t *tile, int tid)
     }
 }
 
-// Converter warp cw (0 or 1).  Visits the V tiles in the producer's order:
+// Converter warp cw (0 or 1); its waits are warp-uniform (warp_wait), so a
+// timeout never splits the warp before the __syncwarp in convert.  Visits
+// the V tiles in the producer's order:
 // the two-tile kernel's ring holds K_j and V_j alternately over an even
 // number of stages, so V copies always land on the odd stages, whose
 // kv_full phases are all V copies; the one-tile kernel loads K_0, K_1, then
@@ -513,8 +515,7 @@ __device__ void run_convert(const Params &p, Bars &b, uint8_t *tiles, int cw)
             for (int i = 0; ok && i < u.n_max; ++i) {
                 const uint32_t at = pos + 2 * i + 1;
                 const uint32_t stage = at % C::kStages;
-                ok = mbar_wait(smem_addr(&b.kv_full[stage]), (at / C::kStages) & 1, kWaitLimitNs,
-                               abort);
+                ok = warp_wait(smem_addr(&b.kv_full[stage]), (at / C::kStages) & 1, abort);
                 if (ok)
                     convert(stage);
             }
@@ -526,8 +527,7 @@ __device__ void run_convert(const Params &p, Bars &b, uint8_t *tiles, int cw)
             pos += n > 1 ? 2 : 1;  // K_0 (and K_1)
             for (int i = 0; ok && i < n; ++i) {
                 const uint32_t stage = pos % C::kStages;
-                ok = mbar_wait(smem_addr(&b.v_full[stage]), (vbits >> stage) & 1u, kWaitLimitNs,
-                               abort);
+                ok = warp_wait(smem_addr(&b.v_full[stage]), (vbits >> stage) & 1u, abort);
                 vbits ^= 1u << stage;
                 if (ok)
                     convert(stage);

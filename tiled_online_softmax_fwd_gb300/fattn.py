@@ -28,7 +28,7 @@ EXPORTED = ["attn_bwd", "attn_bwd_workspace_size", "attn_fwd", "attn_fwd_fp16", 
             "fattn_status_string",
             "fattn_last_cuda_error", "fattn_get_device_status", "fattn_row_sum",
             "fattn_selftest_wait_timeout", "fattn_set_v_conversion", "fattn_softmax_rows",
-            "fattn_trim_scratch", "fattn_v_prepass_planned", "fattn_version"]
+            "fattn_trim_scratch", "fattn_v_conversion_route", "fattn_version"]
 V_CONVERT = {"auto": 0, "on_chip": 1, "prepass": 2}
 
 _lib = None
@@ -109,8 +109,8 @@ def load():
         lib.fattn_set_v_conversion.argtypes = [ip]
         lib.fattn_trim_scratch.restype = ctypes.c_int
         lib.fattn_trim_scratch.argtypes = []
-        lib.fattn_v_prepass_planned.restype = ctypes.c_int
-        lib.fattn_v_prepass_planned.argtypes = [ip, ip, ip]
+        lib.fattn_v_conversion_route.restype = ctypes.c_int
+        lib.fattn_v_conversion_route.argtypes = [ip, ip, ip]
         _lib = lib
         return lib
 
@@ -474,14 +474,14 @@ def set_v_conversion(mode: str) -> str:
     return {v: k for k, v in V_CONVERT.items()}[prev]
 
 
-def v_prepass_planned(N: int, d: int, causal: bool) -> bool:
-    """Whether a bf16 call with N queries per head, head dimension d and the
-    given mask takes the V pre-pass under the current setting
-    (fattn_v_prepass_planned)."""
-    r = load().fattn_v_prepass_planned(N, d, 1 if causal else 0)
+def v_conversion_route(N: int, d: int, causal: bool) -> str:
+    """Where a bf16 call with N queries per head, head dimension d and the
+    given mask rounds V under the current setting: "on_chip" or "prepass"
+    (fattn_v_conversion_route)."""
+    r = load().fattn_v_conversion_route(N, d, 1 if causal else 0)
     if r < 0:
         raise ValueError("unsupported N=%d, d=%d" % (N, d))
-    return r == 1
+    return {v: k for k, v in V_CONVERT.items()}[r]
 
 
 class v_conversion:
