@@ -118,7 +118,8 @@ fattn_status_t attn_fwd_fp16(const void *q, const void *k, const void *v, void *
  * Copies q_host, k_host, v_host to the caller's device buffers dq, dk, dv,
  * runs attn_fwd into do_ / dlse, and copies the results back to o_host and
  * lse_host; it returns once everything has completed.  The work is
- * pipelined over up to eight chunks of consecutive (b, h) heads: the copies
+ * pipelined over up to eleven chunks of consecutive (b, h) heads (short ones
+ * first and last, so that the parts nothing overlaps are short): the copies
  * in run on a library-owned helper stream, the kernels on `stream`, the
  * copies out on a second helper stream, ordered by events, so copies and
  * compute overlap.  The helper streams first wait for the work already

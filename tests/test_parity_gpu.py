@@ -216,11 +216,14 @@ def test_side_stream_and_preallocated_outputs():
 
 
 @pytest.mark.parametrize("B,H,N,d", [(1, 4, 1000, 128), (2, 5, 700, 64), (3, 1, 300, 128),
-                                     (1, 1, 129, 64), (2, 16, 256, 128)])
+                                     (1, 1, 129, 64), (2, 16, 256, 128), (1, 24, 4096, 64),
+                                     (1, 24, 38912, 64)])
 def test_host_entry_point_matches_device_path(B, H, N, d):
     """The pipelined host entry (copies and compute overlapped over chunks of
-    heads, uneven when B*H is not a multiple of the chunk count) gives the
-    device path's bits."""
+    heads, each chunk at least enough heads for one work unit per SM; on 152
+    SMs: one chunk for the small shapes, three equal chunks of 8 heads for
+    24 x 4096, and 1, 1, 4, 4, 3, 3, 3, 3, 1, 1 heads for 24 x 38912) gives
+    the device path's bits."""
     q, k, v = make_qkv(B, H, N, d, seed=31 + B * H)
     hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
     ho = torch.empty_like(hq).pin_memory()

@@ -8,6 +8,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -601,7 +602,38 @@ fattn_status_t noalloc_scratch(int dev, void **out)
 // attn_fwd_host's copy/compute pipeline: per-device helper streams and
 // events, created on first use and kept for the process.  Calls are
 // serialised by g_pipe_mutex (each call synchronises before it returns).
-constexpr int kHostChunks = 8;
+constexpr int kHostChunks = 16;
+
+// Head ranges [bounds[c], bounds[c+1]) of that pipeline.  Nothing overlaps
+// the first chunk's copy in, nor the last chunk's kernel and copy out, so the
+// ends are kept short: chunks of m/4 and m/2 heads first, equal chunks of
+// about m = ceil(BH/8) in the middle, m/2 and m/4 last.  No chunk has fewer
+// than min_heads heads, the heads that give every SM a work unit: a chunk's
+// kernel lasts at least as long as its heaviest unit, so smaller chunks would
+// only leave SMs idle.  Shapes too small for the ramps get equal chunks.
+// Returns the number of chunks (at most 11).
+int host_chunk_plan(long long BH, long long min_heads, long long bounds[kHostChunks + 1])
+{
+    const long long m = std::max((BH + 7) / 8, min_heads);
+    const long long q = std::max(m / 4, min_heads), h = std::max(m / 2, min_heads);
+    const long long rest = BH - 2 * (q + h);
+    int n = 0;
+    bounds[0] = 0;
+    if (rest < m) {
+        n = static_cast<int>(std::min<long long>((BH + m - 1) / m, 8));
+        for (int c = 1; c <= n; ++c)
+            bounds[c] = BH * c / n;
+        return n;
+    }
+    const long long k = rest / m;  // middle chunks, 1..7
+    for (long long sz : {q, h})
+        bounds[n + 1] = bounds[n] + sz, ++n;
+    for (long long i = 0; i < k; ++i)
+        bounds[n + 1] = bounds[n] + rest / k + (i < rest % k ? 1 : 0), ++n;
+    for (long long sz : {h, q})
+        bounds[n + 1] = bounds[n] + sz, ++n;
+    return n;
+}
 struct HostPipe {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
@@ -957,7 +989,10 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
     if ((s = host_pipe(dev, &hp)) != FATTN_OK)
         return s;
     const long long BH = static_cast<long long>(B) * H;
-    const int chunks = static_cast<int>(BH < kHostChunks ? BH : kHostChunks);
+    long long bounds[kHostChunks + 1];
+    const long long q_tiles = (static_cast<long long>(N) + 127) / 128;
+    const long long units = d == 256 ? q_tiles : (q_tiles + 1) / 2;  // work units per head
+    const int chunks = host_chunk_plan(BH, (info.num_sms + units - 1) / units, bounds);
     const size_t head_bytes = static_cast<size_t>(N) * d * 2, head_lse = static_cast<size_t>(N) * 4;
     auto at = [](const void *base, size_t off) {
         return static_cast<const uint8_t *>(base) + off;
@@ -969,7 +1004,7 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
     if (e == cudaSuccess)
         e = cudaStreamWaitEvent(hp->out, hp->start, 0);
     for (int c = 0; c < chunks && e == cudaSuccess && s == FATTN_OK; ++c) {
-        const long long h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+        const long long h0 = bounds[c], h1 = bounds[c + 1];
         const size_t off = static_cast<size_t>(h0) * head_bytes;
         const size_t bytes = static_cast<size_t>(h1 - h0) * head_bytes;
         if ((e = cudaMemcpyAsync(atw(dq, off), at(q_host, off), bytes, cudaMemcpyHostToDevice,
