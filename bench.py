@@ -183,11 +183,16 @@ def arm_config(w, world: int, in_digest: str, fp16: bool = False) -> dict:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_rows_for_steps(w, rows_all, steps):
-    """One seeded row per head for each step (cycling through the sample)."""
+REF_ROWS_PER_HEAD = 16
+
+
+def oracle_rows_for_steps(w, rows_all, steps, per_step=REF_ROWS_PER_HEAD):
+    """per_step seeded rows of every head for each step (cycling through the
+    sample), enough rows that every host thread has work."""
     per_head = rows_all.view(w.B * w.H, -1)
     cols = per_head.shape[1]
-    return [per_head[:, s % cols].clone() for s in range(steps)]
+    return [per_head[:, [(s * per_step + j) % cols for j in range(per_step)]].reshape(-1).clone()
+            for s in range(steps)]
 
 
 def rows_flops(w, rows) -> float:
@@ -250,7 +255,8 @@ def run_reference(args, world, rank):
         flops += rows_flops(w, plan[s])
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
-    sample = "each step: one seeded query row per head (%d rows, all their keys)" % (w.B * w.H)
+    sample = ("each step: %d seeded query rows per head (%d rows, all their keys)"
+              % (REF_ROWS_PER_HEAD, REF_ROWS_PER_HEAD * w.B * w.H))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",

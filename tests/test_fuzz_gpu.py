@@ -2,7 +2,8 @@
 entry point (attn_fwd_strided): head dims 64/96/128/256, bf16 and fp16,
 queries against equal or longer key sequences, causal or not, fixed or
 automatic splits, contiguous or packed strided layouts; each case against
-the fp64 oracle element by element."""
+the fp64 oracle element by element, and the bf16 cases once more on both
+places V can be rounded to fp16 (same bits)."""
 import os
 import random
 import zlib
@@ -79,6 +80,34 @@ def test_fuzz_matches_oracle(case):
     o_ref, lse_ref = oracle.attn_fwd_kv(q, k, v, fattn.default_scale(d), case["causal"])
     r = compare(o.float().cpu().reshape(-1, d), lse.cpu().reshape(-1), o_ref, lse_ref)
     assert_parity(r, case_id(case))
+
+
+BF16_CASES = [c for c in CASES if c["dtype"] == torch.bfloat16]
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=[case_id(c) for c in BF16_CASES])
+def test_fuzz_v_rounding_routes_agree(case):
+    """The same bf16 cases with V rounded on chip and by the pre-pass (which
+    also gathers the packed layout): the bits must agree."""
+    B, H, Nq, Nk, d = case["B"], case["H"], case["Nq"], case["Nk"], case["d"]
+    q, k, v = make_qkv_kv(B, H, Nq, Nk, d, seed=zlib.crc32(case_id(case).encode()) % 100000,
+                          sigma_qk=case["sigma"], dtype=case["dtype"])
+    if case["packed"]:
+        kv = torch.empty((B, Nk, 2, H, d), dtype=case["dtype"], device="cuda")
+        kv[:, :, 0] = k.permute(0, 2, 1, 3).cuda()
+        kv[:, :, 1] = v.permute(0, 2, 1, 3).cuda()
+        dk, dv = kv[:, :, 0].permute(0, 2, 1, 3), kv[:, :, 1].permute(0, 2, 1, 3)
+    else:
+        dk, dv = k.cuda(), v.cuda()
+    dq = q.cuda()
+    outs = []
+    for mode in ("on_chip", "prepass"):
+        with fattn.v_conversion(mode):
+            o, lse = fattn.attn_fwd_strided(dq, dk, dv, causal=case["causal"],
+                                            num_splits=case["splits"])
+            torch.cuda.synchronize()
+        outs.append((o, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 # ---------------------------------------------------------------- backward
