@@ -261,3 +261,9 @@ def test_v_conversion_setting(lib):
     finally:
         lib.fattn_set_v_conversion(prev)
 
+
+def test_trim_scratch_without_pools(lib):
+    """No call has taken pre-pass scratch in this process (no GPU here), so
+    there is no pool to trim: FATTN_OK without touching CUDA."""
+    assert lib.fattn_trim_scratch() == OK
+
