@@ -808,19 +808,29 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
     return alpha;
 }
 
-// O row (and with kOnes the l_round column) times alpha, in TMEM.
+// O row (and with kOnes the l_round column) times alpha, in TMEM.  The
+// rescale sits on the softmax's path to P V, and with wide logits a warp
+// needs one on a large share of its key tiles (some row's maximum rises past
+// the threshold), so the chunks' loads are issued together and waited for
+// once: up to 128 columns at a time (D = 256: two batches).
 template <int D, bool kOnes>
 __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
 {
+    constexpr int kChunksPerBatch = D <= 128 ? D / 32 : 4;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c * 32, o);
+    for (int c0 = 0; c0 < D / 32; c0 += kChunksPerBatch) {
+        uint32_t o[kChunksPerBatch][32];
+#pragma unroll
+        for (int c = 0; c < kChunksPerBatch; ++c)
+            tmem_ld32(t_o + (c0 + c) * 32, o[c]);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(t_o + c * 32, o);
+        for (int c = 0; c < kChunksPerBatch; ++c) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * alpha);
+            tmem_st32(t_o + (c0 + c) * 32, o[c]);
+        }
     }
     if constexpr (kOnes) {  // the l_round column and its 15 zero neighbours
         uint32_t o[16];
