@@ -137,9 +137,13 @@ fattn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void 
                              struct CUstream_st *stream);
 
 /*
- * V conversion.  For bf16 inputs with P in fp16 (attn_fwd, attn_fwd_split,
- * attn_fwd_kv, attn_fwd_strided with dtype 0, attn_fwd_host) every V element
- * is rounded to fp16 for the P V product, in one of two places:
+ * V conversion.  The pages cast P to a 16-bit type before the second product
+ * ("Triton hand-written kernels: vector add -> tiled GEMM -> FlashAttention
+ * core", section 4); this library takes fp16 for it with bf16 inputs (see
+ * attn_fwd), and both operands of a tensor-core product share one type, so
+ * for bf16 inputs with P in fp16 (attn_fwd, attn_fwd_split, attn_fwd_kv,
+ * attn_fwd_strided with dtype 0, attn_fwd_host) every V element is rounded
+ * to fp16 for the P V product, in one of two places:
  *   - on chip: converter warps of the forward kernel round each V tile in
  *     shared memory, once for every work unit that reads it; no memory is
  *     taken;
