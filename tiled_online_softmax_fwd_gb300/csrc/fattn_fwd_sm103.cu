@@ -123,10 +123,12 @@ struct Cfg {
     static constexpr bool kOnes = !kPF16 && D == 64;
     static constexpr uint32_t kOnesOffset = (kQTiles + kStages) * kTileBytes;
     static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
-    // Epilogue staging of the one-tile kernel: 4 KB (32 rows x 128 bytes) for
-    // each of its 4 softmax warps.
+    // Epilogue staging: 4 KB (32 rows x 128 bytes) for each softmax warp (4 in
+    // the one-tile kernel, 8 in the two-tile one; d = 96 stores directly).
+    static constexpr bool kStaged = D % 64 == 0;
     static constexpr uint32_t kStageOffset = kTilesBytes;
-    static constexpr uint32_t kBarsOffset = kStageOffset + (kQTiles == 1 ? 4 * 4096 : 0);
+    static constexpr uint32_t kBarsOffset =
+        kStageOffset + (kStaged ? (kQTiles == 1 ? 4 : 8) * 4096 : 0);
     static constexpr uint32_t kON = D + (kOnes ? 16 : 0);  // O accumulator columns
     // P V in two halves (keys 0-63 as soon as their P is written): faster at
     // d = 64, where the softmax dominates (1101 -> 1148 TFLOP/s on B2 H8
@@ -843,9 +845,9 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
     }
 }
 
-// Staged row stores (the one-tile kernel, where the epilogue holds up the
-// next unit: the tensor cores have no second Q tile to work on meanwhile).
-// Thread r of a warp (row r of the warp's 32) puts a 128-byte piece of its row
+// Staged row stores (both kernels, d a multiple of 64).  The epilogue runs on
+// the softmax warps between units, so with short units (a few key tiles per
+// Q tile) its store time is a large share of the launch.  Thread r of a warp (row r of the warp's 32) puts a 128-byte piece of its row
 // into row r of the warp's staging area, 16-byte granule g at position
 // g ^ (r % 8), so the 8 threads of a store phase hit 8 different bank groups;
 // then 8 lanes per row copy the pieces out as whole 128-byte lines, 4 rows per
@@ -922,23 +924,33 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
             char *dst0 = reinterpret_cast<char *>(
                 static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb + (u.bh % p.H) * p.o_sh +
                 static_cast<long long>(row0) * p.o_sn);
+            // One 64-column piece: its two 32-column chunks of O, loaded
+            // together (one wait) where the registers allow it, i.e. without
+            // converter warps in the kernel, else one chunk per wait.
+            constexpr int kLoads = Cfg<D, kPrec>::kConv ? 1 : 2;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
+            for (int c = 0; c < D / 32; c += kLoads) {
+                uint32_t o[kLoads][32];
                 __syncwarp();
-                tmem_ld32(t_o + c * 32, o);
-                tmem_wait_ld();
-                check(o);
-                auto f = [&](int i) { return __uint_as_float(o[i]) * inv_l; };
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    stage_put(stage, lane, (c % 2) * 4 + i,
-                              make_uint4(pack2<kOutF16>(f(8 * i), f(8 * i + 1)),
-                                         pack2<kOutF16>(f(8 * i + 2), f(8 * i + 3)),
-                                         pack2<kOutF16>(f(8 * i + 4), f(8 * i + 5)),
-                                         pack2<kOutF16>(f(8 * i + 6), f(8 * i + 7))));
-                if (c % 2 == 1)
-                    stage_flush(stage, lane, dst0 + (c / 2) * 128, p.o_sn * 2, live_rows);
+                for (int h = 0; h < kLoads; ++h)
+                    tmem_ld32(t_o + (c + h) * 32, o[h]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < kLoads; ++h) {
+                    check(o[h]);
+                    auto f = [&](int i) { return __uint_as_float(o[h][i]) * inv_l; };
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        stage_put(stage, lane, ((c + h) % 2) * 4 + i,
+                                  make_uint4(pack2<kOutF16>(f(8 * i), f(8 * i + 1)),
+                                             pack2<kOutF16>(f(8 * i + 2), f(8 * i + 3)),
+                                             pack2<kOutF16>(f(8 * i + 4), f(8 * i + 5)),
+                                             pack2<kOutF16>(f(8 * i + 6), f(8 * i + 7))));
+                }
+                if ((c + kLoads - 1) % 2 == 1)
+                    stage_flush(stage, lane, dst0 + ((c + kLoads - 1) / 2) * 128, p.o_sn * 2,
+                                live_rows);
             }
             if (live)
                 p.lse[grow] = (m + log2f(l)) * kLn2;
@@ -1104,7 +1116,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         if (!ok)
             break;
         tc_fence_after();
-        epilogue_row<D, kPrec, C::kOnes>(p, u, t_o, row, m, l, l_round);
+        epilogue_row<D, kPrec, C::kOnes, C::kStaged>(p, u, t_o, row, m, l, l_round);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
