@@ -124,8 +124,8 @@ struct Cfg {
     static constexpr uint32_t kOnesOffset = (kQTiles + kStages) * kTileBytes;
     static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
     // Epilogue staging: 4 KB (32 rows x 128 bytes) for each softmax warp (4 in
-    // the one-tile kernel, 8 in the two-tile one; d = 96 stores directly).
-    static constexpr bool kStaged = D % 64 == 0;
+    // the one-tile kernel, 8 in the two-tile one).
+    static constexpr bool kStaged = true;
     static constexpr uint32_t kStageOffset = kTilesBytes;
     static constexpr uint32_t kBarsOffset =
         kStageOffset + (kStaged ? (kQTiles == 1 ? 4 : 8) * 4096 : 0);
@@ -845,7 +845,7 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
     }
 }
 
-// Staged row stores (both kernels, d a multiple of 64).  The epilogue runs on
+// Staged row stores (both kernels, every d).  The epilogue runs on
 // the softmax warps between units, so with short units (a few key tiles per
 // Q tile) its store time is a large share of the launch.  Thread r of a warp (row r of the warp's 32) puts a 128-byte piece of its row
 // into row r of the warp's staging area, 16-byte granule g at position
@@ -855,6 +855,23 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
 __device__ __forceinline__ void stage_put(uint8_t *stage, int lane, int g, uint4 v)
 {
     reinterpret_cast<uint4 *>(stage + lane * 128)[g ^ (lane & 7)] = v;
+}
+
+// The first 64 bytes of each staged row (the last 32 columns of a d = 96
+// row): 4 lanes per row, 8 rows per instruction.
+__device__ __forceinline__ void stage_flush_half(const uint8_t *stage, int lane, char *dst0,
+                                                 long long row_bytes, int live_rows)
+{
+    __syncwarp();
+    const int g = lane % 4;
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {
+        const int rr = pass * 8 + lane / 4;
+        const uint4 x = reinterpret_cast<const uint4 *>(stage + rr * 128)[g ^ (rr & 7)];
+        if (rr < live_rows)
+            *reinterpret_cast<uint4 *>(dst0 + rr * row_bytes + g * 16) = x;
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ void stage_flush(const uint8_t *stage, int lane, char *dst0,
@@ -886,7 +903,8 @@ __device__ __forceinline__ void nonfinite_acc(const uint32_t (&o)[32], float (&a
 // and lse = ln2 * (m + log2 l); in split mode the fp32 partial O and the two
 // base-2 partial lse go to the workspace instead, for the combine kernel.  kStaged:
 // through the staging area (warp w, among the CTA's first warps, uses its
-// w-th 4 KB), for D a multiple of 64.
+// w-th 4 KB), in 128-byte pieces of the row (and a 64-byte last piece of a
+// d = 96 bf16 row).
 template <int D, int kPrec, bool kOnes, bool kStaged = false>
 __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uint32_t t_o, int row,
                                              float m, float l, float l_round)
@@ -912,7 +930,7 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
             nonfinite_acc(o, nf);
     };
     if constexpr (kStaged) {
-        static_assert(D % 64 == 0, "staged rows are whole 128-byte pieces");
+        static_assert(D % 32 == 0, "staged rows are 64- and 128-byte pieces");
         extern __shared__ __align__(1024) uint8_t smem_raw[];
         const uint32_t raw = smem_addr(smem_raw);
         uint8_t *stage = smem_raw + (((raw + 1023u) & ~1023u) - raw) +
@@ -927,7 +945,7 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
             // One 64-column piece: its two 32-column chunks of O, loaded
             // together (one wait) where the registers allow it, i.e. without
             // converter warps in the kernel, else one chunk per wait.
-            constexpr int kLoads = Cfg<D, kPrec>::kConv ? 1 : 2;
+            constexpr int kLoads = Cfg<D, kPrec>::kConv || D % 64 != 0 ? 1 : 2;
 #pragma unroll 1
             for (int c = 0; c < D / 32; c += kLoads) {
                 uint32_t o[kLoads][32];
@@ -951,6 +969,8 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
                 if ((c + kLoads - 1) % 2 == 1)
                     stage_flush(stage, lane, dst0 + ((c + kLoads - 1) / 2) * 128, p.o_sn * 2,
                                 live_rows);
+                else if (c + kLoads == D / 32)  // d = 96: the row's last 64 bytes
+                    stage_flush_half(stage, lane, dst0 + (c / 2) * 128, p.o_sn * 2, live_rows);
             }
             if (live)
                 p.lse[grow] = (m + log2f(l)) * kLn2;
