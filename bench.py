@@ -44,6 +44,7 @@ ALL_WORKLOADS = {**WORKLOADS, **VARIANT_WORKLOADS}
 DEFAULT_WORKLOAD = "B1_H32_N16384_d128_causal_sigma3"
 METRIC = "attention fwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 tensor peak"
 L2_BYTES = 126 * 1024 * 1024
+FLUSH_BYTES = 1 << 30
 FALLBACK_PEAK_TFLOPS = 1900.0
 KERNEL_SOURCES = ["tiled_online_softmax_fwd_gb300/csrc/fattn_fwd_sm103.cu",
                   "tiled_online_softmax_fwd_gb300/csrc/ptx_sm103.cuh"]
@@ -178,7 +179,7 @@ def arm_config(w, world: int, in_digest: str, fp16: bool = False) -> dict:
     return {"workload": w.name + ("_fp16" if fp16 else ""), **w.describe(),
             "parallelism": "replicas" if world > 1 else "single",
             "l2": ("inputs larger than L2 (%d MB)" % (w.io_bytes // 10**6)) if big
-                  else "L2 flushed (256 MiB write) before every step, outside the timed events",
+                  else "L2 flushed (1 GiB write) before every step, outside the timed events",
             "input_digest": in_digest}
 
 
@@ -571,7 +572,10 @@ def run_gpu(args, world, rank, local):
     dl = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     big = w.io_bytes > L2_BYTES
-    flush = None if big else torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    # The flush (a write far larger than L2) also keeps the GPU busy while the
+    # host enqueues the step, so that the step's events time the device work
+    # and not a host-side gap: 1 GiB takes ~0.17 ms to write.
+    flush = None if big else torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     # Key-range split when the library recommends it (few work units per SM;
     # bf16 only).
     splits = 1 if (args.split == "off" or args.fp16) else fattn.split_count(w.B, w.H, w.N, w.d,
