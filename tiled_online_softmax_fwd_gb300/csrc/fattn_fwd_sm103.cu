@@ -125,10 +125,8 @@ struct Cfg {
     static constexpr uint32_t kTilesBytes = kOnesOffset + (kOnes ? kChunkBytes : 0);
     // Epilogue staging: 4 KB (32 rows x 128 bytes) for each softmax warp (4 in
     // the one-tile kernel, 8 in the two-tile one).
-    static constexpr bool kStaged = true;
     static constexpr uint32_t kStageOffset = kTilesBytes;
-    static constexpr uint32_t kBarsOffset =
-        kStageOffset + (kStaged ? (kQTiles == 1 ? 4 : 8) * 4096 : 0);
+    static constexpr uint32_t kBarsOffset = kStageOffset + (kQTiles == 1 ? 4 : 8) * 4096;
     static constexpr uint32_t kON = D + (kOnes ? 16 : 0);  // O accumulator columns
     // P V in two halves (keys 0-63 as soon as their P is written): faster at
     // d = 64, where the softmax dominates (1101 -> 1148 TFLOP/s on B2 H8
@@ -889,26 +887,29 @@ __device__ __forceinline__ void stage_flush(const uint8_t *stage, int lane, char
     __syncwarp();
 }
 
-// The epilogue's check for non-finite output (kPrecBf16): adds o * 0 over a
-// chunk of the O row, four chains; the sum stays 0 while every value is
-// finite and becomes NaN at the first infinity or NaN.
-__device__ __forceinline__ void nonfinite_acc(const uint32_t (&o)[32], float (&acc)[4])
+// The epilogue's check for non-finite output (V rounded to fp16): sums a
+// chunk of the unnormalised O row into two packed accumulators.  Every
+// finite O element is below 2^8 * Nk * 65504 in magnitude (p <= 2^8 with the
+// rescale threshold, |v| < 65520), so a finite row sums to a finite value far
+// below FLT_MAX, and an infinity or NaN anywhere makes the sum non-finite.
+__device__ __forceinline__ void nonfinite_acc(const uint32_t (&o)[32], uint64_t (&acc)[2])
 {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        acc[i % 4] = fmaf(__uint_as_float(o[i]), 0.f, acc[i % 4]);
+    for (int i = 0; i < 16; ++i)
+        acc[i & 1] = f2_add(acc[i & 1], f2_pack(__uint_as_float(o[2 * i]),
+                                                __uint_as_float(o[2 * i + 1])));
 }
 
 // Epilogue of one row after the unit's last P V: O / l_round in bf16 (fp16)
 // and lse = ln2 * (m + log2 l); in split mode the fp32 partial O and the two
-// base-2 partial lse go to the workspace instead, for the combine kernel.  kStaged:
-// through the staging area (warp w, among the CTA's first warps, uses its
-// w-th 4 KB), in 128-byte pieces of the row (and a 64-byte last piece of a
-// d = 96 bf16 row).
-template <int D, int kPrec, bool kOnes, bool kStaged = false>
+// base-2 partial lse go to the workspace instead, for the combine kernel.  The
+// rows leave through the staging area (softmax warp w uses its w-th 4 KB) in
+// 128-byte pieces of the row (and a 64-byte last piece of a d = 96 bf16 row).
+template <int D, int kPrec, bool kOnes>
 __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uint32_t t_o, int row,
                                              float m, float l, float l_round)
 {
+    static_assert(D % 32 == 0, "staged rows are 64- and 128-byte pieces");
     // fp16 P is rounded 8x more finely than bf16 P: O is normalised by the
     // exact sum there.  With the ones column l_round is O column D.  l is 0
     // only for a split that saw no key of this row.
@@ -919,107 +920,70 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
     constexpr bool kOutF16 = Cfg<D, kPrec>::kInF16;
     const float l_norm = Cfg<D, kPrec>::kPF16 ? l : l_round;
     const float inv_l = l_norm > 0.f ? 1.f / l_norm : 0.f;
+    const uint64_t inv2 = f2_pack(inv_l, inv_l);
     const bool live = row < p.Nq;
     const size_t grow = static_cast<size_t>(u.bh) * p.Nq + row;
-    // With V converted to fp16 (kPrecBf16, kPrecBf16V16), a V element of magnitude 65520
-    // or more turns into an infinity: a non-finite output row (which
-    // non-finite inputs also give) records FATTN_ERR_RANGE.
-    float nf[4] = {0.f, 0.f, 0.f, 0.f};
+    // With V converted to fp16 (kPrecBf16, kPrecBf16V16), a V element of
+    // magnitude 65520 or more turns into an infinity: a non-finite output row
+    // (which non-finite inputs also give) records FATTN_ERR_RANGE.
+    uint64_t nf[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
     auto check = [&](const uint32_t (&o)[32]) {
         if constexpr (Cfg<D, kPrec>::kVRounded)
             nonfinite_acc(o, nf);
     };
-    if constexpr (kStaged) {
-        static_assert(D % 32 == 0, "staged rows are 64- and 128-byte pieces");
-        extern __shared__ __align__(1024) uint8_t smem_raw[];
-        const uint32_t raw = smem_addr(smem_raw);
-        uint8_t *stage = smem_raw + (((raw + 1023u) & ~1023u) - raw) +
-                         Cfg<D, kPrec>::kStageOffset + (threadIdx.x / 32) * 4096;
-        const int lane = threadIdx.x & 31;
-        const int row0 = row - lane;  // the warp's first row
-        const int live_rows = min(32, p.Nq - row0);
-        if (p.splits == 1) {  // 64 columns (128 bytes) a piece
-            char *dst0 = reinterpret_cast<char *>(
-                static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb + (u.bh % p.H) * p.o_sh +
-                static_cast<long long>(row0) * p.o_sn);
-            // One 64-column piece: its two 32-column chunks of O, loaded
-            // together (one wait) where the registers allow it, i.e. without
-            // converter warps in the kernel, else one chunk per wait.
-            constexpr int kLoads = Cfg<D, kPrec>::kConv || D % 64 != 0 ? 1 : 2;
+    // O times 1/l, two columns per packed multiply.
+    auto scaled = [&](const uint32_t (&o)[32], int i, float &a, float &b) {
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), inv2), a, b);
+    };
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *stage = smem_raw + (((raw + 1023u) & ~1023u) - raw) + Cfg<D, kPrec>::kStageOffset +
+                     (threadIdx.x / 32) * 4096;
+    const int lane = threadIdx.x & 31;
+    const int row0 = row - lane;  // the warp's first row
+    const int live_rows = min(32, p.Nq - row0);
+    if (p.splits == 1) {  // 64 columns (128 bytes) a piece
+        char *dst0 = reinterpret_cast<char *>(
+            static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb + (u.bh % p.H) * p.o_sh +
+            static_cast<long long>(row0) * p.o_sn);
+        // One 64-column piece: its two 32-column chunks of O, loaded together
+        // (one wait) where the registers allow it, i.e. without converter
+        // warps in the kernel, else one chunk per wait.
+        constexpr int kLoads = Cfg<D, kPrec>::kConv || D % 64 != 0 ? 1 : 2;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; c += kLoads) {
-                uint32_t o[kLoads][32];
-                __syncwarp();
-#pragma unroll
-                for (int h = 0; h < kLoads; ++h)
-                    tmem_ld32(t_o + (c + h) * 32, o[h]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int h = 0; h < kLoads; ++h) {
-                    check(o[h]);
-                    auto f = [&](int i) { return __uint_as_float(o[h][i]) * inv_l; };
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        stage_put(stage, lane, ((c + h) % 2) * 4 + i,
-                                  make_uint4(pack2<kOutF16>(f(8 * i), f(8 * i + 1)),
-                                             pack2<kOutF16>(f(8 * i + 2), f(8 * i + 3)),
-                                             pack2<kOutF16>(f(8 * i + 4), f(8 * i + 5)),
-                                             pack2<kOutF16>(f(8 * i + 6), f(8 * i + 7))));
-                }
-                if ((c + kLoads - 1) % 2 == 1)
-                    stage_flush(stage, lane, dst0 + ((c + kLoads - 1) / 2) * 128, p.o_sn * 2,
-                                live_rows);
-                else if (c + kLoads == D / 32)  // d = 96: the row's last 64 bytes
-                    stage_flush_half(stage, lane, dst0 + (c / 2) * 128, p.o_sn * 2, live_rows);
-            }
-            if (live)
-                p.lse[grow] = (m + log2f(l)) * kLn2;
-        } else {  // 32 fp32 columns (128 bytes) a piece
-            const size_t srow0 = static_cast<size_t>(u.split) * p.BH * p.Nq + grow - lane;
-            char *dst0 = reinterpret_cast<char *>(p.ws_o + srow0 * D);
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                __syncwarp();
-                tmem_ld32(t_o + c * 32, o);
-                tmem_wait_ld();
-                check(o);
-                auto f = [&](int i) { return __float_as_uint(__uint_as_float(o[i]) * inv_l); };
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    stage_put(stage, lane, i, make_uint4(f(4 * i), f(4 * i + 1), f(4 * i + 2), f(4 * i + 3)));
-                stage_flush(stage, lane, dst0 + c * 128, static_cast<long long>(D) * 4, live_rows);
-            }
-            if (live)
-                p.ws_l[srow0 + lane] = make_float2(m + log2f(l), m + log2f(l_norm));
-        }
-    } else if (p.splits == 1) {
-        uint16_t *orow = static_cast<uint16_t *>(p.o) + (u.bh / p.H) * p.o_sb +
-                         (u.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
+        for (int c = 0; c < D / 32; c += kLoads) {
+            uint32_t o[kLoads][32];
             __syncwarp();
-            tmem_ld32(t_o + c * 32, o);
+#pragma unroll
+            for (int h = 0; h < kLoads; ++h)
+                tmem_ld32(t_o + (c + h) * 32, o[h]);
             tmem_wait_ld();
-            check(o);
-            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                pk[i] = pack2<kOutF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                    __uint_as_float(o[2 * i + 1]) * inv_l);
-            if (live) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+            for (int h = 0; h < kLoads; ++h) {
+                check(o[h]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float a, b;
+                        scaled(o[h], 8 * i + 2 * k, a, b);
+                        w[k] = pack2<kOutF16>(a, b);
+                    }
+                    stage_put(stage, lane, ((c + h) % 2) * 4 + i, make_uint4(w[0], w[1], w[2], w[3]));
+                }
             }
+            if ((c + kLoads - 1) % 2 == 1)
+                stage_flush(stage, lane, dst0 + ((c + kLoads - 1) / 2) * 128, p.o_sn * 2,
+                            live_rows);
+            else if (c + kLoads == D / 32)  // d = 96: the row's last 64 bytes
+                stage_flush_half(stage, lane, dst0 + (c / 2) * 128, p.o_sn * 2, live_rows);
         }
         if (live)
             p.lse[grow] = (m + log2f(l)) * kLn2;
-    } else {
-        const size_t srow = static_cast<size_t>(u.split) * p.BH * p.Nq + grow;
-        float *orow = p.ws_o + srow * D;
+    } else {  // 32 fp32 columns (128 bytes) a piece
+        const size_t srow0 = static_cast<size_t>(u.split) * p.BH * p.Nq + grow - lane;
+        char *dst0 = reinterpret_cast<char *>(p.ws_o + srow0 * D);
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -1027,22 +991,25 @@ __device__ __forceinline__ void epilogue_row(const Params &p, const Unit &u, uin
             tmem_ld32(t_o + c * 32, o);
             tmem_wait_ld();
             check(o);
-            if (live) {
-                float4 *dst = reinterpret_cast<float4 *>(orow + c * 32);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l,
-                                         __uint_as_float(o[4 * i + 1]) * inv_l,
-                                         __uint_as_float(o[4 * i + 2]) * inv_l,
-                                         __uint_as_float(o[4 * i + 3]) * inv_l);
+            for (int i = 0; i < 8; ++i) {
+                float a, b, cc, dd;
+                scaled(o, 4 * i, a, b);
+                scaled(o, 4 * i + 2, cc, dd);
+                stage_put(stage, lane, i, make_uint4(__float_as_uint(a), __float_as_uint(b),
+                                                     __float_as_uint(cc), __float_as_uint(dd)));
             }
+            stage_flush(stage, lane, dst0 + c * 128, static_cast<long long>(D) * 4, live_rows);
         }
         if (live)
-            p.ws_l[srow] = make_float2(m + log2f(l), m + log2f(l_norm));
+            p.ws_l[srow0 + lane] = make_float2(m + log2f(l), m + log2f(l_norm));
     }
     if constexpr (Cfg<D, kPrec>::kVRounded) {
-        const float acc = (nf[0] + nf[1]) + (nf[2] + nf[3]);
-        if (live && acc != acc) {
+        float e0, e1, e2, e3;
+        f2_unpack(nf[0], e0, e1);
+        f2_unpack(nf[1], e2, e3);
+        const float acc = (e0 + e1) + (e2 + e3);
+        if (live && !(fabsf(acc) <= FLT_MAX)) {
             const uint32_t code = 5u /* FATTN_ERR_RANGE */ | (kRoleEpilogue << 8) |
                                   ((blockIdx.x & 0xffffu) << 16);
             atomicCAS(&g_fattn_status, 0u, code);
@@ -1136,7 +1103,7 @@ __device__ void run_softmax(const Params &p, Bars &b, uint32_t tmem, int t)
         if (!ok)
             break;
         tc_fence_after();
-        epilogue_row<D, kPrec, C::kOnes, C::kStaged>(p, u, t_o, row, m, l, l_round);
+        epilogue_row<D, kPrec, C::kOnes>(p, u, t_o, row, m, l, l_round);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
@@ -1506,7 +1473,7 @@ __device__ void run_softmax_single(const Params &p, Bars &b, uint32_t tmem)
         if (!ok)
             break;
         tc_fence_after();
-        epilogue_row<D, kPrec, C::kOnes, true>(p, u, t_o, row, m, l, l_round);
+        epilogue_row<D, kPrec, C::kOnes>(p, u, t_o, row, m, l, l_round);
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
