@@ -817,6 +817,14 @@ template <int D, bool kOnes>
 __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
 {
     constexpr int kChunksPerBatch = D <= 128 ? D / 32 : 4;
+    const uint64_t alpha2 = f2_pack(alpha, alpha);
+    // Two columns per packed multiply.
+    auto scale = [&](uint32_t &a, uint32_t &b) {
+        float x, y;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(a), __uint_as_float(b)), alpha2), x, y);
+        a = __float_as_uint(x);
+        b = __float_as_uint(y);
+    };
 #pragma unroll 1
     for (int c0 = 0; c0 < D / 32; c0 += kChunksPerBatch) {
         uint32_t o[kChunksPerBatch][32];
@@ -827,8 +835,8 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
 #pragma unroll
         for (int c = 0; c < kChunksPerBatch; ++c) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * alpha);
+            for (int i = 0; i < 32; i += 2)
+                scale(o[c][i], o[c][i + 1]);
             tmem_st32(t_o + (c0 + c) * 32, o[c]);
         }
     }
@@ -837,8 +845,8 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha)
         tmem_ld16(t_o + D, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        for (int i = 0; i < 16; i += 2)
+            scale(o[i], o[i + 1]);
         tmem_st16(t_o + D, o);
     }
 }
