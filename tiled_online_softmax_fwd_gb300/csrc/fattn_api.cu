@@ -207,18 +207,19 @@ size_t span_bytes(const long long st[3], int B, int H, int rows, int d)
 }
 
 // 4-D map (d, rows, H, B) of a 16-bit tensor with element strides st
-// (batch, head, row), box (64, 128, 1, 1), 128-byte swizzle, zero fill
-// outside the tensor.
+// (batch, head, row), box (64, box_rows, 1, 1), 128-byte swizzle, zero fill
+// outside the tensor.  box_rows is 128 (one tile's rows), or 64 for V at
+// d = 256, whose kernel copies each V tile as two halves of 64 keys.
 fattn_status_t make_map4(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *m,
                          const void *ptr, int rows, int d, int H, int B, const long long st[3],
-                         bool f16)
+                         bool f16, unsigned box_rows = 128)
 {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2,
                                    static_cast<cuuint64_t>(st[1]) * 2,
                                    static_cast<cuuint64_t>(st[0]) * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t box[4] = {64, box_rows, 1, 1};
     const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
     const CUresult r = encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                               4, const_cast<void *>(ptr), dims, strides, box, elem_strides,
@@ -430,6 +431,7 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
             (s = make_map4(encode, &maps.k, k, Nk, d, H, B, lay.k, f16)) != FATTN_OK)
             return s;
         void *v16 = nullptr;
+        const unsigned v_box_rows = d == 256 ? 64u : 128u;
         if (which == Kernel::kTcgen05 && may_allocate && v_route(N, d, causal) == VRoute::kPrepass)
             v16 = prepass_scratch(info.dev, static_cast<size_t>(B) * H * Nk * d * 2, stream);
         if (v16 != nullptr) {
@@ -438,9 +440,9 @@ fattn_status_t launch(Kernel which, const DeviceInfo &info, const void *q, const
             a.v_sb = lay.v[0];
             a.v_sh = lay.v[1];
             a.v_sn = lay.v[2];
-            s = make_map4(encode, &maps.v, v16, Nk, d, H, B, dense.v, true);
+            s = make_map4(encode, &maps.v, v16, Nk, d, H, B, dense.v, true, v_box_rows);
         } else {
-            s = make_map4(encode, &maps.v, v, Nk, d, H, B, lay.v, f16);
+            s = make_map4(encode, &maps.v, v, Nk, d, H, B, lay.v, f16, v_box_rows);
         }
         e = s == FATTN_OK ? fattn::launch_fwd_sm103(a, maps, split, info.num_sms, stream)
                           : cudaSuccess;

@@ -117,6 +117,13 @@ struct Cfg {
     // two 64 KB K/V stages.  Otherwise two Q tiles and a deeper ring.
     static constexpr int kQTiles = D == 256 ? 1 : 2;
     static constexpr int kStages = kChunks == 4 ? 2 : (kChunks == 2 ? 4 : 8);  // K/V ring
+    // The one-tile kernel fills and frees each 64 KB stage in two 32 KB
+    // halves with barriers of their own (K: d-columns 0-127 and 128-255, the
+    // S product's K-steps 0-7 and 8-15; V: keys 0-63 and 64-127, the P V
+    // product's K-steps 0-3 and 4-7), so the next copy into a half starts
+    // once the products reading that half are done, half a product earlier.
+    static constexpr int kHalves = kQTiles == 1 ? 2 : 1;
+    static constexpr uint32_t kHalfBytes = kTileBytes / kHalves;
     // Ones column: P V runs with N = D + 16 against V extended by a constant
     // atom whose first column is 1.0, so O column D accumulates l_round.
     // Needs 2 * (128 + D + 16) <= 512 TMEM columns; used for bf16 P, d = 64.
@@ -507,6 +514,17 @@ __device__ void run_convert(const Params &p, Bars &b, uint8_t *tiles, int cw)
         if (lane == 0)
             mbar_arrive(smem_addr(&b.v_ready[stage]));
     };
+    // One-tile kernel: half h of the V tile in this stage (slot 2 * stage + h).
+    auto convert_half = [&](uint32_t stage, int h) {
+        convert_linear<C::kHalfBytes / 16>(
+            reinterpret_cast<uint4 *>(tiles + (C::kQTiles + stage) * C::kTileBytes +
+                                      h * C::kHalfBytes),
+            tid);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&b.v_ready[2 * stage + h]));
+    };
     for (int r = 0; ok; ++r) {
         Unit u;
         if (!cta_unit(p, b, r, u))
@@ -527,10 +545,13 @@ __device__ void run_convert(const Params &p, Bars &b, uint8_t *tiles, int cw)
             pos += n > 1 ? 2 : 1;  // K_0 (and K_1)
             for (int i = 0; ok && i < n; ++i) {
                 const uint32_t stage = pos % C::kStages;
-                ok = warp_wait(smem_addr(&b.v_full[stage]), (vbits >> stage) & 1u, abort);
+                const uint32_t parity = (vbits >> stage) & 1u;
                 vbits ^= 1u << stage;
-                if (ok)
-                    convert(stage);
+                for (int h = 0; ok && h < 2; ++h) {
+                    ok = warp_wait(smem_addr(&b.v_full[2 * stage + h]), parity, abort);
+                    if (ok)
+                        convert_half(stage, h);
+                }
                 pos += i + 2 < n ? 2 : 1;  // V_i (and K_(i+2))
             }
         }
@@ -545,14 +566,14 @@ __device__ void run_convert(const Params &p, Bars &b, uint8_t *tiles, int cw)
 // 64-column box, or to the next 16 KB box.  The start address occupies the
 // low 14 bits of the descriptor's low word and never carries out of them
 // (shared memory is below 256 KB), so a step is one 32-bit add.
-template <int D, int kPrec>
+template <int D, int kPrec, int kK0 = 0, int kK1 = D / 16>
 __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem)
 {
     constexpr uint32_t idesc = idesc_f32acc(kBM, kBN, false, Cfg<D, kPrec>::kInF16);
     constexpr uint32_t hi = smem_desc_hi(1024);
     const uint32_t a_lo = smem_desc_lo(q_smem, 16), b_lo = smem_desc_lo(k_smem, 16);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
+    for (int kk = kK0; kk < kK1; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
         mma_ss_w(tmem_d, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
     }
@@ -565,20 +586,26 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32
 // tensor memory, 8 columns (16 keys of bf16 pairs) per K = 16 step.
 // With the ones column (Cfg::kOnes, d = 64) N = 80: the MMA's second atom
 // along N is the constant ones atom, so LBO is its distance from this stage.
+// In the one-tile kernel (Cfg::kHalves = 2) a V tile is two 32 KB halves of
+// 64 keys, each four 8 KB boxes of 64 columns: LBO is 8 KB, and K-step kk
+// reads half kk / 4.
 template <int D, int kPrec, int kK0 = 0, int kK1 = kBN / 16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_d, uint32_t tmem_p, uint32_t v_smem,
                                          uint32_t ones_smem, bool accumulate)
 {
     using C = Cfg<D, kPrec>;
+    constexpr bool kSplitV = C::kHalves == 2;
     constexpr uint32_t idesc = idesc_f32acc(kBM, C::kON, true, C::kPF16);
-    constexpr uint32_t kVLbo = D > 64 ? kChunkBytes : 1024;
+    constexpr uint32_t kVLbo = kSplitV ? kChunkBytes / 2 : (D > 64 ? kChunkBytes : 1024);
     constexpr uint32_t hi = smem_desc_hi(1024);
     const uint32_t b_lo = smem_desc_lo(v_smem, C::kOnes ? ones_smem - v_smem : kVLbo);
     const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
-    for (int kk = kK0; kk < kK1; ++kk)
-        mma_ts_w(tmem_d, tmem_p + kk * 8, b_lo + ((kk * 16 * 128) >> 4), hi, idesc,
-                 kk > 0 ? 1u : acc0);
+    for (int kk = kK0; kk < kK1; ++kk) {
+        const uint32_t off = kSplitV ? (kk / 4) * C::kHalfBytes + (kk % 4) * 16 * 128
+                                     : kk * 16 * 128;
+        mma_ts_w(tmem_d, tmem_p + kk * 8, b_lo + (off >> 4), hi, idesc, kk > 0 ? 1u : acc0);
+    }
 }
 
 template <int D, int kPrec>
@@ -1223,7 +1250,7 @@ __global__ void __launch_bounds__(Cfg<D, kPrec>::kThreads, 1)
 // written.  TMEM: S buffers at columns 0 and 128, O at 256..511.  Roles: warps
 // 0-3 softmax (thread r owns row r), warp 4 TMA, warp 5 MMA.  K/V ring of two
 // 64 KB stages, filled in the order the MMAs consume it: K0, K1, then V(i)
-// and K(i+2) alternately.
+// and K(i+2) alternately, each stage in two 32 KB halves (Cfg::kHalves).
 constexpr int kSingleWarpLoad = 4;
 constexpr int kSingleWarpMma = 5;
 constexpr int kSingleWarpConv = 6;  // and 7 (kPrecBf16)
@@ -1242,31 +1269,45 @@ __device__ void run_load_single(const Params &p, Bars &b, uint32_t smem_base,
     // K and V share the two stages irregularly (K_0, K_1, then V_i and
     // K_(i+2) alternately), so K copies complete on kv_full and V copies on
     // v_full: each barrier then sees only its own tiles, in order, and the
-    // next phase's parity is kept per stage and barrier.
+    // next phase's parity is kept per half-stage slot (2 * stage + half) and
+    // barrier.  A K half is two of the tile's 128-row boxes (d-columns
+    // 128h..128h+127); a V half is four 64-row boxes (keys 64h..64h+63, the
+    // V tensor map's box is 64 rows) stored 8 KB apart.
+    static_assert(C::kHalves == 2 && C::kChunks == 4, "one-tile kernel: d = 256");
     uint32_t kbits = 0, vbits = 0, last_v = 0, used = 0;
     grid_dependency_wait();  // see run_load
     auto load_tile = [&](const CUtensorMap *m, int row, int hh, int bb, bool is_v) {
         const uint32_t stage = pos % C::kStages;
-        ok = warp_wait(smem_addr(&b.kv_empty[stage]), ((pos / C::kStages) & 1) ^ 1, abort);
-        if (!ok)
-            return;
-        if (leader) {
-            const uint32_t full = smem_addr(is_v ? &b.v_full[stage] : &b.kv_full[stage]);
-            mbar_arrive_expect_tx(full, C::kTileBytes);
-            const uint32_t dst = smem_base + (C::kQTiles + stage) * C::kTileBytes;
+        const uint32_t dst = smem_base + (C::kQTiles + stage) * C::kTileBytes;
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t slot = 2 * stage + h;
+            ok = warp_wait(smem_addr(&b.kv_empty[slot]), ((pos / C::kStages) & 1) ^ 1, abort);
+            if (!ok)
+                return;
+            if (leader) {
+                const uint32_t full = smem_addr(is_v ? &b.v_full[slot] : &b.kv_full[slot]);
+                mbar_arrive_expect_tx(full, C::kHalfBytes);
+                if (is_v) {
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(dst + c * kChunkBytes, m, full, 64 * c, row, hh, bb);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(dst + h * C::kHalfBytes + c * (kChunkBytes / 2), m, full,
+                                    64 * c, row + 64 * h, hh, bb);
+                } else {
+#pragma unroll
+                    for (int c = 2 * h; c < 2 * h + 2; ++c)
+                        tma_load_4d(dst + c * kChunkBytes, m, full, 64 * c, row, hh, bb);
+                }
+            }
+            const uint32_t bit = 1u << slot;
+            if (is_v) {
+                vbits ^= bit;
+                last_v |= bit;
+            } else {
+                kbits ^= bit;
+                last_v &= ~bit;
+            }
+            used |= bit;
         }
-        const uint32_t bit = 1u << stage;
-        if (is_v) {
-            vbits ^= bit;
-            last_v |= bit;
-        } else {
-            kbits ^= bit;
-            last_v &= ~bit;
-        }
-        used |= bit;
         ++pos;
     };
     for (int r = 0; ok; ++r) {
@@ -1303,8 +1344,8 @@ __device__ void run_load_single(const Params &p, Bars &b, uint32_t smem_base,
         if (leader)
             record_failure(b, kRoleLoad);
         // Let the copies already issued land before the CTA exits: only the
-        // last copy into each stage can still be in flight.
-        for (int st = 0; st < C::kStages; ++st) {
+        // last copy into each half-stage slot can still be in flight.
+        for (int st = 0; st < 2 * C::kStages; ++st) {
             const uint32_t bit = 1u << st;
             if (!(used & bit))
                 continue;
@@ -1332,23 +1373,35 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
         if (leader)
             mma_commit(smem_addr(&bar));
     };
-    // Waits for the next ring position; returns its shared-memory address.
-    // K tiles complete on kv_full, V tiles on v_full, or with converter warps
-    // on v_ready once converted; each keeps one phase bit per stage.
+    // The next ring position: its stage and shared-memory address, and the
+    // parity of its fill.  Its two halves complete separately (see
+    // run_load_single): K halves on kv_full, V halves on v_full, or with
+    // converter warps on v_ready once converted; both halves of a stage
+    // share one phase bit per barrier kind.
     uint32_t kbits = 0, vbits = 0;
+    uint32_t fill_parity = 0;
+    bool fill_v = false;
     auto next_tile = [&](uint32_t &addr, bool is_v = false) {
         const uint32_t stage = pos % C::kStages;
         const uint32_t bit = 1u << stage;
+        fill_v = is_v;
         if (is_v) {
-            const uint32_t bar = smem_addr(C::kConv ? &b.v_ready[stage] : &b.v_full[stage]);
-            ok = warp_wait(bar, (vbits & bit) ? 1u : 0u, abort);
+            fill_parity = (vbits & bit) ? 1u : 0u;
             vbits ^= bit;
         } else {
-            ok = warp_wait(smem_addr(&b.kv_full[stage]), (kbits & bit) ? 1u : 0u, abort);
+            fill_parity = (kbits & bit) ? 1u : 0u;
             kbits ^= bit;
         }
         addr = smem_base + (C::kQTiles + stage) * C::kTileBytes;
         return stage;
+    };
+    // Waits for half h of the position next_tile returned last.
+    auto wait_half = [&](uint32_t stage, int h) {
+        const uint32_t slot = 2 * stage + h;
+        const uint32_t bar = smem_addr(!fill_v ? &b.kv_full[slot]
+                                               : (C::kConv ? &b.v_ready[slot] : &b.v_full[slot]));
+        ok = warp_wait(bar, fill_parity, abort);
+        return ok;
     };
     for (int r = 0; ok; ++r) {
         Unit u;
@@ -1361,17 +1414,31 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
         q_phase ^= 1;
         if (!ok)
             break;
+        // S over one K tile into S buffer buf, a half of the tile at a time:
+        // each half of the stage is freed once the products reading it are
+        // done.
+        auto s_product = [&](uint32_t buf, uint32_t k_addr, uint32_t stage) {
+            if (!wait_half(stage, 0))
+                return;
+            tc_fence_after();
+            if (leader)
+                issue_s<D, kPrec, 0, D / 32>(tmem + buf * 128u, smem_base, k_addr);
+            commit(b.kv_empty[2 * stage]);
+            if (!wait_half(stage, 1))
+                return;
+            tc_fence_after();
+            if (leader)
+                issue_s<D, kPrec, D / 32, D / 16>(tmem + buf * 128u, smem_base, k_addr);
+            commit(b.s_full[buf]);
+            commit(b.kv_empty[2 * stage + 1]);
+        };
         // S(0) and S(1) into the two buffers.
         for (int i = 0; i < 2 && i < n && ok; ++i) {
             uint32_t k_addr;
             const uint32_t stage = next_tile(k_addr);
+            s_product(i, k_addr, stage);
             if (!ok)
                 break;
-            tc_fence_after();
-            if (leader)
-                issue_s<D, kPrec>(tmem + i * 128u, smem_base, k_addr);
-            commit(b.s_full[i]);
-            commit(b.kv_empty[stage]);
             ++pos;
             if (i == n - 1)
                 commit(b.q_empty[0]);
@@ -1384,28 +1451,34 @@ __device__ void run_mma_single(const Params &p, Bars &b, uint32_t smem_base, uin
                 ok = warp_wait(smem_addr(&b.o_empty[0]), oe_phase ^ 1, abort);
                 oe_phase ^= 1;
             }
-            uint32_t v_addr = 0, stage = 0;
-            if (ok)
-                stage = next_tile(v_addr, true);
             if (!ok)
+                break;
+            uint32_t v_addr = 0;
+            const uint32_t stage = next_tile(v_addr, true);
+            // P V(i), keys 0-63 then 64-127, each half of V freed after its
+            // products.
+            if (!wait_half(stage, 0))
                 break;
             tc_fence_after();
             if (leader)
-                issue_pv<D, kPrec>(tmem + C::kColO0, tmem + buf * 128u, v_addr,
-                                  smem_base + C::kOnesOffset, i > 0);
+                issue_pv<D, kPrec, 0, kBN / 32>(tmem + C::kColO0, tmem + buf * 128u, v_addr,
+                                                smem_base + C::kOnesOffset, i > 0);
+            commit(b.kv_empty[2 * stage]);
+            if (!wait_half(stage, 1))
+                break;
+            tc_fence_after();
+            if (leader)
+                issue_pv<D, kPrec, kBN / 32, kBN / 16>(tmem + C::kColO0, tmem + buf * 128u,
+                                                      v_addr, smem_base + C::kOnesOffset, true);
             commit(b.pv_done);
-            commit(b.kv_empty[stage]);
+            commit(b.kv_empty[2 * stage + 1]);
             ++pos;
             if (i + 2 < n) {  // S(i+2) into the buffer P V(i) has just read
                 uint32_t k_addr;
                 const uint32_t ks = next_tile(k_addr);
+                s_product(buf, k_addr, ks);
                 if (!ok)
                     break;
-                tc_fence_after();
-                if (leader)
-                    issue_s<D, kPrec>(tmem + buf * 128u, smem_base, k_addr);
-                commit(b.s_full[buf]);
-                commit(b.kv_empty[ks]);
                 ++pos;
                 if (i + 2 == n - 1)
                     commit(b.q_empty[0]);
@@ -1513,7 +1586,7 @@ __global__ void __launch_bounds__(Cfg<D, kPrec>::kThreads, 1)
             mbar_init(smem_addr(&b.o_full[t]), 1);
             mbar_init(smem_addr(&b.o_empty[t]), 4);
         }
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < 2 * C::kStages; ++s) {  // two half-stage slots a stage
             mbar_init(smem_addr(&b.kv_full[s]), 1);
             mbar_init(smem_addr(&b.kv_empty[s]), 1);
             mbar_init(smem_addr(&b.v_ready[s]), 2);
