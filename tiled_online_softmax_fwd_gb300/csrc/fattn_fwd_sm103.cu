@@ -761,11 +761,14 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
                                               float &l, float &l_round, Pre pre = Pre(),
                                               Mid mid = Mid())
 {
-    // The whole S row: four 32-column loads in flight, one wait.
+    // The whole S row: four 32-column loads in flight, one wait.  The
+    // loads also reduce: each returns the maximum of its 32 columns, which
+    // is the row maximum's input wherever no key is masked.
     uint32_t sraw[kBN / 32][32];
+    float cmax[kBN / 32];
 #pragma unroll
     for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld32(t_s + c * 32, sraw[c]);
+        tmem_ld32_max(t_s + c * 32, sraw[c], cmax[c]);
     tmem_wait_ld();
     float s[kBN];
 #pragma unroll
@@ -774,9 +777,13 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
     // Mask (only on tiles that cross the diagonal and on the ragged last
     // tile; the branch is uniform across the warp): keys past row position +
     // off and keys past Nk get -inf, i.e. weight exactly 0.  first_vis is
-    // the last visible column of row 0 in this key tile.
+    // the last visible column of row 0 in this key tile.  The row max is
+    // then taken over the masked values: four independent chains of 3-input
+    // max over s[0..kBN).
     const bool diag = p.causal && first_vis < kBN - 1;
     const bool tail = (j + 1) * kBN > p.Nk;
+    static_assert(kBN == 128, "four 32-column loads a row");
+    float smax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
     if (diag || tail) {
         int limit = diag ? first_vis + r : kBN - 1;
         if (tail)
@@ -784,17 +791,15 @@ __device__ __forceinline__ float softmax_tile(const Params &p, uint32_t t_s, int
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
             s[i] = i > limit ? -INFINITY : s[i];
-    }
-    // Row max: four independent chains of 3-input max over s[0..kBN).
-    float mx[4] = {fmaxf(s[0], s[1]), fmaxf(s[2], s[3]), fmaxf(s[4], s[5]), fmaxf(s[6], s[7])};
-    static_assert(kBN % 8 == 0, "the row max takes eight columns per step");
+        float mx[4] = {fmaxf(s[0], s[1]), fmaxf(s[2], s[3]), fmaxf(s[4], s[5]), fmaxf(s[6], s[7])};
 #pragma unroll
-    for (int i = 8; i < kBN; i += 8) {
+        for (int i = 8; i < kBN; i += 8) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
+            for (int c = 0; c < 4; ++c)
+                mx[c] = fmax3(mx[c], s[i + 2 * c], s[i + 2 * c + 1]);
+        }
+        smax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
     }
-    const float smax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
     const float cand = smax * p.sl2;
     m_new = (first || cand > m + kRescaleLog2) ? fmaxf(m, cand) : m;
     const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 when m is kept
