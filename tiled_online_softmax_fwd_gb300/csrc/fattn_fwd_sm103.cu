@@ -138,7 +138,10 @@ struct Cfg {
     // P V in two halves (keys 0-63 as soon as their P is written): faster at
     // d = 64, where the softmax dominates (1101 -> 1148 TFLOP/s on B2 H8
     // N65536), slower at d = 128 (1441 -> 1389 on the headline workload).
-    static constexpr bool kHalfP = D == 64;
+    // At d = 96 it pays only with converter warps (B8 H16 N2048 d96 causal
+    // 782-789 -> 809-820, its register spills gone) and costs 0.3-0.8 %
+    // with V rounded beforehand.
+    static constexpr bool kHalfP = D == 64 || (D == 96 && kConv);
     static constexpr uint32_t kColO0 = 256;
     static constexpr uint32_t kColO1 = 256 + kON;
 };
