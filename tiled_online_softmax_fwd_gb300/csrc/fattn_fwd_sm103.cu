@@ -135,13 +135,17 @@ struct Cfg {
     static constexpr uint32_t kStageOffset = kTilesBytes;
     static constexpr uint32_t kBarsOffset = kStageOffset + (kQTiles == 1 ? 4 : 8) * 4096;
     static constexpr uint32_t kON = D + (kOnes ? 16 : 0);  // O accumulator columns
-    // P V in two halves (keys 0-63 as soon as their P is written): faster at
-    // d = 64, where the softmax dominates (1101 -> 1148 TFLOP/s on B2 H8
-    // N65536), slower at d = 128 (1441 -> 1389 on the headline workload).
-    // At d = 96 it pays only with converter warps (B8 H16 N2048 d96 causal
-    // 782-789 -> 809-820, its register spills gone) and costs 0.3-0.8 %
+    // P V in two halves (keys 0-63 as soon as their P is written), so only
+    // the second half's product lies between the last P and the next S:
+    // faster at d = 64, where the softmax dominates (1101 -> 1148 TFLOP/s on
+    // B2 H8 N65536), and at d = 128 since the row maximum comes from the
+    // reducing TMEM load (B4 H16 N4096 d128 causal 1277-1282 -> 1324-1334,
+    // B8 H16 N2048 d128 causal 1010-1017 -> 1047-1061, the headline level or
+    // up to 1 %; with the software max it had been slower there, 1441 ->
+    // 1389).  At d = 96 it pays only with converter warps (B8 H16 N2048 d96
+    // causal 782-789 -> 809-820, its register spills gone) and cost 0.3-0.8 %
     // with V rounded beforehand.
-    static constexpr bool kHalfP = D == 64 || (D == 96 && kConv);
+    static constexpr bool kHalfP = D == 64 || D == 128 || (D == 96 && kConv);
     static constexpr uint32_t kColO0 = 256;
     static constexpr uint32_t kColO1 = 256 + kON;
 };
